@@ -1,0 +1,594 @@
+// MXFP4 (W4A16) grouped GEMM over expert-sorted row bands, sm_103a.
+//
+// What it computes ("Running DeepSeek V4 Flash on TPU v6", section 1, the
+// grouped-matmul loop nest with the decode step): for every expert e with a
+// non-empty band of rows, out[r, n] = sum_k act[r, k] * w_e[n, k], where
+// w_e[n, k] = e2m1(code) * 2^(scale - 127) is decoded exactly to bf16 before
+// the matmul, bf16 products are exact in f32 and accumulate in f32.
+//
+// How (GB300 design, not the page's TPU design):
+//  * Swap-AB: the decoded weight tile (128 output columns n x K) is the MMA's
+//    A operand (M = 128) and the band's token rows are the B operand (MMA N =
+//    16..128, rounded up to 16).  Decode-sized bands (a few rows per expert) thus
+//    fill the 128-wide tensor-core dimension with weights, not with padding.
+//  * TMA streams the packed 4-bit codes (128 rows x 64 bytes per stage, 64-byte
+//    swizzle) and the activation rows (64-element boxes, 128-byte swizzle) into
+//    two shared-memory rings.
+//  * Two converter warpgroups (alternate K stages) decode codes x 2^k into bf16
+//    and write them straight into tensor memory with tcgen05.st; tcgen05.mma
+//    then reads A from tensor memory (no shared-memory round trip for the
+//    decoded weights, which would exceed the SM's shared-memory bandwidth at
+//    HBM rate).
+//  * One thread issues tcgen05.mma kind::f16 into one of two TMEM accumulators
+//    (128 columns each), so the epilogue of one work item overlaps the main
+//    loop of the next.
+//  * Four epilogue warps read the accumulator with tcgen05.ld (lane = output
+//    column n, column = token) and store rows of out with coalesced 128-byte
+//    writes, masking rows outside the band and columns >= N.
+//  * Persistent CTAs (one per SM) walk a static list of work items
+//    (expert, 128-token chunk, 128-column tile) built on the device from
+//    group_sizes; empty experts contribute no items and their weights are
+//    never read.
+//  * Every barrier wait is bounded; on timeout the kernel records
+//    MOE_ERR_TIMEOUT, drains its own copies and MMAs, frees TMEM and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <stdint.h>
+
+#include "device_common.cuh"
+#include "launch.h"
+#include "mxfp4_decode.cuh"
+
+namespace moe {
+namespace gemm {
+
+constexpr int kThreads = 512;                 // 16 warps
+constexpr int kBN = 128;                      // output columns per tile (MMA M)
+constexpr int kKS = 128;                      // K per pipeline stage
+constexpr int kMaxNT = 128;                   // tokens per work item (MMA N)
+constexpr int kCodeStages = 10;               // must be even (WG parity)
+constexpr int kActStages = 4;
+constexpr int kAStages = 4;                   // TMEM decoded-weight stages (even)
+constexpr int kCodeStageBytes = kBN * kKS / 2;            // 8 KB
+constexpr int kActHalfBytes = kMaxNT * 128;               // 64 bf16 per row
+constexpr int kActStageBytes = 2 * kActHalfBytes;         // 32 KB
+constexpr int kTmemCols = 512;
+constexpr int kAccCols = 128;
+constexpr int kACol0 = 2 * kAccCols;                      // A stages after the two accumulators
+constexpr int kAColsPerStage = kKS / 2;                   // bf16 pairs
+constexpr int kMaxE = 1024;
+
+constexpr int kOffCode = 0;
+constexpr int kOffAct = kOffCode + kCodeStages * kCodeStageBytes;
+constexpr int kOffLut = kOffAct + kActStages * kActStageBytes;
+constexpr int kOffRowOff = kOffLut + 256 * 16;
+constexpr int kOffItemOff = kOffRowOff + (kMaxE + 1) * 4;
+constexpr int kOffBars = (kOffItemOff + (kMaxE + 1) * 4 + 7) & ~7;
+constexpr int kNumBars = 2 * kCodeStages + 2 * kActStages + 2 * kAStages + 2 * 2 + 1;
+constexpr int kOffMisc = kOffBars + kNumBars * 8;
+constexpr int kSmemBytes = kOffMisc + 64 + 1024;          // + alignment slack
+
+static_assert(kCodeStages % 2 == 0 && kAStages % 2 == 0, "WG parity needs even ring sizes");
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kOffBars % 8 == 0, "barrier alignment");
+static_assert(kACol0 + kAStages * kAColsPerStage <= kTmemCols, "TMEM budget");
+
+struct Params {
+    const uint8_t *scales;
+    const int32_t *group_sizes;
+    void *out;
+    int *status;
+    int rows, K, N, E;
+    int out_bf16;
+    int n_tiles;       // ceil(N / 128)
+    int k_stages;      // ceil(K / 128)
+    int scale_row;     // K / 32
+    int scale_vec4;    // scale rows 4-byte aligned: load 4 scale bytes at once
+    uint64_t wait_limit_ns;
+};
+
+struct Item {
+    int e, row0, nvalid, nt, n0;
+};
+
+// Work item j -> (expert, token chunk, column tile); ioff/roff in shared memory.
+__device__ __forceinline__ Item decode_item(int j, const int *roff, const int *ioff, int E,
+                                            int n_tiles) {
+    int lo = 0, hi = E - 1;   // last e with ioff[e] <= j (its band is non-empty)
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (ioff[mid] <= j) lo = mid; else hi = mid - 1;
+    }
+    Item it;
+    it.e = lo;
+    const int r = j - ioff[lo];
+    const int chunk = r / n_tiles;
+    it.n0 = (r - chunk * n_tiles) * kBN;
+    const int t0 = chunk * kMaxNT;
+    const int rem = roff[lo + 1] - roff[lo] - t0;
+    it.nvalid = rem < kMaxNT ? rem : kMaxNT;
+    it.nt = (it.nvalid + 15) & ~15;
+    it.row0 = roff[lo] + t0;
+    return it;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
+                    const __grid_constant__ CUtensorMap tm_act, const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint4 *lut_tab = reinterpret_cast<uint4 *>(smem + kOffLut);
+    int *roff = reinterpret_cast<int *>(smem + kOffRowOff);
+    int *ioff = reinterpret_cast<int *>(smem + kOffItemOff);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBars);
+    uint64_t *code_full = bars;
+    uint64_t *code_empty = code_full + kCodeStages;
+    uint64_t *act_full = code_empty + kCodeStages;
+    uint64_t *act_empty = act_full + kActStages;
+    uint64_t *a_full = act_empty + kActStages;
+    uint64_t *a_empty = a_full + kAStages;
+    uint64_t *acc_full = a_empty + kAStages;
+    uint64_t *acc_empty = acc_full + 2;
+    uint64_t *final_bar = acc_empty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 8);
+    int *bad_flag = reinterpret_cast<int *>(smem + kOffMisc + 16);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int E = p.E;
+
+    // ---------------------------------------------------------------- prologue
+    if (tid < 256) {
+        const DecodeLut t = make_decode_lut(static_cast<uint32_t>(tid));
+        lut_tab[tid] = make_uint4(t.lo0, t.lo1, t.hi0, t.hi1);
+    }
+    if (tid == 0) {
+        *abort_flag = 0;
+        *bad_flag = 0;
+    }
+    __syncthreads();
+    // Row offsets and work-item offsets: exclusive prefix sums over experts,
+    // done by warp 0 in chunks of 32 (E <= 1024).
+    if (warp == 0) {
+        int run_rows = 0, run_items = 0;
+        for (int base = 0; base < E; base += 32) {
+            const int e = base + lane;
+            int gs = 0;
+            if (e < E) {
+                gs = p.group_sizes[e];
+                if (gs < 0) *bad_flag = 1;
+            }
+            const int g = gs > 0 ? gs : 0;
+            const int items = ((g + kMaxNT - 1) / kMaxNT) * p.n_tiles;
+            int incl_r = g, incl_i = items;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int a = __shfl_up_sync(0xffffffffu, incl_r, d);
+                const int b = __shfl_up_sync(0xffffffffu, incl_i, d);
+                if (lane >= d) {
+                    incl_r += a;
+                    incl_i += b;
+                }
+            }
+            if (e < E) {
+                roff[e] = run_rows + incl_r - g;
+                ioff[e] = run_items + incl_i - items;
+            }
+            run_rows += __shfl_sync(0xffffffffu, incl_r, 31);
+            run_items += __shfl_sync(0xffffffffu, incl_i, 31);
+        }
+        if (lane == 0) {
+            roff[E] = run_rows;
+            ioff[E] = run_items;
+            if (run_rows != p.rows) *bad_flag = 1;
+        }
+    }
+    __syncthreads();
+    if (*bad_flag) {
+        if (blockIdx.x == 0 && tid == 0) set_status(p.status, MOE_ERR_DATA);
+        return;
+    }
+    const int total_items = ioff[E];
+    if (static_cast<int>(blockIdx.x) >= total_items) return;
+    const int my_items = (total_items - static_cast<int>(blockIdx.x) + gridDim.x - 1) / gridDim.x;
+
+    if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+    if (tid == 0) {
+        for (int i = 0; i < kCodeStages; ++i) {
+            mbar_init(&code_full[i], 1);
+            mbar_init(&code_empty[i], 4);
+        }
+        for (int i = 0; i < kActStages; ++i) {
+            mbar_init(&act_full[i], 1);
+            mbar_init(&act_empty[i], 1);
+        }
+        for (int i = 0; i < kAStages; ++i) {
+            mbar_init(&a_full[i], 4);
+            mbar_init(&a_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_empty[i], 4);
+        }
+        mbar_init(final_bar, 1);
+        mbar_fence_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const uint32_t code_smem = smem_u32(smem + kOffCode);
+    const uint32_t act_smem = smem_u32(smem + kOffAct);
+    const int KT = p.k_stages;
+    const uint64_t lim = p.wait_limit_ns;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ code producer
+        if (lane == 0) {
+            tma_prefetch_map(&tm_codes);
+            uint32_t g = 0;
+            bool ok = true;
+            for (int i = 0; i < my_items && ok; ++i) {
+                const Item it = decode_item(blockIdx.x + i * gridDim.x, roff, ioff, E, p.n_tiles);
+                const int y = it.e * p.N + it.n0;
+                for (int ks = 0; ks < KT; ++ks, ++g) {
+                    const uint32_t slot = g % kCodeStages;
+                    if (!wait_bounded(&code_empty[slot], ((g / kCodeStages) & 1u) ^ 1u, abort_flag,
+                                      p.status, lim)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&code_full[slot], kCodeStageBytes);
+                    tma_load_2d(code_smem + slot * kCodeStageBytes, &tm_codes, ks * (kKS / 2), y,
+                                &code_full[slot]);
+                }
+            }
+            if (!ok) {   // drain: every issued copy must land before the CTA exits
+                const uint32_t first = g > kCodeStages ? g - kCodeStages : 0;
+                for (uint32_t h = first; h < g; ++h)
+                    wait_bounded(&code_full[h % kCodeStages], (h / kCodeStages) & 1u, nullptr,
+                                 p.status, lim);
+            }
+        }
+    } else if (warp == 2) {
+        // ---------------------------------------------------- activation producer
+        if (lane == 0) {
+            tma_prefetch_map(&tm_act);
+            uint32_t g = 0;
+            bool ok = true;
+            for (int i = 0; i < my_items && ok; ++i) {
+                const Item it = decode_item(blockIdx.x + i * gridDim.x, roff, ioff, E, p.n_tiles);
+                for (int ks = 0; ks < KT; ++ks, ++g) {
+                    const uint32_t slot = g % kActStages;
+                    if (!wait_bounded(&act_empty[slot], ((g / kActStages) & 1u) ^ 1u, abort_flag,
+                                      p.status, lim)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&act_full[slot], static_cast<uint32_t>(it.nt) * 256u);
+                    const uint32_t dst = act_smem + slot * kActStageBytes;
+                    for (int h = 0; h < 2; ++h)
+                        for (int grp = 0; grp < it.nt / 16; ++grp)
+                            tma_load_2d(dst + h * kActHalfBytes + grp * 2048, &tm_act,
+                                        ks * kKS + h * 64, it.row0 + grp * 16, &act_full[slot]);
+                }
+            }
+            if (!ok) {
+                const uint32_t first = g > kActStages ? g - kActStages : 0;
+                for (uint32_t h = first; h < g; ++h)
+                    wait_bounded(&act_full[h % kActStages], (h / kActStages) & 1u, nullptr,
+                                 p.status, lim);
+            }
+        }
+    } else if (warp == 1) {
+        // --------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            uint32_t g = 0;
+            bool ok = true;
+            for (int i = 0; i < my_items && ok; ++i) {
+                const Item it = decode_item(blockIdx.x + i * gridDim.x, roff, ioff, E, p.n_tiles);
+                const uint32_t accslot = i & 1;
+                if (!wait_bounded(&acc_empty[accslot], ((i >> 1) & 1) ^ 1, abort_flag, p.status,
+                                  lim)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t idesc = idesc_bf16_f32(128, it.nt);
+                const uint32_t d_tmem = tmem_base + accslot * kAccCols;
+                for (int ks = 0; ks < KT; ++ks, ++g) {
+                    const uint32_t aslot = g % kAStages;
+                    const uint32_t xslot = g % kActStages;
+                    if (!wait_bounded(&a_full[aslot], (g / kAStages) & 1u, abort_flag, p.status,
+                                      lim) ||
+                        !wait_bounded(&act_full[xslot], (g / kActStages) & 1u, abort_flag,
+                                      p.status, lim)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_col = tmem_base + kACol0 + aslot * kAColsPerStage;
+                    const uint32_t b_base = act_smem + xslot * kActStageBytes;
+#pragma unroll
+                    for (int kk = 0; kk < kKS / 16; ++kk) {
+                        const uint64_t bdesc =
+                            smem_desc_sw128(b_base + (kk >> 2) * kActHalfBytes + (kk & 3) * 32);
+                        mma_bf16_ts(d_tmem, a_col + kk * 8, bdesc, idesc, (ks | kk) != 0);
+                    }
+                    mma_commit(&a_empty[aslot]);
+                    mma_commit(&act_empty[xslot]);
+                }
+                if (ok) mma_commit(&acc_full[accslot]);
+            }
+            // All MMAs issued by this thread must finish before TMEM is freed.
+            mma_commit(final_bar);
+            wait_bounded(final_bar, 0, nullptr, p.status, lim);
+        }
+    } else if (warp >= 4 && warp < 12) {
+        // ----------------------------------------------------------- converters
+        const int wg = (warp - 4) >> 2;            // 0 or 1: even / odd stages
+        const int q = warp & 3;                    // TMEM lane quarter
+        const int row = q * 32 + lane;             // weight row (output column) in the tile
+        const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+        const bool k_aligned = p.scale_vec4 != 0;
+        uint32_t g = 0;
+        bool ok = true;
+        int bad_scale = 0;
+        for (int i = 0; i < my_items && ok; ++i) {
+            const Item it = decode_item(blockIdx.x + i * gridDim.x, roff, ioff, E, p.n_tiles);
+            const int n = it.n0 + row;
+            const uint8_t *srow =
+                p.scales + (static_cast<size_t>(it.e) * p.N + (n < p.N ? n : 0)) * p.scale_row;
+            for (int ks = 0; ks < KT; ++ks, ++g) {
+                if (static_cast<int>(g & 1u) != wg) continue;
+                // Scale bytes of this row's four 32-element blocks in the stage.
+                uint32_t sw = 0x7F7F7F7Fu;
+                if (n < p.N) {
+                    if (k_aligned) {
+                        sw = __ldg(reinterpret_cast<const uint32_t *>(srow + ks * 4));
+                    } else {
+                        sw = 0;
+                        for (int b = 0; b < 4; ++b) {
+                            const int blk = ks * 4 + b;
+                            const uint32_t v = blk < p.scale_row ? __ldg(srow + blk) : 127u;
+                            sw |= v << (8 * b);
+                        }
+                    }
+                }
+                const uint32_t cslot = g % kCodeStages;
+                if (!warp_wait_bounded(&code_full[cslot], (g / kCodeStages) & 1u, abort_flag,
+                                       p.status, lim)) {
+                    ok = false;
+                    break;
+                }
+                // This row's 64 code bytes (4 chunks of 16, 64-byte swizzle).
+                uint32_t cw[4][4];
+                const uint8_t *crow = smem + kOffCode + cslot * kCodeStageBytes + row * 64;
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(
+                        crow + ((ch ^ ((row >> 1) & 3)) << 4));
+                    cw[ch][0] = v.x;
+                    cw[ch][1] = v.y;
+                    cw[ch][2] = v.z;
+                    cw[ch][3] = v.w;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&code_empty[cslot]);
+                const uint32_t aslot = g % kAStages;
+                if (!warp_wait_bounded(&a_empty[aslot], ((g / kAStages) & 1u) ^ 1u, abort_flag,
+                                       p.status, lim)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a_addr = lane_base + kACol0 + aslot * kAColsPerStage;
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) {
+                    const uint32_t s = (sw >> (8 * ch)) & 0xFFu;
+                    const uint4 l = lut_tab[s];
+                    const DecodeLut lut = {l.x, l.y, l.z, l.w};
+                    uint32_t o[16];
+                    if (!decode32(cw[ch], s, lut, o)) bad_scale = 1;
+                    __syncwarp();
+                    tmem_st16(a_addr + ch * 16, o);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&a_full[aslot]);
+            }
+        }
+        if (bad_scale) set_status(p.status, MOE_ERR_DATA);
+    } else if (warp >= 12) {
+        // ------------------------------------------------------------- epilogue
+        const int q = warp & 3;
+        const int row = q * 32 + lane;
+        const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+        for (int i = 0; i < my_items; ++i) {
+            const Item it = decode_item(blockIdx.x + i * gridDim.x, roff, ioff, E, p.n_tiles);
+            const uint32_t accslot = i & 1;
+            if (!warp_wait_bounded(&acc_full[accslot], (i >> 1) & 1, abort_flag, p.status, lim))
+                break;
+            tc_fence_after();
+            const int n = it.n0 + row;
+            const bool col_ok = n < p.N;
+            for (int c = 0; c < it.nt / 16; ++c) {
+                uint32_t v[16];
+                __syncwarp();
+                tmem_ld16(lane_base + accslot * kAccCols + c * 16, v);
+                tmem_ld_wait();
+                if (col_ok) {
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) {
+                        const int tok = c * 16 + t;
+                        if (tok < it.nvalid) {
+                            const size_t off = static_cast<size_t>(it.row0 + tok) * p.N + n;
+                            if (p.out_bf16) {
+                                const float f = __uint_as_float(v[t]);
+                                reinterpret_cast<__nv_bfloat16 *>(p.out)[off] = __float2bfloat16_rn(f);
+                            } else {
+                                reinterpret_cast<float *>(p.out)[off] = __uint_as_float(v[t]);
+                            }
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[accslot]);
+        }
+    }
+
+    // ---------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// Debug view of the decode: one thread per (weight row n, 32-element block).
+__global__ void decode_expert_kernel(const uint8_t *codes, const uint8_t *scales, int N, int K,
+                                     int e, uint16_t *out, int *status) {
+    __shared__ uint4 lut_tab[256];
+    for (int s = threadIdx.x; s < 256; s += blockDim.x) {
+        const DecodeLut t = make_decode_lut(static_cast<uint32_t>(s));
+        lut_tab[s] = make_uint4(t.lo0, t.lo1, t.hi0, t.hi1);
+    }
+    __syncthreads();
+    const int nblk = K / 32;
+    const long long total = static_cast<long long>(N) * nblk;
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int n = static_cast<int>(i / nblk), b = static_cast<int>(i % nblk);
+        const size_t row = static_cast<size_t>(e) * N + n;
+        const uint8_t *src = codes + row * (K / 2) + b * 16;
+        uint32_t c[4];
+        for (int w = 0; w < 4; ++w)
+            c[w] = static_cast<uint32_t>(src[4 * w]) | (static_cast<uint32_t>(src[4 * w + 1]) << 8) |
+                   (static_cast<uint32_t>(src[4 * w + 2]) << 16) |
+                   (static_cast<uint32_t>(src[4 * w + 3]) << 24);
+        const uint32_t s = scales[row * nblk + b];
+        const uint4 l = lut_tab[s];
+        const DecodeLut lut = {l.x, l.y, l.z, l.w};
+        uint32_t o[16];
+        if (!decode32(c, s, lut, o)) set_status(status, MOE_ERR_DATA);
+        uint32_t *dst = reinterpret_cast<uint32_t *>(out + static_cast<size_t>(n) * K + b * 32);
+        for (int w = 0; w < 16; ++w) dst[w] = o[w];
+    }
+}
+
+// Failure-detection self-test: wait on a barrier that never completes.
+__global__ void bounded_wait_kernel(uint64_t limit_ns, int *status) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        mbar_fence_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) wait_bounded(&bar, 0, &abort_flag, status, limit_ns);
+}
+
+}  // namespace gemm
+
+// ----------------------------------------------------------------- host side
+
+static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+moe_status launch_grouped_gemm(const uint16_t *act, int rows, int K, const uint8_t *codes,
+                               const uint8_t *scales, const int32_t *group_sizes, int E, int N,
+                               void *out, int out_bf16, int *status, uint64_t wait_limit_ns,
+                               cudaStream_t stream, int num_sms) {
+    using namespace gemm;
+    if (rows == 0) return MOE_OK;
+    PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode_fn();
+    if (!encode) return MOE_ERR_CUDA;
+
+    CUtensorMap tm_codes, tm_act;
+    {
+        cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2),
+                              static_cast<cuuint64_t>(E) * static_cast<cuuint64_t>(N)};
+        cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
+        cuuint32_t box[2] = {64, 128};
+        cuuint32_t estr[2] = {1, 1};
+        if (encode(&tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(codes), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return MOE_ERR_CUDA;
+    }
+    {
+        cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+        cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+        cuuint32_t box[2] = {64, 16};
+        cuuint32_t estr[2] = {1, 1};
+        if (encode(&tm_act, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(act), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return MOE_ERR_CUDA;
+    }
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        attr_set = true;
+    }
+    Params p;
+    p.scales = scales;
+    p.group_sizes = group_sizes;
+    p.out = out;
+    p.status = status;
+    p.rows = rows;
+    p.K = K;
+    p.N = N;
+    p.E = E;
+    p.out_bf16 = out_bf16;
+    p.n_tiles = (N + kBN - 1) / kBN;
+    p.k_stages = (K + kKS - 1) / kKS;
+    p.scale_row = K / 32;
+    p.scale_vec4 = ((K / 32) % 4 == 0) && ((reinterpret_cast<uintptr_t>(scales) & 3) == 0);
+    p.wait_limit_ns = wait_limit_ns;
+    grouped_gemm_kernel<<<num_sms, kThreads, kSmemBytes, stream>>>(tm_codes, tm_act, p);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status launch_decode_expert(const uint8_t *codes, const uint8_t *scales, int N, int K, int e,
+                                uint16_t *out, int *status, cudaStream_t stream) {
+    const long long total = static_cast<long long>(N) * (K / 32);
+    int blocks = static_cast<int>((total + 255) / 256);
+    if (blocks > 4096) blocks = 4096;
+    if (blocks < 1) blocks = 1;
+    gemm::decode_expert_kernel<<<blocks, 256, 0, stream>>>(codes, scales, N, K, e, out, status);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status launch_bounded_wait(uint64_t limit_ns, int *status, cudaStream_t stream) {
+    gemm::bounded_wait_kernel<<<1, 32, 0, stream>>>(limit_ns, status);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace moe

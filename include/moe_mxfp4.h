@@ -1,0 +1,224 @@
+/*
+ * moe_mxfp4.h — C ABI of the GB300 (sm_103a) MXFP4 grouped MoE library.
+ *
+ * The library runs the routed-expert hot path of a DeepSeek-V4-Flash-style MoE
+ * layer: tokens routed top-k, sorted into one contiguous row band per expert,
+ * multiplied by that expert's MXFP4 weights (W4A16), gated by SwiGLU, multiplied
+ * again, and reduced back per token.  The operations follow:
+ *
+ *  [TPU]    "Running DeepSeek V4 Flash on TPU v6", section 1 "Four bits that v6e
+ *           can't hold": expert-sorted row bands, the grouped-matmul loop nest
+ *           (N tiles, (expert, M tile) pairs, K inner, f32 accumulator), the e2m1
+ *           decode (magnitudes 0, .5, 1, 1.5, 2, 3, 4, 6), per-32 block scales
+ *           applied before the matmul, bf16 activations, ragged groups with
+ *           empty ones, gate/up (w13) and w2 shapes.
+ *  [NVFP4]  "DeepSeek-V4-Flash-0731-NVFP4", "The lossless weight cast": E8M0
+ *           per-32 power-of-two scales, fused w1/w3, E2M1 -0 read as +0.
+ *  [Pocket] "DeepSeek-V4-Flash" (PocketLLM), "Implemented execution paths" and
+ *           "Correctness and precision": deterministic expert reduction with no
+ *           atomicAdd.
+ *
+ * Conventions for every call:
+ *  - Pointers named as device buffers must be device memory of the current
+ *    CUDA device; the caller owns all of them.  The library allocates nothing
+ *    and keeps no state between calls.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Every call only enqueues work on it and returns; results are ready when
+ *    the stream reaches that point.
+ *  - bf16 values travel as their raw 16-bit patterns (uint16_t); nothing is
+ *    converted on the host.
+ *  - Return value: argument errors found on the host (null pointer, bad size,
+ *    misalignment, unsupported device) and launch failures are returned
+ *    synchronously.  Errors that depend on device data (an expert id out of
+ *    range, group sizes that do not add up, a scale byte above 252, a pipeline
+ *    wait that gave up) are recorded in the status word of the caller's
+ *    workspace and read with moe_read_status().  The first error recorded wins.
+ *  - Only compute capability 10.3 (GB300, sm_103a) is supported.
+ */
+#ifndef MOE_MXFP4_H
+#define MOE_MXFP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1, /* bad pointer, size, alignment or dtype (host check) */
+    MOE_ERR_UNSUPPORTED = 2, /* device is not compute capability 10.3 */
+    MOE_ERR_CUDA = 3,        /* a CUDA runtime/driver call or launch failed */
+    MOE_ERR_DATA = 4,        /* device-side: id out of range, sum(group_sizes) != rows,
+                                negative group size, or scale byte > 252 */
+    MOE_ERR_TIMEOUT = 5      /* device-side: a pipeline wait exceeded its bound */
+} moe_status;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+
+/* Human-readable name of a status code (static string). */
+MOE_API const char *moe_status_string(moe_status status);
+
+/* Bytes of device workspace needed by moe_route_sort for T tokens, top-k and E
+ * experts; at least 256 (the status word lives in the first 4 bytes).  The GEMM
+ * and the combine only use the status word, so any workspace >= 256 bytes
+ * serves them. */
+MOE_API size_t moe_workspace_bytes(int32_t T, int32_t k, int32_t E);
+
+/* Clear the status word (async memset of the first 4 bytes of `workspace`).
+ * A fresh workspace must be cleared once before first use. */
+MOE_API moe_status moe_clear_status(void *workspace, void *stream);
+
+/* Synchronise `stream`, then return the status word recorded in `workspace`
+ * (MOE_OK if no device-side error was recorded).  Does not clear it. */
+MOE_API moe_status moe_read_status(const void *workspace, void *stream);
+
+/*
+ * moe_route_sort — expert-sorted row order for top-k routing ([TPU] section 1:
+ * the token rows are ordered by expert so that each expert owns one contiguous
+ * band of activation rows), by a stable counting sort.
+ *
+ *  topk_ids     device int32 [T, k]: expert of routing slot s = t*k + j.
+ *  T, k, E      tokens (>= 0), choices per token (1..E), experts (1..1024).
+ *  group_sizes  device int32 [E] out: rows per expert (0 allowed).
+ *  group_offsets device int32 [E+1] out: exclusive prefix sum; last = T*k.
+ *  sorted_slot  device int32 [T*k] out: row -> slot.  Within an expert the
+ *               slots appear in ascending s (stable).
+ *  slot_to_row  device int32 [T*k] out: slot -> row (inverse of sorted_slot).
+ *  x            device bf16 [T, hidden] or NULL: token activations.
+ *  hidden       row length of x (multiple of 8 when x is given).
+ *  x_sorted     device bf16 [T*k, hidden] out, or NULL: x_sorted[row] =
+ *               x[sorted_slot[row] / k] (the activation permutation).
+ *  workspace    device, >= moe_workspace_bytes(T, k, E) bytes, 16-byte aligned.
+ * Ids outside [0, E) set MOE_ERR_DATA; the outputs are then unspecified.
+ * Launches three kernels (count, scan, scatter+gather); no atomics on data.
+ */
+MOE_API moe_status moe_route_sort(const int32_t *topk_ids, int32_t T, int32_t k, int32_t E,
+                          int32_t *group_sizes, int32_t *group_offsets, int32_t *sorted_slot,
+                          int32_t *slot_to_row, const uint16_t *x, int32_t hidden,
+                          uint16_t *x_sorted, void *workspace, size_t workspace_bytes,
+                          void *stream);
+
+/*
+ * moe_mxfp4_grouped_gemm — W4A16 grouped matmul over expert row bands ([TPU]
+ * section 1: the grouped-matmul loop nest with the 4-bit decode step, and the
+ * block scale of every 32 weights applied to the decoded tile before the matmul).
+ *
+ *   out[r, n] = sum_k act[r, k] * e2m1(code[e, n, k]) * 2^(scale[e, n, k/32] - 127)
+ *
+ * for every row r of band e (bands laid out in expert order by group_sizes).
+ *
+ *  act          device bf16 [rows, K], 16-byte aligned; rows >= 0.
+ *  K            reduction length, multiple of 32 (one E8M0 scale per 32).
+ *  codes        device uint8 [E, N, K/2], 16-byte aligned: two e2m1 nibbles per
+ *               byte, element 2j in bits 0-3; nibble bit 3 = sign, bits 2-1 =
+ *               exponent, bit 0 = mantissa; code 0x8 reads as +0.
+ *  scales       device uint8 [E, N, K/32]: E8M0 bytes (127 = 1.0); 0..252
+ *               supported, 253..255 set MOE_ERR_DATA and produce NaN.
+ *  group_sizes  device int32 [E]: rows per expert, >= 0, summing to rows
+ *               (else MOE_ERR_DATA and no output is written).
+ *  E            1..1024 experts.  N >= 1 output columns.
+ *  out          device [rows, N], f32 (4-byte aligned) or bf16 (RNE).
+ *  workspace    device, >= 256 bytes (status word).
+ * Products of bf16 activations and the exactly decoded bf16 weights are exact
+ * in f32; results differ from an exact sum only by f32 accumulation order.
+ * Empty experts launch no work and their weights are never read.
+ */
+MOE_API moe_status moe_mxfp4_grouped_gemm(const uint16_t *act, int64_t rows, int32_t K,
+                                  const uint8_t *codes, const uint8_t *scales,
+                                  const int32_t *group_sizes, int32_t E, int32_t N, void *out,
+                                  moe_dtype out_dtype, void *workspace, size_t workspace_bytes,
+                                  void *stream);
+
+/*
+ * moe_swiglu — gate/up activation on the fused w13 output ([TPU] section 1,
+ * where the activation is timed apart from the grouped matmuls; [NVFP4]: w1
+ * and w3 fused into the first GEMM).
+ *
+ *   h[r, i] = silu(gu[r, i]) * gu[r, I + i],  silu(g) = g / (1 + e^-g),
+ * computed in f32 and rounded once to bf16 (nearest-even).
+ *
+ *  gu     device [rows, 2*I], f32 or bf16 (in_dtype), 16-byte aligned.
+ *  h      device bf16 [rows, I] out, 16-byte aligned.
+ */
+MOE_API moe_status moe_swiglu(const void *gu, moe_dtype in_dtype, int64_t rows, int32_t I, uint16_t *h,
+                      void *stream);
+
+/*
+ * moe_combine — deterministic top-k weighted unpermute ([Pocket]: expert
+ * reduction without atomicAdd).
+ *
+ *   out[t, n] = sum_{j = 0..k-1} topk_w[t, j] * y[slot_to_row[t*k + j], n]
+ *
+ * summed as an f32 fused-multiply-add chain in ascending j, so results are
+ * bitwise reproducible run to run.
+ *
+ *  y            device f32 [T*k, N], 16-byte aligned.
+ *  slot_to_row  device int32 [T*k] (from moe_route_sort).
+ *  topk_w       device f32 [T, k].
+ *  out          device [T, N], f32 or bf16.
+ */
+MOE_API moe_status moe_combine(const float *y, const int32_t *slot_to_row, const float *topk_w,
+                       int32_t T, int32_t k, int32_t N, void *out, moe_dtype out_dtype,
+                       void *stream);
+
+/*
+ * moe_layer_forward — the whole routed-expert path in one call:
+ * route_sort (with gather) -> w13 grouped GEMM -> SwiGLU -> w2 grouped GEMM ->
+ * combine, each stage as described above, all on `stream`.
+ *
+ *  x            device bf16 [T, hidden]; topk_ids int32 [T, k]; topk_w f32 [T, k].
+ *  w13_codes/scales  [E, 2*inter, hidden/2] / [E, 2*inter, hidden/32]
+ *               (output columns [0, inter) gate, [inter, 2*inter) up).
+ *  w2_codes/scales   [E, hidden, inter/2] / [E, hidden, inter/32].
+ *  out          device f32 [T, hidden].
+ *  Caller-owned intermediates (device): group_sizes int32 [E], group_offsets
+ *  int32 [E+1], sorted_slot / slot_to_row int32 [T*k], x_sorted bf16
+ *  [T*k, hidden], y13 f32 [T*k, 2*inter], h bf16 [T*k, inter], y2 f32
+ *  [T*k, hidden], workspace >= moe_workspace_bytes(T, k, E).
+ * hidden and inter must be multiples of 32.
+ */
+MOE_API moe_status moe_layer_forward(const uint16_t *x, const int32_t *topk_ids, const float *topk_w,
+                             int32_t T, int32_t k, int32_t E, int32_t hidden, int32_t inter,
+                             const uint8_t *w13_codes, const uint8_t *w13_scales,
+                             const uint8_t *w2_codes, const uint8_t *w2_scales, float *out,
+                             int32_t *group_sizes, int32_t *group_offsets, int32_t *sorted_slot,
+                             int32_t *slot_to_row, uint16_t *x_sorted, float *y13, uint16_t *h,
+                             float *y2, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * moe_mxfp4_decode_expert — debug view of the GEMM's weight decode: writes
+ * expert e's weights e2m1(code) * 2^(scale - 127) as bf16 [N, K], produced by
+ * the same device routine the GEMM's converter warps run.  Used to check the
+ * decode bit for bit.  Same code/scale layout and status rules as the GEMM.
+ */
+MOE_API moe_status moe_mxfp4_decode_expert(const uint8_t *codes, const uint8_t *scales, int32_t E,
+                                   int32_t N, int32_t K, int32_t e, uint16_t *out,
+                                   void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * moe_debug_bounded_wait — failure-detection self-test.  Launches one block
+ * that waits on a shared-memory barrier nothing will ever complete, using the
+ * same bounded wait as the GEMM pipeline with a limit of `limit_ns`
+ * nanoseconds (1e3..5e9).  The wait gives up, records MOE_ERR_TIMEOUT in the
+ * status word and the kernel returns; the CUDA context stays usable.
+ */
+MOE_API moe_status moe_debug_bounded_wait(uint64_t limit_ns, void *workspace, size_t workspace_bytes,
+                                  void *stream);
+
+/* Number of kernel launches the last successful call on this host thread
+ * enqueued (for launch accounting in benchmarks). */
+MOE_API int32_t moe_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_MXFP4_H */

@@ -151,8 +151,7 @@ int oracle_decode_expert_bf16(const uint8_t *codes, const uint8_t *scales, long 
 /* --------------------------------------------------------------- route sort */
 
 /* Stable counting sort of the T*k routing slots by expert ([TPU] section 1:
- * "Tokens are sorted by expert, so the activations form one band of rows per
- * expert").  Outputs: group_sizes[E], group_offsets[E+1], sorted_slot[rows]
+ * rows are ordered by expert so each expert owns one contiguous band).  Outputs: group_sizes[E], group_offsets[E+1], sorted_slot[rows]
  * (row -> slot), slot_to_row[rows].  Returns -1 on an out-of-range id. */
 int oracle_route_sort(const int32_t *ids, long T, long k, long E, int32_t *group_sizes,
                       int32_t *group_offsets, int32_t *sorted_slot, int32_t *slot_to_row) {

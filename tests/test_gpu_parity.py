@@ -1,0 +1,345 @@
+"""GPU parity: every kernel, called through the C ABI, against the CPU oracle on
+the same seeded inputs.
+
+Bars: route sort, gather and decoded weights bit-exact; GEMM f32 outputs within
+|gpu - oracle| <= 1e-5 * sum_k |a_k w_k| + 1e-6 per element (bf16 outputs: one
+bf16 ulp more); SwiGLU within 1 bf16 ulp of the oracle fed the GPU's input;
+combine within 1e-6 * sum_j |w_j y_j| + 1e-6; every kernel bitwise repeatable.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp4_weight_grouped_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def B():
+    import __graft_entry__ as g
+    g.build()
+    from fp4_weight_grouped_gb300 import binding
+    binding.load()
+    return binding
+
+
+def _tol_check(gpu, ref, mag, rel=1e-5, abs_=1e-6, extra=None, what=""):
+    gpu = np.asarray(gpu, np.float64)
+    bound = rel * mag + abs_
+    if extra is not None:
+        bound = bound + extra
+    diff = np.abs(gpu - ref)
+    bad = ~(diff <= bound)
+    assert not bad.any(), (f"{what}: {int(bad.sum())} of {diff.size} outside tolerance; "
+                           f"worst ratio {float(np.max(diff / bound)):.3g}")
+    return float(np.max(diff / bound)) if diff.size else 0.0
+
+
+def _bf16_ulp(x):
+    a = np.abs(np.asarray(x, np.float64))
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -133)))
+    return np.ldexp(1.0, (np.maximum(e, -126) - 7).astype(np.int64))
+
+
+def _gemm_gpu(B, act, codes, scales, gs, out_dtype=torch.float32):
+    ws = B.make_workspace(0, 1, 1, DEV)
+    out = B.grouped_gemm(B.bf16_from_bits(act, DEV), B.to_device(codes, DEV), B.to_device(scales, DEV),
+                         B.to_device(np.asarray(gs, np.int32), DEV), out_dtype=out_dtype, workspace=ws)
+    st = B.read_status(ws)
+    assert st == B.MOE_OK, B.status_string(st)
+    if out_dtype == torch.bfloat16:
+        return B.bits_from_bf16(out)
+    return out.cpu().numpy()
+
+
+# ------------------------------------------------------------------ route sort
+
+ROUTE_CASES = [
+    ("tiny", lambda: (inputs.gemm_case("tiny")["ids"], 8)),
+    ("decode_w13", lambda: (inputs.route_uniform(0, 64, 256, 6), 256)),
+    ("decode_w2", lambda: (inputs.route_uniform(0, 256, 256, 6), 256)),
+    ("prefill_zipf", lambda: (inputs.route_zipf(0, 4096, 256, 6), 256)),
+    ("layer", lambda: (inputs.route_logits(0, 8192, 256, 6)[0], 256)),
+    ("one_expert", lambda: (np.zeros((37, 1), np.int32), 1)),
+    ("dup_and_wide", lambda: (np.random.default_rng(5).integers(0, 1024, (3001, 3)).astype(np.int32), 1024)),
+    ("empty", lambda: (np.zeros((0, 6), np.int32), 16)),
+]
+
+
+@pytest.mark.parametrize("name,make", ROUTE_CASES, ids=[c[0] for c in ROUTE_CASES])
+def test_route_sort_bit_exact(B, name, make):
+    ids, E = make()
+    T, k = ids.shape
+    hidden = 64
+    x = inputs.normal_bf16(1, 99, (T, hidden))
+    ws = B.make_workspace(T, k, E, DEV)
+    gs, off, ss, s2r, xs = B.route_sort(B.to_device(ids, DEV), E, B.bf16_from_bits(x, DEV), ws)
+    assert B.read_status(ws) == B.MOE_OK
+    o_gs, o_off, o_ss, o_s2r = oracle.route_sort(ids, E)
+    np.testing.assert_array_equal(gs.cpu().numpy(), o_gs)
+    np.testing.assert_array_equal(off.cpu().numpy(), o_off)
+    np.testing.assert_array_equal(ss.cpu().numpy(), o_ss)
+    np.testing.assert_array_equal(s2r.cpu().numpy(), o_s2r)
+    np.testing.assert_array_equal(B.bits_from_bf16(xs), oracle.gather(x, o_ss, k))
+
+
+def test_route_sort_repeatable_and_flags_bad_ids(B):
+    ids = inputs.route_logits(3, 2048, 256, 6)[0]
+    dids = B.to_device(ids, DEV)
+    a = [t.clone() for t in B.route_sort(dids, 256)[:4]]
+    b = B.route_sort(dids, 256)[:4]
+    for u, v in zip(a, b):
+        assert torch.equal(u, v)
+    bad = ids.copy()
+    bad[100, 3] = 256
+    ws = B.make_workspace(*bad.shape, 256, DEV)
+    B.route_sort(B.to_device(bad, DEV), 256, workspace=ws)
+    assert B.read_status(ws) == B.MOE_ERR_DATA
+
+
+# -------------------------------------------------------------- weight decode
+
+def test_decode_bit_exact_all_codes_and_scale_edges(B):
+    rng = np.random.default_rng(7)
+    E, N, K = 2, 256, 512
+    codes = rng.integers(0, 256, (E, N, K // 2), dtype=np.uint8)
+    codes[1, :, :128] = np.arange(256, dtype=np.uint8)[None, :128].repeat(N, 0)
+    codes[1, :, 128:] = np.arange(128, 256, dtype=np.uint8)[None, :].repeat(N, 0)
+    scales = rng.integers(0, 253, (E, N, K // 32), dtype=np.uint8)
+    scales[1, :8, :] = np.array([0, 1, 2, 3, 126, 127, 251, 252], np.uint8)[:, None]
+    for e in range(E):
+        got = B.bits_from_bf16(B.decode_expert(B.to_device(codes, DEV), B.to_device(scales, DEV), e))
+        np.testing.assert_array_equal(got, oracle.decode_expert_bf16(codes, scales, e))
+
+
+def test_decode_flags_out_of_range_scale(B):
+    codes = np.full((1, 16, 32), 0x22, np.uint8)
+    scales = np.full((1, 16, 2), 127, np.uint8)
+    scales[0, 3, 1] = 253
+    ws = B.make_workspace(0, 1, 1, DEV)
+    out = B.decode_expert(B.to_device(codes, DEV), B.to_device(scales, DEV), 0, workspace=ws)
+    assert B.read_status(ws) == B.MOE_ERR_DATA
+    assert torch.isnan(out[3, 32:].float()).all() and not torch.isnan(out[3, :32].float()).any()
+
+
+def test_gemm_identity_activations_expose_decoded_weights(B):
+    # act = I_K: out[k, n] = w[n, k] exactly, so the converter's decode is checked bit for bit.
+    rng = np.random.default_rng(8)
+    K, N = 256, 384
+    codes = rng.integers(0, 256, (1, N, K // 2), dtype=np.uint8)
+    scales = rng.integers(0, 253, (1, N, K // 32), dtype=np.uint8)
+    scales[0, :, 0] = 0
+    scales[0, :, 1] = 1
+    scales[0, :, 2] = 252
+    one = inputs.f32_to_bf16_bits(np.ones(1, np.float32))[0]
+    act = np.zeros((K, K), np.uint16)
+    act[np.arange(K), np.arange(K)] = one
+    out = _gemm_gpu(B, act, codes, scales, [K])
+    dec = inputs.bf16_bits_to_f32(oracle.decode_expert_bf16(codes, scales, 0))
+    np.testing.assert_array_equal(out, dec.T)
+
+
+# ---------------------------------------------------------------- grouped GEMM
+
+def _explicit(gs, K, N, E=None, seed=0, exp=(-9, -3)):
+    gs = np.asarray(gs, np.int32)
+    E = len(gs) if E is None else E
+    act = inputs.normal_bf16(seed, 11, (int(gs.sum()), K))
+    codes, scales = inputs.mxfp4_weights(seed, 12, E, N, K, exp)
+    return act, codes, scales, gs
+
+
+GEMM_CASES = {
+    # bands of every shape class: empty, 1 row, around 16, around 128, > 2 chunks
+    "ragged_bands": lambda: _explicit([0, 1, 15, 16, 17, 127, 128, 129, 300, 0, 5], 512, 256),
+    # K not a multiple of the 128-wide stage, N not a multiple of the 128-wide tile
+    "k_tail_96": lambda: _explicit([9, 0, 33], 96, 200),
+    "k_tail_160": lambda: _explicit([40, 3], 160, 136),
+    "k_tail_224": lambda: _explicit([1, 2, 250], 224, 72),
+    "few_rows": lambda: _explicit([3, 0, 2], 256, 128),
+    "one_expert_long_band": lambda: _explicit([700], 256, 128),
+    "many_items": lambda: _explicit(np.random.default_rng(3).integers(0, 40, 64), 512, 512),
+}
+
+
+@pytest.mark.parametrize("name", sorted(GEMM_CASES))
+def test_gemm_matches_oracle(B, name):
+    act, codes, scales, gs = GEMM_CASES[name]()
+    out = _gemm_gpu(B, act, codes, scales, gs)
+    ref, mag = oracle.grouped_gemm(act, codes, scales, gs)
+    _tol_check(out, ref, mag, what=name)
+
+
+def test_gemm_tiny_config(B):
+    c = inputs.gemm_case("tiny")
+    gs, *_ = oracle.route_sort(c["ids"], c["E"])
+    g_gs = B.route_sort(B.to_device(c["ids"], DEV), c["E"])[0]
+    np.testing.assert_array_equal(g_gs.cpu().numpy(), gs)
+    assert gs[5] == 0
+    out = _gemm_gpu(B, c["act"], c["codes"], c["scales"], gs)
+    ref, mag = oracle.grouped_gemm(c["act"], c["codes"], c["scales"], gs)
+    _tol_check(out, ref, mag, what="tiny")
+
+
+def test_gemm_bf16_output(B):
+    act, codes, scales, gs = _explicit([5, 0, 130, 17], 384, 256)
+    out = inputs.bf16_bits_to_f32(_gemm_gpu(B, act, codes, scales, gs, torch.bfloat16))
+    ref, mag = oracle.grouped_gemm(act, codes, scales, gs)
+    _tol_check(out, ref, mag, extra=_bf16_ulp(ref), what="bf16 out")
+
+
+def test_gemm_empty_experts_are_not_read(B):
+    c = inputs.gemm_case("tiny")
+    gs, *_ = oracle.route_sort(c["ids"], c["E"])
+    base = _gemm_gpu(B, c["act"], c["codes"], c["scales"], gs)
+    codes, scales = c["codes"].copy(), c["scales"].copy()
+    codes[5] = 0x77
+    scales[5] = 0xFE                 # would flag MOE_ERR_DATA if it were decoded
+    poisoned = _gemm_gpu(B, c["act"], codes, scales, gs)
+    np.testing.assert_array_equal(base, poisoned)
+
+
+def test_gemm_repeatable(B):
+    act, codes, scales, gs = GEMM_CASES["many_items"]()
+    a = _gemm_gpu(B, act, codes, scales, gs)
+    b = _gemm_gpu(B, act, codes, scales, gs)
+    np.testing.assert_array_equal(a, b)
+
+
+def test_gemm_flags_inconsistent_group_sizes(B):
+    act, codes, scales, gs = _explicit([4, 4], 128, 128)
+    ws = B.make_workspace(0, 1, 1, DEV)
+    out = torch.full((8, 128), float("nan"), device=DEV)
+    bad = B.to_device(np.array([4, 5], np.int32), DEV)
+    B.grouped_gemm(B.bf16_from_bits(act, DEV), B.to_device(codes, DEV), B.to_device(scales, DEV), bad,
+                   out=out, workspace=ws)
+    assert B.read_status(ws) == B.MOE_ERR_DATA
+    assert torch.isnan(out).all()
+
+
+def test_gemm_flags_out_of_range_scale(B):
+    act, codes, scales, gs = _explicit([20], 128, 128)
+    scales[0, 7, 2] = 255
+    ws = B.make_workspace(0, 1, 1, DEV)
+    B.grouped_gemm(B.bf16_from_bits(act, DEV), B.to_device(codes, DEV), B.to_device(scales, DEV),
+                   B.to_device(gs, DEV), workspace=ws)
+    assert B.read_status(ws) == B.MOE_ERR_DATA
+
+
+def _sample_pairs(gs, N, n=3000, seed=0):
+    """(row, col) samples: random ones plus the first and last row of every band
+    and the first and last column."""
+    rng = np.random.default_rng(seed)
+    rows = int(np.sum(gs))
+    off = np.concatenate([[0], np.cumsum(gs)])
+    ne = np.nonzero(gs)[0]
+    edge_r = np.concatenate([off[ne], off[ne + 1] - 1])
+    r = np.concatenate([rng.integers(0, rows, n), edge_r, edge_r])
+    c = np.concatenate([rng.integers(0, N, n), rng.integers(0, N, edge_r.size), np.full(edge_r.size, N - 1)])
+    return r.astype(np.int64), c.astype(np.int64)
+
+
+@pytest.mark.parametrize("name", ["decode_w13", "decode_w2", "prefill_w13"])
+def test_gemm_full_size_sampled(B, name):
+    c = inputs.gemm_case(name)
+    gs, *_ = oracle.route_sort(c["ids"], c["E"])
+    g_gs = B.route_sort(B.to_device(c["ids"], DEV), c["E"])[0]
+    np.testing.assert_array_equal(g_gs.cpu().numpy(), gs)
+    out = _gemm_gpu(B, c["act"], c["codes"], c["scales"], gs)
+    r, col = _sample_pairs(gs, c["N"])
+    ref, mag = oracle.grouped_gemm_sampled(c["act"], c["codes"], c["scales"], gs, r, col)
+    _tol_check(out[r, col], ref, mag, what=name)
+    assert np.isfinite(out).all()
+
+
+def test_layer_size_gemms_sampled(B):
+    c = inputs.layer_case(seed=0)
+    gs, off, ss, s2r = oracle.route_sort(c["ids"], c["E"])
+    dev_ids = B.to_device(c["ids"], DEV)
+    x = B.bf16_from_bits(c["x"], DEV)
+    g_gs, _, g_ss, _, xs = B.route_sort(dev_ids, c["E"], x)
+    np.testing.assert_array_equal(g_ss.cpu().numpy(), ss)
+    xs_bits = B.bits_from_bf16(xs)
+    ws = B.make_workspace(0, 1, 1, DEV)
+    y13 = B.grouped_gemm(xs, B.to_device(c["w13_codes"], DEV), B.to_device(c["w13_scales"], DEV), g_gs,
+                         workspace=ws)
+    r, col = _sample_pairs(gs, 2 * c["inter"], seed=1)
+    ref, mag = oracle.grouped_gemm_sampled(xs_bits, c["w13_codes"], c["w13_scales"], gs, r, col)
+    _tol_check(y13.cpu().numpy()[r, col], ref, mag, what="layer w13")
+    h = B.swiglu(y13)
+    y2 = B.grouped_gemm(h, B.to_device(c["w2_codes"], DEV), B.to_device(c["w2_scales"], DEV), g_gs,
+                        workspace=ws)
+    assert B.read_status(ws) == B.MOE_OK
+    r, col = _sample_pairs(gs, c["hidden"], seed=2)
+    ref, mag = oracle.grouped_gemm_sampled(B.bits_from_bf16(h), c["w2_codes"], c["w2_scales"], gs, r, col)
+    _tol_check(y2.cpu().numpy()[r, col], ref, mag, what="layer w2")
+
+
+# ------------------------------------------------------------ SwiGLU, combine
+
+@pytest.mark.parametrize("dtype,I", [(torch.float32, 2048), (torch.bfloat16, 512), (torch.float32, 40),
+                                     (torch.bfloat16, 12)])
+def test_swiglu_within_one_ulp(B, dtype, I):
+    gu = inputs.gate_up_f32(4, 300, I)
+    gu[0, :4] = [0.0, -100.0, 95.0, -88.7]
+    t = torch.from_numpy(gu).to(DEV).to(dtype)
+    h = B.bits_from_bf16(B.swiglu(t))
+    ref = oracle.swiglu(t.float().cpu().numpy().astype(np.float64))
+    assert np.abs(h.astype(np.int64) - ref.astype(np.int64)).max() <= 1
+
+
+@pytest.mark.parametrize("T,k,N", [(500, 6, 4096), (7, 3, 10), (64, 1, 256)])
+def test_combine_matches_oracle_and_repeats(B, T, k, N):
+    rng = np.random.default_rng(T)
+    y = rng.standard_normal((T * k, N)).astype(np.float32)
+    s2r = rng.permutation(T * k).astype(np.int32)
+    w = rng.random((T, k)).astype(np.float32)
+    dy, ds, dw = B.to_device(y, DEV), B.to_device(s2r, DEV), B.to_device(w, DEV)
+    out = B.combine(dy, ds, dw)
+    ref, mag = oracle.combine(y.astype(np.float64), s2r, w)
+    _tol_check(out.cpu().numpy(), ref, mag, rel=1e-6, what="combine")
+    assert torch.equal(out, B.combine(dy, ds, dw))
+    if k == 1:
+        np.testing.assert_array_equal(B.combine(dy, ds, B.to_device(np.ones((T, 1), np.float32), DEV))
+                                      .cpu().numpy(), y[s2r])
+
+
+# --------------------------------------------------------------------- layer
+
+def test_layer_forward_stagewise(B):
+    c = inputs.layer_case(seed=1, T=96, E=16, hidden=512, inter=256, k=4)
+    T, k, E, H, I = c["T"], c["k"], c["E"], c["hidden"], c["inter"]
+    bufs = B.LayerBuffers(T, k, E, H, I, DEV)
+    out = B.layer_forward(B.bf16_from_bits(c["x"], DEV), B.to_device(c["ids"], DEV),
+                          B.to_device(c["topk_w"], DEV), B.to_device(c["w13_codes"], DEV),
+                          B.to_device(c["w13_scales"], DEV), B.to_device(c["w2_codes"], DEV),
+                          B.to_device(c["w2_scales"], DEV), bufs)
+    assert B.read_status(bufs.workspace) == B.MOE_OK
+    gs, off, ss, s2r = oracle.route_sort(c["ids"], E)
+    np.testing.assert_array_equal(bufs.slot_to_row.cpu().numpy(), s2r)
+    xs = oracle.gather(c["x"], ss, k)
+    np.testing.assert_array_equal(B.bits_from_bf16(bufs.x_sorted), xs)
+    y13, m13 = oracle.grouped_gemm(xs, c["w13_codes"], c["w13_scales"], gs)
+    _tol_check(bufs.y13.cpu().numpy(), y13, m13, what="w13")
+    href = oracle.swiglu(bufs.y13.cpu().numpy().astype(np.float64))
+    assert np.abs(B.bits_from_bf16(bufs.h).astype(np.int64) - href.astype(np.int64)).max() <= 1
+    y2, m2 = oracle.grouped_gemm(B.bits_from_bf16(bufs.h), c["w2_codes"], c["w2_scales"], gs)
+    _tol_check(bufs.y2.cpu().numpy(), y2, m2, what="w2")
+    o, mo = oracle.combine(bufs.y2.cpu().numpy().astype(np.float64), s2r, c["topk_w"])
+    _tol_check(out.cpu().numpy(), o, mo, rel=1e-6, what="combine")
+    assert B.last_launch_count() == 7
+
+
+# ------------------------------------------------------- failure detection
+
+def test_bounded_wait_times_out_and_context_survives(B):
+    ws = B.make_workspace(0, 1, 1, DEV)
+    B.debug_bounded_wait(2_000_000, ws)          # 2 ms on a barrier nothing completes
+    assert B.read_status(ws) == B.MOE_ERR_TIMEOUT
+    act, codes, scales, gs = _explicit([10, 0, 3], 128, 128)
+    out = _gemm_gpu(B, act, codes, scales, gs)
+    ref, mag = oracle.grouped_gemm(act, codes, scales, gs)
+    _tol_check(out, ref, mag, what="after timeout")
