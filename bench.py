@@ -1,0 +1,440 @@
+#!/usr/bin/env python
+"""Benchmark of the MXFP4 grouped MoE hot path on GB300.
+
+One step = one pass of the whole routed-expert path over one batch:
+route sort (+ activation gather) -> w13 grouped GEMM -> SwiGLU -> w2 grouped GEMM
+-> combine, all launched through the C ABI on one CUDA stream.
+
+Default workload (N=1): the decode shape of 64 tokens, 256 experts, top-6 (384
+sorted rows), w13 K = N = 4096, w2 K = 2048, N = 4096.  Other workloads
+(--workload) are the prefill and full-layer shapes.
+
+Prints one JSON line (rank 0).  value = grouped-GEMM TFLOP/s of the whole step
+(2 * rows * K * N for both GEMMs / step time); also reported: weight GB/s
+(touched experts x N x K x 17/32 bytes per GEMM), the roofline of the dominant
+kernel, an end-to-end number through host buffers, the CPU oracle baseline and
+the SM clocks seen during the timed region.
+
+--impl reference times the CPU oracle on the host cores instead (a bounded
+sample of the same workload per step).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "grouped MXFP4 GEMM TFLOP/s and weight GB/s, % of GB300 roofline, 1 GPU"
+WORKLOADS = {
+    "decode_T64": "Decode w13 shape: T=64 tokens, E=256 experts, top-6 (384 rows), uniform distinct "
+                  "routing; full path with w13 K=N=4096 and w2 K=2048 N=4096",
+    "decode_T256": "Decode w2 shape: T=256 tokens (1536 rows), uniform routing; full path",
+    "prefill_T4096": "Prefill w13 shape: T=4096 tokens (24576 rows), Zipf(1.1) routing with 20 "
+                     "experts unused; full path",
+    "layer_T8192": "Full MoE layer: T=8192 tokens (49152 rows), top-6 of N(0,1) logits, softmax "
+                   "router weights; full path",
+}
+DEFAULT_STEPS = {"decode_T64": 2000, "decode_T256": 1000, "prefill_T4096": 60, "layer_T8192": 30}
+
+# Fallback peaks (only if the measured-peaks file is absent).
+FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
+
+# DRAM bytes (read + write) per launch of the w13 GEMM kernel measured by ncu for
+# each workload, with the hash of the kernel source they were taken on.  A
+# changed kernel reports traffic = null until re-measured.
+NCU_TRAFFIC = {}
+NCU_KERNEL_HASH = None
+
+WEIGHT_BYTES_PER_ELEM = 17.0 / 32.0       # 4-bit code + one E8M0 byte per 32
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("grouped_gemm.cu", "mxfp4_decode.cuh", "device_common.cuh"):
+        with open(os.path.join(ROOT, "fp4_weight_grouped_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d["bf16_tflops_sustained"]), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def gemm_work(gs, K, N):
+    """FLOPs and algorithmic bytes of one grouped GEMM with group sizes gs."""
+    import numpy as np
+    gs = np.asarray(gs)
+    rows = int(gs.sum())
+    touched = int((gs > 0).sum())
+    flops = 2.0 * rows * K * N
+    wbytes = touched * N * K * WEIGHT_BYTES_PER_ELEM
+    return flops, wbytes, touched, rows
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t_start: float, t_end: float):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for ln in f:
+                parts = [x.strip() for x in ln.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        # Samples at 50 ms; keep the middle ones, which fall inside the timed region.
+        mid = rows[2:-2] if len(rows) > 6 else rows
+        sm = [float(r[1]) for r in mid if r[1].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in mid:
+            for nm, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": float(rows[0][2]) if rows[0][2].replace(".", "").isdigit() else None,
+                "power_w_max": max(float(r[3]) for r in mid if r[3].replace(".", "").isdigit()) if mid else None,
+                "samples": len(mid), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, local):
+    import numpy as np
+    import torch
+
+    import __graft_entry__ as ge
+    ge.build()
+    from fp4_weight_grouped_gb300 import binding as B
+    from fp4_weight_grouped_gb300 import inputs
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    c = inputs.layer_workload(args.workload, seed=args.seed + rank)
+    T, k, E, H, I = c["T"], c["k"], c["E"], c["hidden"], c["inter"]
+    x = B.bf16_from_bits(c["x"], dev)
+    ids = B.to_device(c["ids"], dev)
+    w = B.to_device(c["topk_w"], dev)
+    w13c, w13s = B.to_device(c["w13_codes"], dev), B.to_device(c["w13_scales"], dev)
+    w2c, w2s = B.to_device(c["w2_codes"], dev), B.to_device(c["w2_scales"], dev)
+    del c
+    bufs = B.LayerBuffers(T, k, E, H, I, dev)
+    stream = torch.cuda.current_stream(dev)
+    ws = bufs.workspace
+
+    def step(ev13=None):
+        gsz, _, _, s2r, xs = B.route_sort(ids, E, x, ws, out=(bufs.group_sizes, bufs.group_offsets,
+                                                                bufs.sorted_slot, bufs.slot_to_row,
+                                                                bufs.x_sorted))
+        if ev13 is not None:
+            ev13[0].record(stream)
+        B.grouped_gemm(xs, w13c, w13s, gsz, out=bufs.y13, workspace=ws)
+        if ev13 is not None:
+            ev13[1].record(stream)
+        B.swiglu(bufs.y13, out=bufs.h)
+        B.grouped_gemm(bufs.h, w2c, w2s, gsz, out=bufs.y2, workspace=ws)
+        B.combine(bufs.y2, s2r, w, out=bufs.out)
+
+    launches_per_step = 7
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    st = B.read_status(ws)
+    if st != B.MOE_OK:
+        raise RuntimeError(f"device status after warm-up: {B.status_string(st)}")
+    # Work accounting from the library's own routing output.
+    gs_np = bufs.group_sizes.cpu().numpy()
+    f13, b13, touched, rows = gemm_work(gs_np, H, 2 * I)
+    f2, b2, _, _ = gemm_work(gs_np, I, H)
+    act_bytes13 = rows * H * 2 + rows * 2 * I * 4          # x_sorted read + y13 (f32) write
+
+    K = args.steps
+    ev_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        wall0 = time.time()
+        t0.record(stream)
+        for i in range(K):
+            step(ev_pairs[i])
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+        wall1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = clk.summary(wall0, wall1)
+    ms_total = t0.elapsed_time(t1)
+    w13_ms = [a.elapsed_time(b) for a, b in ev_pairs]
+    st = B.read_status(ws)
+    if st != B.MOE_OK:
+        raise RuntimeError(f"device status after timing: {B.status_string(st)}")
+
+    # ---- end to end through host buffers (pinned), same path via moe_layer_forward
+    hx = torch.from_numpy(B.bits_from_bf16(x).view(np.int16)).pin_memory()
+    hids = ids.cpu().pin_memory()
+    hw = w.cpu().pin_memory()
+    hout = torch.empty((T, H), dtype=torch.float32).pin_memory()
+    dx, dids, dw = torch.empty_like(x), torch.empty_like(ids), torch.empty_like(w)
+    e2e_steps = max(3, min(K, 200))
+
+    def e2e_step():
+        dx.view(torch.int16).copy_(hx, non_blocking=True)
+        dids.copy_(hids, non_blocking=True)
+        dw.copy_(hw, non_blocking=True)
+        B.layer_forward(dx, dids, dw, w13c, w13s, w2c, w2s, bufs)
+        hout.copy_(bufs.out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    h2d = hx.numel() * 2 + hids.numel() * 4 + hw.numel() * 4
+    d2h = hout.numel() * 4
+
+    # ---- aggregate over ranks (max time)
+    ms_step = ms_total / K
+    if world > 1:
+        t = torch.tensor([ms_step, e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step, e2e_ms = float(t[0]), float(t[1])
+    flops = f13 + f2
+    hbm, bf16_burst, bf16_sus, peak_src = load_peaks()
+    w13_avg_ms = statistics.fmean(w13_ms)
+    w13_alg_bytes = b13 + act_bytes13
+    achieved = w13_alg_bytes / (w13_avg_ms * 1e-3) / 1e9
+    traffic = None
+    if NCU_KERNEL_HASH is not None and NCU_KERNEL_HASH == kernel_source_hash():
+        traffic = NCU_TRAFFIC.get(args.workload)
+    result = {
+        "metric": METRIC,
+        "value": round(world * flops / (ms_step * 1e-3) / 1e12, 3),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic: seeded numpy PCG64; bf16 N(0,1) tokens; uniform e2m1 nibbles with E8M0 "
+                "exponents in [-10,-2]; routing per workload",
+        "config": {"workload": args.workload, "description": WORKLOADS[args.workload], "T": T, "E": E,
+                   "top_k": k, "hidden": H, "inter": I, "rows": rows, "touched_experts": touched,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2: %.2f GB of touched MXFP4 weights per step vs 129 MB L2; "
+                         "no flush" % ((b13 + b2) / 1e9)},
+        "weight_GBps": round(world * (b13 + b2) / (ms_step * 1e-3) / 1e9, 1),
+        "gemm_flops_per_step": flops,
+        "weight_bytes_per_step": b13 + b2,
+        "roofline": {
+            "kernel": "grouped_gemm_kernel (w13)",
+            "bound": "hbm" if b13 / (hbm * 1e9) > f13 / (bf16_sus * 1e12) else "tensor",
+            "achieved": round(achieved, 1) if b13 / (hbm * 1e9) > f13 / (bf16_sus * 1e12)
+            else round(f13 / (w13_avg_ms * 1e-3) / 1e12, 1),
+            "peak": hbm if b13 / (hbm * 1e9) > f13 / (bf16_sus * 1e12) else bf16_burst,
+            "unit": "GB/s" if b13 / (hbm * 1e9) > f13 / (bf16_sus * 1e12) else "TFLOP/s",
+            "frac": None,
+            "traffic": traffic,
+            "peak_source": peak_src,
+            "algorithmic_bytes_per_launch": w13_alg_bytes,
+            "flops_per_launch": f13,
+            "avg_launch_ms": round(w13_avg_ms, 5),
+            "roofline_frac_of_max": None,
+        },
+        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "api": "moe_layer_forward with pinned host copies"},
+        "gpu_launches": launches_per_step * K,
+        "clocks": clocks,
+    }
+    r = result["roofline"]
+    r["frac"] = round(r["achieved"] / r["peak"], 4)
+    # Roofline fraction in the max(flop time, byte time) sense for the w13 launch.
+    t_roof = max(f13 / (bf16_burst * 1e12), b13 / (hbm * 1e9))
+    r["roofline_frac_of_max"] = round(t_roof / (w13_avg_ms * 1e-3), 4)
+    return result, dict(workload=args.workload, rank=rank)
+
+
+# --------------------------------------------------------------- CPU oracle arm
+
+def oracle_sample(workload: str, seed: int, max_experts: int):
+    """A bounded sample of the workload for the CPU oracle: the grouped GEMMs
+    of the first `max_experts` non-empty expert bands, SwiGLU on them and a
+    combine over the same rows."""
+    import numpy as np
+
+    from fp4_weight_grouped_gb300 import inputs
+    import oracle
+    c = inputs.layer_workload(workload, seed)
+    gs, off, ss, s2r = oracle.route_sort(c["ids"], c["E"])
+    keep = np.nonzero(gs)[0][:max_experts]
+    gs_s = np.zeros_like(gs)
+    gs_s[keep] = gs[keep]
+    rows_idx = np.concatenate([np.arange(off[e], off[e + 1]) for e in keep])
+    xs = oracle.gather(c["x"], ss, c["k"])[rows_idx]
+    return c, gs_s, xs
+
+
+def run_oracle_steps(c, gs_s, xs, steps):
+    import numpy as np
+
+    import oracle
+    H, I = c["hidden"], c["inter"]
+    times = []
+    for _ in range(steps):
+        t = time.perf_counter()
+        y13, _ = oracle.grouped_gemm(xs, c["w13_codes"], c["w13_scales"], gs_s, with_abs=False)
+        h = oracle.swiglu(y13)
+        y2, _ = oracle.grouped_gemm(h, c["w2_codes"], c["w2_scales"], gs_s, with_abs=False)
+        rows = y2.shape[0]
+        oracle.combine(y2, np.arange(rows, dtype=np.int32), np.ones((rows, 1), np.float32))
+        times.append(time.perf_counter() - t)
+    f13, _, _, _ = gemm_work(gs_s, H, 2 * I)
+    f2, _, _, _ = gemm_work(gs_s, I, H)
+    return (f13 + f2), times, oracle.threads_used()
+
+
+def cpu_baseline(workload: str, seed: int):
+    import numpy as np
+    n_exp = 64
+    c, gs_s, xs = oracle_sample(workload, seed, n_exp)
+    flops, times, threads = run_oracle_steps(c, gs_s, xs, 1)
+    return {"value": round(flops / times[0] / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"w13 + SwiGLU + w2 + combine over the first {n_exp} non-empty expert bands "
+                      f"({int(gs_s.sum())} rows) of the same workload, fp64 C oracle, one pass "
+                      f"({times[0]:.1f} s)"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    n_exp = 16
+    c, gs_s, xs = oracle_sample(args.workload, args.seed, n_exp)
+    run_oracle_steps(c, gs_s, xs, args.warmup_ref)
+    flops, times, threads = run_oracle_steps(c, gs_s, xs, args.steps_ref)
+    ms = 1e3 * sum(times) / len(times)
+    val = round(flops / (ms * 1e-3) / 1e12, 6)
+    sample = (f"w13 + SwiGLU + w2 + combine over the first {n_exp} non-empty expert bands "
+              f"({int(gs_s.sum())} rows) of {args.workload}, fp64 C oracle")
+    return {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps_ref, "warmup": args.warmup_ref, "ms_per_step": round(ms, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (same generator and seed as the GPU arm)",
+        "config": {"workload": args.workload, "description": WORKLOADS[args.workload],
+                   "sample": sample},
+        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decode_T64")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle leg")
+    args = ap.parse_args()
+    if args.steps is None:
+        args.steps = DEFAULT_STEPS[args.workload]
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local = dist_env()
+
+    if args.impl == "reference":
+        # The reference arm is the CPU oracle: bounded steps so the run stays short.
+        args.steps_ref = max(1, min(args.steps, 3))
+        args.warmup_ref = 1
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    res, _ = run_ours(args, rank, world, local)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline(args.workload, args.seed)
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -169,3 +169,27 @@ def gate_up_f32(seed: int, rows: int, inter: int) -> np.ndarray:
     """Random fused gate|up rows [rows, 2*inter] in float32 for SwiGLU tests."""
     rng = _rng(seed, _TAG_GATE)
     return (rng.standard_normal((rows, 2 * inter), dtype=np.float32) * np.float32(3.0))
+
+
+def router_weights_uniform(seed: int, T: int, k: int) -> np.ndarray:
+    """Positive router weights [T, k] for workloads whose ids are drawn directly
+    (uniform or Zipf routing): U(0,1) draws scaled to sum to 1 per token."""
+    rng = _rng(seed, _TAG_GATE, 1)
+    w = rng.random((T, k)) + 1e-3
+    return (w / w.sum(axis=1, keepdims=True)).astype(np.float32)
+
+
+def layer_workload(name: str, seed: int = 0) -> dict:
+    """Full-path inputs (route sort -> w13 -> SwiGLU -> w2 -> combine) for the
+    named workload; the token count and routing follow the named config."""
+    E, k, hidden, inter = 256, 6, 4096, 2048
+    if name == "layer_T8192":
+        return layer_case(seed)
+    T, routing = {"decode_T64": (64, "uniform"), "decode_T256": (256, "uniform"),
+                  "prefill_T4096": (4096, "zipf")}[name]
+    ids = route_uniform(seed, T, E, k) if routing == "uniform" else route_zipf(seed, T, E, k)
+    x = normal_bf16(seed, _TAG_X, (T, hidden))
+    c13, s13 = mxfp4_weights(seed, _TAG_W13, E, 2 * inter, hidden)
+    c2, s2 = mxfp4_weights(seed, _TAG_W2, E, hidden, inter)
+    return dict(ids=ids, topk_w=router_weights_uniform(seed, T, k), x=x, w13_codes=c13,
+                w13_scales=s13, w2_codes=c2, w2_scales=s2, T=T, E=E, k=k, hidden=hidden, inter=inter)
