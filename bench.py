@@ -176,18 +176,19 @@ def run_ours(args, rank, world, local):
     bufs = B.LayerBuffers(T, k, E, H, I, dev)
     stream = torch.cuda.current_stream(dev)
     ws = bufs.workspace
+    K8 = B.MOE_ACT_K8_INTERLEAVED     # the layer path keeps activations in the GEMM's k order
 
     def step(ev13=None):
         gsz, _, _, s2r, xs = B.route_sort(ids, E, x, ws, out=(bufs.group_sizes, bufs.group_offsets,
                                                                 bufs.sorted_slot, bufs.slot_to_row,
-                                                                bufs.x_sorted))
+                                                                bufs.x_sorted), x_layout=K8)
         if ev13 is not None:
             ev13[0].record(stream)
-        B.grouped_gemm(xs, w13c, w13s, gsz, out=bufs.y13, workspace=ws)
+        B.grouped_gemm(xs, w13c, w13s, gsz, out=bufs.y13, workspace=ws, act_layout=K8)
         if ev13 is not None:
             ev13[1].record(stream)
-        B.swiglu(bufs.y13, out=bufs.h)
-        B.grouped_gemm(bufs.h, w2c, w2s, gsz, out=bufs.y2, workspace=ws)
+        B.swiglu(bufs.y13, out=bufs.h, layout=K8)
+        B.grouped_gemm(bufs.h, w2c, w2s, gsz, out=bufs.y2, workspace=ws, act_layout=K8)
         B.combine(bufs.y2, s2r, w, out=bufs.out)
 
     launches_per_step = 7

@@ -15,6 +15,7 @@ from . import build_lib
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_DATA, MOE_ERR_TIMEOUT = range(6)
 MOE_F32, MOE_BF16 = 0, 1
+MOE_ACT_ROW_MAJOR, MOE_ACT_K8_INTERLEAVED = 0, 1
 
 SYMBOLS = (
     "moe_status_string", "moe_workspace_bytes", "moe_clear_status", "moe_read_status",
@@ -51,10 +52,10 @@ def load(path: str | None = None):
                 "moe_workspace_bytes": ([I32, I32, I32], SZ),
                 "moe_clear_status": ([P, P], C.c_int),
                 "moe_read_status": ([P, P], C.c_int),
-                "moe_route_sort": ([P, I32, I32, I32, P, P, P, P, P, I32, P, P, SZ, P], C.c_int),
-                "moe_mxfp4_grouped_gemm": ([P, I64, I32, P, P, P, I32, I32, P, C.c_int, P, SZ, P],
-                                           C.c_int),
-                "moe_swiglu": ([P, C.c_int, I64, I32, P, P], C.c_int),
+                "moe_route_sort": ([P, I32, I32, I32, P, P, P, P, P, I32, P, C.c_int, P, SZ, P], C.c_int),
+                "moe_mxfp4_grouped_gemm": ([P, C.c_int, I64, I32, P, P, P, I32, I32, P, C.c_int, P, SZ,
+                                            P], C.c_int),
+                "moe_swiglu": ([P, C.c_int, I64, I32, P, C.c_int, P], C.c_int),
                 "moe_combine": ([P, P, P, I32, I32, I32, P, C.c_int, P], C.c_int),
                 "moe_layer_forward": ([P, P, P, I32, I32, I32, I32, I32, P, P, P, P, P,
                                        P, P, P, P, P, P, P, P, P, SZ, P], C.c_int),
@@ -126,9 +127,10 @@ def read_status(workspace: torch.Tensor, stream=None) -> int:
 # ---------------------------------------------------------------- operations
 
 def route_sort(topk_ids: torch.Tensor, E: int, x: torch.Tensor | None = None,
-               workspace: torch.Tensor | None = None, out=None, stream=None):
+               workspace: torch.Tensor | None = None, out=None, stream=None,
+               x_layout: int = MOE_ACT_ROW_MAJOR):
     """Returns (group_sizes[E], group_offsets[E+1], sorted_slot[T*k],
-    slot_to_row[T*k], x_sorted or None)."""
+    slot_to_row[T*k], x_sorted or None); x_sorted in `x_layout` order."""
     T, k = topk_ids.shape
     dev = topk_ids.device
     rows = T * k
@@ -144,36 +146,39 @@ def route_sort(topk_ids: torch.Tensor, E: int, x: torch.Tensor | None = None,
         workspace = make_workspace(T, k, E, dev, stream)
     hidden = 0 if x is None else x.shape[1]
     rc = load().moe_route_sort(_ptr(topk_ids), T, k, E, _ptr(gs), _ptr(off), _ptr(ss), _ptr(s2r),
-                               _ptr(x), hidden, _ptr(xs), _ptr(workspace), workspace.numel(),
-                               _stream(stream))
+                               _ptr(x), hidden, _ptr(xs), x_layout, _ptr(workspace),
+                               workspace.numel(), _stream(stream))
     _check(rc, "moe_route_sort")
     return gs, off, ss, s2r, xs
 
 
 def grouped_gemm(act: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor,
                  group_sizes: torch.Tensor, out: torch.Tensor | None = None,
-                 out_dtype=torch.float32, workspace: torch.Tensor | None = None, stream=None):
-    """act bf16 [rows, K]; codes uint8 [E, N, K/2]; scales uint8 [E, N, K/32];
-    group_sizes int32 [E] -> out [rows, N] (f32 or bf16)."""
+                 out_dtype=torch.float32, workspace: torch.Tensor | None = None, stream=None,
+                 act_layout: int = MOE_ACT_ROW_MAJOR):
+    """act bf16 [rows, K] (row-major or K8-interleaved); codes uint8 [E, N, K/2];
+    scales uint8 [E, N, K/32]; group_sizes int32 [E] -> out [rows, N] (f32 or bf16)."""
     rows, K = act.shape
     E, N, _ = codes.shape
     if out is None:
         out = torch.empty((rows, N), dtype=out_dtype, device=act.device)
     if workspace is None:
         workspace = make_workspace(0, 1, 1, act.device, stream)
-    rc = load().moe_mxfp4_grouped_gemm(_ptr(act), rows, K, _ptr(codes), _ptr(scales),
+    rc = load().moe_mxfp4_grouped_gemm(_ptr(act), act_layout, rows, K, _ptr(codes), _ptr(scales),
                                        _ptr(group_sizes), E, N, _ptr(out), _dtype_code(out.dtype),
                                        _ptr(workspace), workspace.numel(), _stream(stream))
     _check(rc, "moe_mxfp4_grouped_gemm")
     return out
 
 
-def swiglu(gu: torch.Tensor, out: torch.Tensor | None = None, stream=None):
+def swiglu(gu: torch.Tensor, out: torch.Tensor | None = None, stream=None,
+           layout: int = MOE_ACT_ROW_MAJOR):
     rows, two_i = gu.shape
     I = two_i // 2
     if out is None:
         out = torch.empty((rows, I), dtype=torch.bfloat16, device=gu.device)
-    rc = load().moe_swiglu(_ptr(gu), _dtype_code(gu.dtype), rows, I, _ptr(out), _stream(stream))
+    rc = load().moe_swiglu(_ptr(gu), _dtype_code(gu.dtype), rows, I, _ptr(out), layout,
+                           _stream(stream))
     _check(rc, "moe_swiglu")
     return out
 

@@ -45,7 +45,7 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 int *status_word(void *workspace) { return static_cast<int *>(workspace); }
 
-moe_status check_gemm_args(const uint16_t *act, int64_t rows, int32_t K, const uint8_t *codes,
+moe_status check_gemm_args(const uint16_t *act, int layout, int64_t rows, int32_t K, const uint8_t *codes,
                            const uint8_t *scales, const int32_t *group_sizes, int32_t E, int32_t N,
                            const void *out, moe_dtype out_dtype, const void *workspace,
                            size_t workspace_bytes) {
@@ -53,6 +53,7 @@ moe_status check_gemm_args(const uint16_t *act, int64_t rows, int32_t K, const u
         return MOE_ERR_INVALID_ARG;
     if (static_cast<int64_t>(E) * N > INT32_MAX) return MOE_ERR_INVALID_ARG;
     if (out_dtype != MOE_F32 && out_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+    if (layout != MOE_ACT_ROW_MAJOR && layout != MOE_ACT_K8_INTERLEAVED) return MOE_ERR_INVALID_ARG;
     if (!codes || !scales || !group_sizes || !workspace || workspace_bytes < kStatusBytes)
         return MOE_ERR_INVALID_ARG;
     if (rows > 0 && (!act || !out)) return MOE_ERR_INVALID_ARG;
@@ -65,12 +66,14 @@ moe_status check_gemm_args(const uint16_t *act, int64_t rows, int32_t K, const u
 moe_status check_route_args(const int32_t *ids, int32_t T, int32_t k, int32_t E,
                             const int32_t *gs, const int32_t *off, const int32_t *ss,
                             const int32_t *s2r, const uint16_t *x, int32_t hidden,
-                            const uint16_t *xs, const void *workspace, size_t workspace_bytes) {
+                            const uint16_t *xs, int layout, const void *workspace,
+                            size_t workspace_bytes) {
     if (T < 0 || E <= 0 || E > kMaxE || k <= 0 || k > E) return MOE_ERR_INVALID_ARG;
     if (static_cast<int64_t>(T) * k > INT32_MAX) return MOE_ERR_INVALID_ARG;
     if (!gs || !off || !workspace) return MOE_ERR_INVALID_ARG;
     if (T > 0 && (!ids || !ss || !s2r)) return MOE_ERR_INVALID_ARG;
     if ((x == nullptr) != (xs == nullptr)) return MOE_ERR_INVALID_ARG;
+    if (layout != MOE_ACT_ROW_MAJOR && layout != MOE_ACT_K8_INTERLEAVED) return MOE_ERR_INVALID_ARG;
     if (x && (hidden <= 0 || hidden % 8 != 0 || !aligned(x, 16) || !aligned(xs, 16)))
         return MOE_ERR_INVALID_ARG;
     if (!aligned(workspace, 16) || workspace_bytes < moe_workspace_bytes(T, k, E))
@@ -121,16 +124,18 @@ moe_status moe_read_status(const void *workspace, void *stream) {
 moe_status moe_route_sort(const int32_t *topk_ids, int32_t T, int32_t k, int32_t E,
                           int32_t *group_sizes, int32_t *group_offsets, int32_t *sorted_slot,
                           int32_t *slot_to_row, const uint16_t *x, int32_t hidden,
-                          uint16_t *x_sorted, void *workspace, size_t workspace_bytes,
-                          void *stream) {
+                          uint16_t *x_sorted, moe_act_layout x_sorted_layout, void *workspace,
+                          size_t workspace_bytes, void *stream) {
     moe_status st = check_route_args(topk_ids, T, k, E, group_sizes, group_offsets, sorted_slot,
-                                     slot_to_row, x, hidden, x_sorted, workspace, workspace_bytes);
+                                     slot_to_row, x, hidden, x_sorted, x_sorted_layout, workspace,
+                                     workspace_bytes);
     if (st != MOE_OK) return st;
     int sms = 0;
     if ((st = current_device(&sms)) != MOE_OK) return st;
     int launches = 0;
     st = moe::launch_route_sort(topk_ids, T, k, E, group_sizes, group_offsets, sorted_slot,
                                 slot_to_row, x, hidden, x_sorted,
+                                x_sorted_layout == MOE_ACT_K8_INTERLEAVED,
                                 static_cast<uint8_t *>(workspace) + kStatusBytes,
                                 status_word(workspace), static_cast<cudaStream_t>(stream),
                                 &launches);
@@ -138,32 +143,36 @@ moe_status moe_route_sort(const int32_t *topk_ids, int32_t T, int32_t k, int32_t
     return st;
 }
 
-moe_status moe_mxfp4_grouped_gemm(const uint16_t *act, int64_t rows, int32_t K,
-                                  const uint8_t *codes, const uint8_t *scales,
+moe_status moe_mxfp4_grouped_gemm(const uint16_t *act, moe_act_layout act_layout, int64_t rows,
+                                  int32_t K, const uint8_t *codes, const uint8_t *scales,
                                   const int32_t *group_sizes, int32_t E, int32_t N, void *out,
                                   moe_dtype out_dtype, void *workspace, size_t workspace_bytes,
                                   void *stream) {
-    moe_status st = check_gemm_args(act, rows, K, codes, scales, group_sizes, E, N, out,
-                                    out_dtype, workspace, workspace_bytes);
+    moe_status st = check_gemm_args(act, act_layout, rows, K, codes, scales, group_sizes, E, N,
+                                    out, out_dtype, workspace, workspace_bytes);
     if (st != MOE_OK) return st;
     int sms = 0;
     if ((st = current_device(&sms)) != MOE_OK) return st;
     st = moe::launch_grouped_gemm(act, static_cast<int>(rows), K, codes, scales, group_sizes, E, N,
-                                  out, out_dtype == MOE_BF16, status_word(workspace), kWaitLimitNs,
+                                  out, out_dtype == MOE_BF16, act_layout == MOE_ACT_K8_INTERLEAVED,
+                                  status_word(workspace), kWaitLimitNs,
                                   static_cast<cudaStream_t>(stream), sms);
     g_last_launches = rows > 0 ? 1 : 0;
     return st;
 }
 
 moe_status moe_swiglu(const void *gu, moe_dtype in_dtype, int64_t rows, int32_t I, uint16_t *h,
-                      void *stream) {
+                      moe_act_layout h_layout, void *stream) {
     if (rows < 0 || I <= 0 || (in_dtype != MOE_F32 && in_dtype != MOE_BF16))
+        return MOE_ERR_INVALID_ARG;
+    if (h_layout != MOE_ACT_ROW_MAJOR && (h_layout != MOE_ACT_K8_INTERLEAVED || I % 8 != 0))
         return MOE_ERR_INVALID_ARG;
     if (rows > 0 && (!gu || !h || !aligned(gu, 16) || !aligned(h, 16))) return MOE_ERR_INVALID_ARG;
     int sms = 0;
     moe_status st = current_device(&sms);
     if (st != MOE_OK) return st;
-    st = moe::launch_swiglu(gu, in_dtype == MOE_BF16, rows, I, h, static_cast<cudaStream_t>(stream),
+    st = moe::launch_swiglu(gu, in_dtype == MOE_BF16, rows, I, h,
+                            h_layout == MOE_ACT_K8_INTERLEAVED, static_cast<cudaStream_t>(stream),
                             sms);
     g_last_launches = rows > 0 ? 1 : 0;
     return st;
@@ -197,12 +206,15 @@ moe_status moe_layer_forward(const uint16_t *x, const int32_t *topk_ids, const f
         return MOE_ERR_INVALID_ARG;
     const int64_t rows = static_cast<int64_t>(T) * k;
     moe_status st = check_route_args(topk_ids, T, k, E, group_sizes, group_offsets, sorted_slot,
-                                     slot_to_row, x, hidden, x_sorted, workspace, workspace_bytes);
+                                     slot_to_row, x, hidden, x_sorted, MOE_ACT_K8_INTERLEAVED,
+                                     workspace, workspace_bytes);
     if (st != MOE_OK) return st;
-    if ((st = check_gemm_args(x_sorted, rows, hidden, w13_codes, w13_scales, group_sizes, E,
-                              2 * inter, y13, MOE_F32, workspace, workspace_bytes)) != MOE_OK ||
-        (st = check_gemm_args(h, rows, inter, w2_codes, w2_scales, group_sizes, E, hidden, y2,
-                              MOE_F32, workspace, workspace_bytes)) != MOE_OK)
+    if ((st = check_gemm_args(x_sorted, MOE_ACT_K8_INTERLEAVED, rows, hidden, w13_codes,
+                              w13_scales, group_sizes, E, 2 * inter, y13, MOE_F32, workspace,
+                              workspace_bytes)) != MOE_OK ||
+        (st = check_gemm_args(h, MOE_ACT_K8_INTERLEAVED, rows, inter, w2_codes, w2_scales,
+                              group_sizes, E, hidden, y2, MOE_F32, workspace, workspace_bytes)) !=
+            MOE_OK)
         return st;
     if (T > 0 && (!aligned(y13, 16) || !aligned(h, 16) || !aligned(y2, 16) || !aligned(out, 16)))
         return MOE_ERR_INVALID_ARG;
@@ -212,22 +224,23 @@ moe_status moe_layer_forward(const uint16_t *x, const int32_t *topk_ids, const f
     int launches = 0, n = 0;
     int *status = status_word(workspace);
     st = moe::launch_route_sort(topk_ids, T, k, E, group_sizes, group_offsets, sorted_slot,
-                                slot_to_row, x, hidden, x_sorted,
+                                slot_to_row, x, hidden, x_sorted, 1,
                                 static_cast<uint8_t *>(workspace) + kStatusBytes, status, s, &n);
     launches += n;
     if (st == MOE_OK && rows > 0) {
         st = moe::launch_grouped_gemm(x_sorted, static_cast<int>(rows), hidden, w13_codes,
-                                      w13_scales, group_sizes, E, 2 * inter, y13, 0, status,
+                                      w13_scales, group_sizes, E, 2 * inter, y13, 0, 1, status,
                                       kWaitLimitNs, s, sms);
         ++launches;
     }
     if (st == MOE_OK && rows > 0) {
-        st = moe::launch_swiglu(y13, 0, rows, inter, h, s, sms);
+        st = moe::launch_swiglu(y13, 0, rows, inter, h, 1, s, sms);
         ++launches;
     }
     if (st == MOE_OK && rows > 0) {
         st = moe::launch_grouped_gemm(h, static_cast<int>(rows), inter, w2_codes, w2_scales,
-                                      group_sizes, E, hidden, y2, 0, status, kWaitLimitNs, s, sms);
+                                      group_sizes, E, hidden, y2, 0, 1, status, kWaitLimitNs, s,
+                                      sms);
         ++launches;
     }
     if (st == MOE_OK && T > 0) {

@@ -63,7 +63,7 @@ constexpr int kMaxE = 1024;
 constexpr int kOffCode = 0;
 constexpr int kOffAct = kOffCode + kCodeStages * kCodeStageBytes;
 constexpr int kOffLut = kOffAct + kActStages * kActStageBytes;
-constexpr int kOffRowOff = kOffLut + 256 * 16;
+constexpr int kOffRowOff = kOffLut;
 constexpr int kOffItemOff = kOffRowOff + (kMaxE + 1) * 4;
 constexpr int kOffBars = (kOffItemOff + (kMaxE + 1) * 4 + 7) & ~7;
 constexpr int kNumBars = 2 * kCodeStages + 2 * kActStages + 2 * kAStages + 2 * 2 + 1;
@@ -86,6 +86,7 @@ struct Params {
     int k_stages;      // ceil(K / 128)
     int scale_row;     // K / 32
     int scale_vec4;    // scale rows 4-byte aligned: load 4 scale bytes at once
+    int act_k8;        // activations already in the K8-interleaved order
     uint64_t wait_limit_ns;
 };
 
@@ -120,7 +121,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint4 *lut_tab = reinterpret_cast<uint4 *>(smem + kOffLut);
     int *roff = reinterpret_cast<int *>(smem + kOffRowOff);
     int *ioff = reinterpret_cast<int *>(smem + kOffItemOff);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBars);
@@ -143,10 +143,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
     const int E = p.E;
 
     // ---------------------------------------------------------------- prologue
-    if (tid < 256) {
-        const DecodeLut t = make_decode_lut(static_cast<uint32_t>(tid));
-        lut_tab[tid] = make_uint4(t.lo0, t.lo1, t.hi0, t.hi1);
-    }
     if (tid == 0) {
         *abort_flag = 0;
         *bad_flag = 0;
@@ -331,78 +327,113 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
         }
     } else if (warp >= 4 && warp < 12) {
         // ----------------------------------------------------------- converters
-        const int wg = (warp - 4) >> 2;            // 0 or 1: even / odd stages
+        // Warpgroup wg handles the stages g with g % 2 == wg.  Thread `row` owns
+        // weight row n0 + row (TMEM lane row) and decodes its 128 codes of the
+        // stage into 64 bf16 pairs (reduction order of the K8 interleave).  For
+        // activations given in natural order the warpgroup also interleaves the
+        // stage's activation tile in shared memory before the MMA reads it.
+        const int wg = (warp - 4) >> 2;
+        const int wtid = tid - 128 * (wg + 1);     // 0..127 within the warpgroup
         const int q = warp & 3;                    // TMEM lane quarter
-        const int row = q * 32 + lane;             // weight row (output column) in the tile
+        const int row = q * 32 + lane;
         const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-        const bool k_aligned = p.scale_vec4 != 0;
-        uint32_t g = 0;
-        bool ok = true;
+        const bool vec4 = p.scale_vec4 != 0;
+        const uint32_t total = static_cast<uint32_t>(my_items) * KT;
         int bad_scale = 0;
-        for (int i = 0; i < my_items && ok; ++i) {
-            const Item it = decode_item(blockIdx.x + i * gridDim.x, roff, ioff, E, p.n_tiles);
-            const int n = it.n0 + row;
-            const uint8_t *srow =
-                p.scales + (static_cast<size_t>(it.e) * p.N + (n < p.N ? n : 0)) * p.scale_row;
-            for (int ks = 0; ks < KT; ++ks, ++g) {
-                if (static_cast<int>(g & 1u) != wg) continue;
-                // Scale bytes of this row's four 32-element blocks in the stage.
-                uint32_t sw = 0x7F7F7F7Fu;
-                if (n < p.N) {
-                    if (k_aligned) {
-                        sw = __ldg(reinterpret_cast<const uint32_t *>(srow + ks * 4));
-                    } else {
-                        sw = 0;
-                        for (int b = 0; b < 4; ++b) {
-                            const int blk = ks * 4 + b;
-                            const uint32_t v = blk < p.scale_row ? __ldg(srow + blk) : 127u;
-                            sw |= v << (8 * b);
-                        }
-                    }
-                }
-                const uint32_t cslot = g % kCodeStages;
-                if (!warp_wait_bounded(&code_full[cslot], (g / kCodeStages) & 1u, abort_flag,
-                                       p.status, lim)) {
-                    ok = false;
-                    break;
-                }
-                // This row's 64 code bytes (4 chunks of 16, 64-byte swizzle).
-                uint32_t cw[4][4];
-                const uint8_t *crow = smem + kOffCode + cslot * kCodeStageBytes + row * 64;
-#pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
-                    const uint4 v = *reinterpret_cast<const uint4 *>(
-                        crow + ((ch ^ ((row >> 1) & 3)) << 4));
-                    cw[ch][0] = v.x;
-                    cw[ch][1] = v.y;
-                    cw[ch][2] = v.z;
-                    cw[ch][3] = v.w;
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&code_empty[cslot]);
-                const uint32_t aslot = g % kAStages;
-                if (!warp_wait_bounded(&a_empty[aslot], ((g / kAStages) & 1u) ^ 1u, abort_flag,
-                                       p.status, lim)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t a_addr = lane_base + kACol0 + aslot * kAColsPerStage;
-#pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
-                    const uint32_t s = (sw >> (8 * ch)) & 0xFFu;
-                    const uint4 l = lut_tab[s];
-                    const DecodeLut lut = {l.x, l.y, l.z, l.w};
-                    uint32_t o[16];
-                    if (!decode32(cw[ch], s, lut, o)) bad_scale = 1;
-                    __syncwarp();
-                    tmem_st16(a_addr + ch * 16, o);
-                }
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&a_full[aslot]);
+        int pf_item = -1, cur_item = -1, cur_nt = 16;
+        const uint8_t *srow = nullptr;
+        // Scale bytes of this row for stage g (four 32-element blocks); the
+        // row's scale pointer is looked up once per work item.
+        auto load_scales = [&](uint32_t g) -> uint32_t {
+            const int i = static_cast<int>(g / KT), ks = static_cast<int>(g - i * KT);
+            if (i != pf_item) {
+                const Item it = decode_item(blockIdx.x + i * gridDim.x, roff, ioff, E, p.n_tiles);
+                const int n = it.n0 + row;
+                srow = n < p.N ? p.scales + (static_cast<size_t>(it.e) * p.N + n) * p.scale_row
+                               : nullptr;
+                pf_item = i;
             }
+            if (!srow) return 0x7F7F7F7Fu;
+            if (vec4) return __ldg(reinterpret_cast<const uint32_t *>(srow + ks * 4));
+            uint32_t sw = 0;
+            for (int b = 0; b < 4; ++b) {
+                const int blk = ks * 4 + b;
+                sw |= (blk < p.scale_row ? static_cast<uint32_t>(__ldg(srow + blk)) : 127u) << (8 * b);
+            }
+            return sw;
+        };
+        uint32_t sw_next = wg < static_cast<int>(total) ? load_scales(wg) : 0u;
+        for (uint32_t g = wg; g < total; g += 2) {
+            const uint32_t sw = sw_next;
+            if (g + 2 < total) sw_next = load_scales(g + 2);   // one stage ahead
+            if (!p.act_k8) {
+                const int i = static_cast<int>(g / KT);
+                if (i != cur_item) {
+                    cur_nt = decode_item(blockIdx.x + i * gridDim.x, roff, ioff, E, p.n_tiles).nt;
+                    cur_item = i;
+                }
+            }
+            const uint32_t cslot = g % kCodeStages;
+            if (!warp_wait_bounded(&code_full[cslot], (g / kCodeStages) & 1u, abort_flag, p.status,
+                                   lim))
+                break;
+            // This row's 64 code bytes (4 chunks of 16, 64-byte swizzle).
+            uint32_t cw[4][4];
+            const uint8_t *crow = smem + kOffCode + cslot * kCodeStageBytes + row * 64;
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                const uint4 v = *reinterpret_cast<const uint4 *>(crow + ((ch ^ ((row >> 1) & 3)) << 4));
+                cw[ch][0] = v.x;
+                cw[ch][1] = v.y;
+                cw[ch][2] = v.z;
+                cw[ch][3] = v.w;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&code_empty[cslot]);
+            if (!p.act_k8) {
+                // Interleave every 16-byte chunk of the stage's activation rows in
+                // place (the permutation stays inside a chunk, so the swizzle of
+                // the tile does not matter).
+                const uint32_t xslot = g % kActStages;
+                if (!warp_wait_bounded(&act_full[xslot], (g / kActStages) & 1u, abort_flag,
+                                       p.status, lim))
+                    break;
+                uint8_t *abase = smem + kOffAct + xslot * kActStageBytes;
+                const int chunks = cur_nt * 8;          // per half: nt rows x 128 bytes
+                for (int c = wtid; c < 2 * chunks; c += 128) {
+                    const int h = c >= chunks;
+                    uint4 *ptr = reinterpret_cast<uint4 *>(abase + h * kActHalfBytes +
+                                                           (c - h * chunks) * 16);
+                    *ptr = interleave8(*ptr);
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            }
+            // Scale bytes 0..128 take one bf16 FMA, 129..252 two, 253..255 are
+            // errors; the warp agrees on the path.
+            const bool any_big = __any_sync(0xffffffffu, __vcmpgtu4(sw, 0x80808080u) != 0);
+            const bool any_bad = __any_sync(0xffffffffu, __vcmpgtu4(sw, 0xFCFCFCFCu) != 0);
+            const uint32_t aslot = g % kAStages;
+            if (!warp_wait_bounded(&a_empty[aslot], ((g / kAStages) & 1u) ^ 1u, abort_flag, p.status,
+                                   lim))
+                break;
+            tc_fence_after();
+            const uint32_t a_addr = lane_base + kACol0 + aslot * kAColsPerStage;
+            uint32_t o[64];
+            if (!any_big && !any_bad) {
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch)
+                    decode32_single(cw[ch], scale_pair_single((sw >> (8 * ch)) & 0xFFu), &o[16 * ch]);
+            } else {
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch)
+                    if (!decode32_any(cw[ch], (sw >> (8 * ch)) & 0xFFu, &o[16 * ch])) bad_scale = 1;
+            }
+            __syncwarp();
+            tmem_st64(a_addr, o);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&a_full[aslot]);
         }
         if (bad_scale) set_status(p.status, MOE_ERR_DATA);
     } else if (warp >= 12) {
@@ -455,15 +486,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
     }
 }
 
-// Debug view of the decode: one thread per (weight row n, 32-element block).
+// Debug view of the decode: one thread per (weight row n, 32-element block); the
+// GEMM's decode routine, with the reduction order mapped back to natural k.
 __global__ void decode_expert_kernel(const uint8_t *codes, const uint8_t *scales, int N, int K,
                                      int e, uint16_t *out, int *status) {
-    __shared__ uint4 lut_tab[256];
-    for (int s = threadIdx.x; s < 256; s += blockDim.x) {
-        const DecodeLut t = make_decode_lut(static_cast<uint32_t>(s));
-        lut_tab[s] = make_uint4(t.lo0, t.lo1, t.hi0, t.hi1);
-    }
-    __syncthreads();
     const int nblk = K / 32;
     const long long total = static_cast<long long>(N) * nblk;
     for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
@@ -477,12 +503,12 @@ __global__ void decode_expert_kernel(const uint8_t *codes, const uint8_t *scales
                    (static_cast<uint32_t>(src[4 * w + 2]) << 16) |
                    (static_cast<uint32_t>(src[4 * w + 3]) << 24);
         const uint32_t s = scales[row * nblk + b];
-        const uint4 l = lut_tab[s];
-        const DecodeLut lut = {l.x, l.y, l.z, l.w};
         uint32_t o[16];
-        if (!decode32(c, s, lut, o)) set_status(status, MOE_ERR_DATA);
-        uint32_t *dst = reinterpret_cast<uint32_t *>(out + static_cast<size_t>(n) * K + b * 32);
-        for (int w = 0; w < 16; ++w) dst[w] = o[w];
+        if (s <= 128u) decode32_single(c, scale_pair_single(s), o);
+        else if (!decode32_any(c, s, o)) set_status(status, MOE_ERR_DATA);
+        uint4 *dst = reinterpret_cast<uint4 *>(out + static_cast<size_t>(n) * K + b * 32);
+        for (int w = 0; w < 4; ++w)
+            dst[w] = deinterleave8(make_uint4(o[4 * w], o[4 * w + 1], o[4 * w + 2], o[4 * w + 3]));
     }
 }
 
@@ -519,8 +545,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
 
 moe_status launch_grouped_gemm(const uint16_t *act, int rows, int K, const uint8_t *codes,
                                const uint8_t *scales, const int32_t *group_sizes, int E, int N,
-                               void *out, int out_bf16, int *status, uint64_t wait_limit_ns,
-                               cudaStream_t stream, int num_sms) {
+                               void *out, int out_bf16, int act_k8, int *status,
+                               uint64_t wait_limit_ns, cudaStream_t stream, int num_sms) {
     using namespace gemm;
     if (rows == 0) return MOE_OK;
     PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode_fn();
@@ -572,6 +598,7 @@ moe_status launch_grouped_gemm(const uint16_t *act, int rows, int K, const uint8
     p.scale_row = K / 32;
     p.scale_vec4 = ((K / 32) % 4 == 0) && ((reinterpret_cast<uintptr_t>(scales) & 3) == 0);
     p.wait_limit_ns = wait_limit_ns;
+    p.act_k8 = act_k8;
     grouped_gemm_kernel<<<num_sms, kThreads, kSmemBytes, stream>>>(tm_codes, tm_act, p);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

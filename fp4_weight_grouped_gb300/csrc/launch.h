@@ -14,13 +14,13 @@ size_t route_sort_scratch_bytes(int T, int k, int E);
 
 moe_status launch_route_sort(const int32_t *ids, int T, int k, int E, int32_t *group_sizes,
                              int32_t *offsets, int32_t *sorted_slot, int32_t *slot_to_row,
-                             const uint16_t *x, int hidden, uint16_t *x_sorted, void *scratch,
-                             int *status, cudaStream_t stream, int *launches);
+                             const uint16_t *x, int hidden, uint16_t *x_sorted, int x_k8,
+                             void *scratch, int *status, cudaStream_t stream, int *launches);
 
 moe_status launch_grouped_gemm(const uint16_t *act, int rows, int K, const uint8_t *codes,
                                const uint8_t *scales, const int32_t *group_sizes, int E, int N,
-                               void *out, int out_bf16, int *status, uint64_t wait_limit_ns,
-                               cudaStream_t stream, int num_sms);
+                               void *out, int out_bf16, int act_k8, int *status,
+                               uint64_t wait_limit_ns, cudaStream_t stream, int num_sms);
 
 moe_status launch_decode_expert(const uint8_t *codes, const uint8_t *scales, int N, int K, int e,
                                 uint16_t *out, int *status, cudaStream_t stream);
@@ -28,7 +28,7 @@ moe_status launch_decode_expert(const uint8_t *codes, const uint8_t *scales, int
 moe_status launch_bounded_wait(uint64_t limit_ns, int *status, cudaStream_t stream);
 
 moe_status launch_swiglu(const void *gu, int in_bf16, long long rows, int I, uint16_t *h,
-                         cudaStream_t stream, int num_sms);
+                         int h_k8, cudaStream_t stream, int num_sms);
 
 moe_status launch_combine(const float *y, const int32_t *s2r, const float *w, int T, int k, int N,
                           void *out, int out_bf16, cudaStream_t stream, int num_sms);

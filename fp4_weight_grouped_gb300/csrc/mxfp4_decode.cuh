@@ -2,108 +2,119 @@
 //
 // "Running DeepSeek V4 Flash on TPU v6", section 1: the eight e2m1 magnitudes are
 // 0, 0.5, 1, 1.5, 2, 3, 4, 6, and the per-32 block scale is applied to the decoded
-// values before the matmul.  Every such product with s in 0..252 is a bf16 number,
-// so the decode is exact.  Code 0x8 (-0) yields +0 ("DeepSeek-V4-Flash-0731-NVFP4",
-// the E2M1 -0 -> +0 canonicalisation).
+// values before the matmul.  Every such product with s in 0..252 is a bf16 number
+// (normal or subnormal), so the decode is exact.  Code 0x8 (-0) yields +0
+// ("DeepSeek-V4-Flash-0731-NVFP4", the E2M1 -0 -> +0 canonicalisation).
 //
-// GB300 design: instead of the page's three vector ops on a re-encoded integer,
-// each 32-code block gets a byte lookup table for its scale s.  For s in 2..252
-// every bf16 result is a normal number whose 16-bit pattern is
-//     V[m] = (s-1)<<7 + {0, 0, 0x80, 0xC0, 0x100, 0x140, 0x180, 0x1C0}[m]   (m >= 1),
-//     V[0] = 0,
-// for magnitude index m = 2e + mant.  The low and high bytes of V[0..7] form two
-// 8-byte tables; `prmt` looks four nibbles up at once, the sign bit (of nonzero
-// codes only) is OR-ed into the high byte, and a final `prmt` interleaves the
-// bytes into bf16 pairs.  Scale bytes 0 and 1 give bf16 subnormals and take a
-// slower exact path; 253..255 are out of range (status MOE_ERR_DATA, NaN).
+// GB300 design.  Integer logic (LOP3/PRMT/shifts) issues at half rate on the SM's
+// ALU pipe, while IMAD and bf16x2 FMA go to the FMA pipe, so the decode splits
+// its work across both:
+//   1. Two codes of one 32-bit code word, nibbles j and j+4, are masked into the
+//      low nibble of each 16-bit half (one LOP3).
+//   2. One IMAD by 0x1040 copies each nibble to bits 6..9 and 12..15 of its half;
+//      a second LOP3 keeps bits 6..8 (exponent+mantissa e1 e0 m) and bit 15
+//      (sign).  As a bf16 pattern that is exactly e2m1 * 2^-126: e = 0 lands in
+//      bf16's subnormal range, which represents 0 and 0.5 * 2^-126 exactly.
+//   3. One fma.rn.bf16x2 by 2^(s-1) (and +0) gives e2m1 * 2^(s-127) exactly; the
+//      +0 addend turns the -0 of code 0x8 into +0.  For s > 128 the constant
+//      would overflow, so the product is split into * 2^126 then * 2^(s-127).
+// So one pair of weights costs 2 ALU + 2 FMA-pipe instructions.
+//
+// Pairing nibbles j and j+4 means one 32-bit result holds elements (8w + j,
+// 8w + j + 4) of a code word w.  The GEMM therefore consumes the reduction
+// dimension in the order [0,4,1,5,2,6,3,7] within every group of 8, and the
+// activations must use the same order (the "K8-interleaved" layout).
 #pragma once
 
 #include "device_common.cuh"
 
 namespace moe {
 
-struct DecodeLut {
-    uint32_t lo0, lo1, hi0, hi1;   // bytes 0..7: low / high byte of V[m]
-};
-
-// Lookup table for scale byte s (valid for 2 <= s <= 252; zeros otherwise).
-__device__ __forceinline__ DecodeLut make_decode_lut(uint32_t s) {
-    DecodeLut t = {0u, 0u, 0u, 0u};
-    if (s >= 2u && s <= 252u) {
-        const uint32_t q = (s - 1u) << 7;          // bf16 bits of 0.5 * 2^(s-127)
-        const uint32_t qq = q * 0x10001u;
-        const uint32_t v01 = q << 16;              // V0 = 0,        V1 = 0.5
-        const uint32_t v23 = qq + 0x00C00080u;     // V2 = 1.0,      V3 = 1.5
-        const uint32_t v45 = qq + 0x01400100u;     // V4 = 2.0,      V5 = 3.0
-        const uint32_t v67 = qq + 0x01C00180u;     // V6 = 4.0,      V7 = 6.0
-        t.lo0 = prmt(v01, v23, 0x6420u);
-        t.lo1 = prmt(v45, v67, 0x6420u);
-        t.hi0 = prmt(v01, v23, 0x7531u);
-        t.hi1 = prmt(v45, v67, 0x7531u);
-    }
-    return t;
+__device__ __forceinline__ uint32_t bf16x2_fma(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
 }
 
-// Eight codes (one 32-bit word, code i in bits 4i..4i+3, element order) to four
-// bf16 pairs (element 2j in the low half of o[j]).
-__device__ __forceinline__ void decode8_lut(uint32_t c, const DecodeLut &t, uint32_t *o) {
-    const uint32_t m = c & 0x77777777u;                       // magnitude index per nibble
-    const uint32_t sgn = (m + 0x77777777u) & c & 0x88888888u; // sign bit of nonzero codes
-    const uint32_t mh = m >> 16;
-    uint32_t L0 = prmt(t.lo0, t.lo1, m);                      // low bytes, codes 0..3
-    uint32_t H0 = prmt(t.hi0, t.hi1, m);                      // high bytes, codes 0..3
-    uint32_t L1 = prmt(t.lo0, t.lo1, mh);                     // codes 4..7
-    uint32_t H1 = prmt(t.hi0, t.hi1, mh);
-    const uint32_t s4 = sgn << 4;                             // even-code signs to bit 7 of a byte
-    H0 |= prmt(s4, sgn, 0x5140u) & 0x80808080u;
-    H1 |= prmt(s4, sgn, 0x7362u) & 0x80808080u;
-    o[0] = prmt(L0, H0, 0x5140u);
-    o[1] = prmt(L0, H0, 0x7362u);
-    o[2] = prmt(L1, H1, 0x5140u);
-    o[3] = prmt(L1, H1, 0x7362u);
+// bf16 patterns of e2m1 * 2^-126 for the code pairs of word c:
+// x[j] = (code j, code j+4), j = 0..3.
+__device__ __forceinline__ void e2m1_pairs_scaled_down(uint32_t c, uint32_t (&x)[4]) {
+    const uint32_t c8 = c >> 8;
+    x[0] = ((c & 0x000F000Fu) * 0x1040u) & 0x81C081C0u;
+    x[1] = ((c & 0x00F000F0u) * 0x0104u) & 0x81C081C0u;
+    x[2] = ((c8 & 0x000F000Fu) * 0x1040u) & 0x81C081C0u;
+    x[3] = ((c8 & 0x00F000F0u) * 0x0104u) & 0x81C081C0u;
 }
 
-// Exact slow path for one code with scale byte 0 or 1 (bf16 subnormal range).
-__device__ __forceinline__ uint32_t decode1_small_scale(uint32_t code, uint32_t s) {
-    const uint32_t mag = code & 7u;
-    const uint32_t e = mag >> 1, mt = mag & 1u;
-    // e2m1 magnitude as f32 bits: e == 0 -> 0 or 0.5; else 2^(e-1) * (1 + mt/2).
-    uint32_t fbits;
-    if (mag == 0u) fbits = 0u;
-    else if (e == 0u) fbits = 0x3F000000u;                      // 0.5
-    else fbits = ((126u + e) << 23) | (mt << 22);
-    const float v = __uint_as_float(fbits);
-    const float scale = __uint_as_float(s == 0u ? 0x00400000u : 0x00800000u);  // 2^-127, 2^-126
-    float w = v * scale;                                        // exact (no flush to zero)
-    uint32_t b = __float_as_uint(w) >> 16;                      // exact: at most 2 significant bits
-    if ((code & 8u) && mag) b |= 0x8000u;
-    return b;
+// bf16x2 of 2^(s-1) in both halves, for scale byte s in 0..128.
+__device__ __forceinline__ uint32_t scale_pair_single(uint32_t s) {
+    return s * 0x00800080u + 0x3F003F00u;          // (s + 126) << 7, twice
 }
 
-// Decode one 32-code block (16 bytes in c[0..3]) with scale byte s into 16 bf16
-// pairs.  `lut` must be make_decode_lut(s).  Returns false if s > 252 (the block
-// is then filled with NaN).
-__device__ __forceinline__ bool decode32(const uint32_t (&c)[4], uint32_t s, const DecodeLut &lut,
-                                         uint32_t (&o)[16]) {
-    if (s - 2u <= 250u) {
+// Scale pairs (first, second) for any s in 0..252: s <= 128 -> (2^(s-1), 1);
+// s > 128 -> (2^126, 2^(s-127)).
+__device__ __forceinline__ void scale_pair_split(uint32_t s, uint32_t &first, uint32_t &second) {
+    const bool big = s > 128u;
+    first = big ? 0x7E807E80u : scale_pair_single(s);
+    second = big ? s * 0x00800080u : 0x3F803F80u;
+}
+
+// Decode one 32-code block (16 bytes in c[0..3]) into 16 bf16 pairs in GEMM
+// reduction order; o[4w + j] = (element 8w + j, element 8w + j + 4).
+__device__ __forceinline__ void decode32_single(const uint32_t (&c)[4], uint32_t S,
+                                                uint32_t *o) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) decode8_lut(c[i], lut, &o[4 * i]);
-        return true;
+    for (int w = 0; w < 4; ++w) {
+        uint32_t x[4];
+        e2m1_pairs_scaled_down(c[w], x);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) o[4 * w + j] = bf16x2_fma(x[j], S, 0u);
     }
-    if (s <= 1u) {
+}
+
+__device__ __forceinline__ void decode32_split(const uint32_t (&c)[4], uint32_t S1, uint32_t S2,
+                                               uint32_t *o) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+    for (int w = 0; w < 4; ++w) {
+        uint32_t x[4];
+        e2m1_pairs_scaled_down(c[w], x);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t b = (c[i] >> (8 * j)) & 0xFFu;
-                o[4 * i + j] = decode1_small_scale(b & 15u, s) |
-                               (decode1_small_scale(b >> 4, s) << 16);
-            }
-        return true;
+        for (int j = 0; j < 4; ++j) o[4 * w + j] = bf16x2_fma(bf16x2_fma(x[j], S1, 0u), S2, 0u);
     }
+}
+
+// Any scale byte: 0..252 decode exactly; 253..255 give NaN and return false.
+__device__ __forceinline__ bool decode32_any(const uint32_t (&c)[4], uint32_t s, uint32_t *o) {
+    if (s > 252u) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) o[i] = 0x7FC07FC0u;
-    return false;
+        for (int i = 0; i < 16; ++i) o[i] = 0x7FC07FC0u;
+        return false;
+    }
+    uint32_t S1, S2;
+    scale_pair_split(s, S1, S2);
+    decode32_split(c, S1, S2, o);
+    return true;
+}
+
+// K8 interleave of 8 bf16 (one 16-byte chunk): natural (e0..e7) in (x, y, z, w)
+// -> (e0,e4), (e1,e5), (e2,e6), (e3,e7).
+__device__ __forceinline__ uint4 interleave8(uint4 v) {
+    uint4 r;
+    r.x = prmt(v.x, v.z, 0x5410u);
+    r.y = prmt(v.x, v.z, 0x7632u);
+    r.z = prmt(v.y, v.w, 0x5410u);
+    r.w = prmt(v.y, v.w, 0x7632u);
+    return r;
+}
+
+// Inverse of interleave8.
+__device__ __forceinline__ uint4 deinterleave8(uint4 v) {
+    uint4 r;
+    r.x = prmt(v.x, v.y, 0x5410u);
+    r.y = prmt(v.z, v.w, 0x5410u);
+    r.z = prmt(v.x, v.y, 0x7632u);
+    r.w = prmt(v.z, v.w, 0x7632u);
+    return r;
 }
 
 }  // namespace moe

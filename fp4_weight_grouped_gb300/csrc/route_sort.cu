@@ -20,6 +20,7 @@
 
 #include "device_common.cuh"
 #include "launch.h"
+#include "mxfp4_decode.cuh"
 
 namespace moe {
 namespace rs {
@@ -106,7 +107,7 @@ scan_kernel(int32_t *chunk_tot, int n_chunks, int E, int32_t *group_sizes, int32
 __global__ void __launch_bounds__(256)
 scatter_kernel(const int32_t *ids, int rows, int k, int E, const int32_t *chunk_base,
                const int32_t *offsets, const int32_t *rank, int32_t *sorted_slot,
-               int32_t *slot_to_row, const uint16_t *x, int hidden, uint16_t *x_sorted) {
+               int32_t *slot_to_row, const uint16_t *x, int hidden, uint16_t *x_sorted, int x_k8) {
     const int lane = threadIdx.x & 31;
     const int s = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (s >= rows) return;
@@ -123,15 +124,27 @@ scatter_kernel(const int32_t *ids, int rows, int k, int E, const int32_t *chunk_
         uint4 *dst = reinterpret_cast<uint4 *>(x_sorted + static_cast<size_t>(row) * hidden);
         const int nvec = hidden / 8;
         int i = lane;
-        for (; i + 96 < nvec; i += 128) {  // four independent 16-byte loads in flight
-            const uint4 a = __ldg(src + i), b = __ldg(src + i + 32), c = __ldg(src + i + 64),
-                        d = __ldg(src + i + 96);
-            dst[i] = a;
-            dst[i + 32] = b;
-            dst[i + 64] = c;
-            dst[i + 96] = d;
+        if (x_k8) {   // write the K8-interleaved order: a permutation inside each 16 bytes
+            for (; i + 96 < nvec; i += 128) {
+                const uint4 a = __ldg(src + i), b = __ldg(src + i + 32), c = __ldg(src + i + 64),
+                            d = __ldg(src + i + 96);
+                dst[i] = interleave8(a);
+                dst[i + 32] = interleave8(b);
+                dst[i + 64] = interleave8(c);
+                dst[i + 96] = interleave8(d);
+            }
+            for (; i < nvec; i += 32) dst[i] = interleave8(__ldg(src + i));
+        } else {
+            for (; i + 96 < nvec; i += 128) {  // four independent 16-byte loads in flight
+                const uint4 a = __ldg(src + i), b = __ldg(src + i + 32), c = __ldg(src + i + 64),
+                            d = __ldg(src + i + 96);
+                dst[i] = a;
+                dst[i + 32] = b;
+                dst[i + 64] = c;
+                dst[i + 96] = d;
+            }
+            for (; i < nvec; i += 32) dst[i] = __ldg(src + i);
         }
-        for (; i < nvec; i += 32) dst[i] = __ldg(src + i);
     }
 }
 
@@ -146,8 +159,8 @@ size_t route_sort_scratch_bytes(int T, int k, int E) {
 
 moe_status launch_route_sort(const int32_t *ids, int T, int k, int E, int32_t *group_sizes,
                              int32_t *offsets, int32_t *sorted_slot, int32_t *slot_to_row,
-                             const uint16_t *x, int hidden, uint16_t *x_sorted, void *scratch,
-                             int *status, cudaStream_t stream, int *launches) {
+                             const uint16_t *x, int hidden, uint16_t *x_sorted, int x_k8,
+                             void *scratch, int *status, cudaStream_t stream, int *launches) {
     const int rows = T * k;
     const int chunks = (rows + rs::kChunk - 1) / rs::kChunk;
     auto up = [](size_t b) { return (b + 255) & ~static_cast<size_t>(255); };
@@ -175,7 +188,7 @@ moe_status launch_route_sort(const int32_t *ids, int T, int k, int E, int32_t *g
     if (rows > 0) {
         rs::scatter_kernel<<<(rows + 7) / 8, 256, 0, stream>>>(ids, rows, k, E, chunk_tot, offsets,
                                                                rank, sorted_slot, slot_to_row, x,
-                                                               hidden, x_sorted);
+                                                               hidden, x_sorted, x_k8);
         ++*launches;
     }
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;

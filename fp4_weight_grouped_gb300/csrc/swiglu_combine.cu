@@ -17,6 +17,7 @@
 
 #include "device_common.cuh"
 #include "launch.h"
+#include "mxfp4_decode.cuh"
 
 namespace moe {
 namespace ew {
@@ -52,7 +53,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 template <typename T>
-__global__ void swiglu_vec8(const T *gu, long long rows, int I, uint16_t *h) {
+__global__ void swiglu_vec8(const T *gu, long long rows, int I, uint16_t *h, int h_k8) {
     const int per_row = I / 8;
     const long long total = rows * per_row;
     for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
@@ -68,7 +69,7 @@ __global__ void swiglu_vec8(const T *gu, long long rows, int I, uint16_t *h) {
         o.y = pack_bf16x2(silu(g[2]) * u[2], silu(g[3]) * u[3]);
         o.z = pack_bf16x2(silu(g[4]) * u[4], silu(g[5]) * u[5]);
         o.w = pack_bf16x2(silu(g[6]) * u[6], silu(g[7]) * u[7]);
-        *reinterpret_cast<uint4 *>(h + r * I + i) = o;
+        *reinterpret_cast<uint4 *>(h + r * I + i) = h_k8 ? interleave8(o) : o;
     }
 }
 
@@ -146,7 +147,7 @@ __global__ void combine_scalar(const float *y, const int32_t *s2r, const float *
 }  // namespace ew
 
 moe_status launch_swiglu(const void *gu, int in_bf16, long long rows, int I, uint16_t *h,
-                         cudaStream_t stream, int num_sms) {
+                         int h_k8, cudaStream_t stream, int num_sms) {
     if (rows == 0 || I == 0) return MOE_OK;
     const bool vec = (I % 8) == 0;
     const long long work = vec ? rows * (I / 8) : rows * I;
@@ -156,10 +157,10 @@ moe_status launch_swiglu(const void *gu, int in_bf16, long long rows, int I, uin
     if (vec) {
         if (in_bf16)
             ew::swiglu_vec8<<<static_cast<int>(blocks), 256, 0, stream>>>(
-                static_cast<const __nv_bfloat16 *>(gu), rows, I, h);
+                static_cast<const __nv_bfloat16 *>(gu), rows, I, h, h_k8);
         else
             ew::swiglu_vec8<<<static_cast<int>(blocks), 256, 0, stream>>>(
-                static_cast<const float *>(gu), rows, I, h);
+                static_cast<const float *>(gu), rows, I, h, h_k8);
     } else {
         if (in_bf16)
             ew::swiglu_scalar<<<static_cast<int>(blocks), 256, 0, stream>>>(

@@ -63,6 +63,15 @@ typedef enum {
 
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
 
+/* Order of the reduction dimension of a bf16 activation matrix [rows, K].
+ *  MOE_ACT_ROW_MAJOR      element k of a row at position k.
+ *  MOE_ACT_K8_INTERLEAVED within every group of 8 consecutive k (8g .. 8g+7)
+ *                         the stored order is 8g + {0,4,1,5,2,6,3,7}; K % 8 == 0.
+ * The grouped GEMM reduces in the interleaved order (its weight decode pairs
+ * codes j and j+4 of every 8); route sort and SwiGLU can write it at no cost,
+ * and the GEMM interleaves row-major input itself in shared memory. */
+typedef enum { MOE_ACT_ROW_MAJOR = 0, MOE_ACT_K8_INTERLEAVED = 1 } moe_act_layout;
+
 /* Human-readable name of a status code (static string). */
 MOE_API const char *moe_status_string(moe_status status);
 
@@ -95,7 +104,8 @@ MOE_API moe_status moe_read_status(const void *workspace, void *stream);
  *  x            device bf16 [T, hidden] or NULL: token activations.
  *  hidden       row length of x (multiple of 8 when x is given).
  *  x_sorted     device bf16 [T*k, hidden] out, or NULL: x_sorted[row] =
- *               x[sorted_slot[row] / k] (the activation permutation).
+ *               x[sorted_slot[row] / k] (the activation permutation), x row-major.
+ *  x_sorted_layout  order of the reduction dimension written to x_sorted.
  *  workspace    device, >= moe_workspace_bytes(T, k, E) bytes, 16-byte aligned.
  * Ids outside [0, E) set MOE_ERR_DATA; the outputs are then unspecified.
  * Launches three kernels (count, scan, scatter+gather); no atomics on data.
@@ -103,8 +113,8 @@ MOE_API moe_status moe_read_status(const void *workspace, void *stream);
 MOE_API moe_status moe_route_sort(const int32_t *topk_ids, int32_t T, int32_t k, int32_t E,
                           int32_t *group_sizes, int32_t *group_offsets, int32_t *sorted_slot,
                           int32_t *slot_to_row, const uint16_t *x, int32_t hidden,
-                          uint16_t *x_sorted, void *workspace, size_t workspace_bytes,
-                          void *stream);
+                          uint16_t *x_sorted, moe_act_layout x_sorted_layout, void *workspace,
+                          size_t workspace_bytes, void *stream);
 
 /*
  * moe_mxfp4_grouped_gemm — W4A16 grouped matmul over expert row bands ([TPU]
@@ -116,6 +126,7 @@ MOE_API moe_status moe_route_sort(const int32_t *topk_ids, int32_t T, int32_t k,
  * for every row r of band e (bands laid out in expert order by group_sizes).
  *
  *  act          device bf16 [rows, K], 16-byte aligned; rows >= 0.
+ *  act_layout   order of act's reduction dimension (row-major or K8-interleaved).
  *  K            reduction length, multiple of 32 (one E8M0 scale per 32).
  *  codes        device uint8 [E, N, K/2], 16-byte aligned: two e2m1 nibbles per
  *               byte, element 2j in bits 0-3; nibble bit 3 = sign, bits 2-1 =
@@ -131,7 +142,8 @@ MOE_API moe_status moe_route_sort(const int32_t *topk_ids, int32_t T, int32_t k,
  * in f32; results differ from an exact sum only by f32 accumulation order.
  * Empty experts launch no work and their weights are never read.
  */
-MOE_API moe_status moe_mxfp4_grouped_gemm(const uint16_t *act, int64_t rows, int32_t K,
+MOE_API moe_status moe_mxfp4_grouped_gemm(const uint16_t *act, moe_act_layout act_layout,
+                                  int64_t rows, int32_t K,
                                   const uint8_t *codes, const uint8_t *scales,
                                   const int32_t *group_sizes, int32_t E, int32_t N, void *out,
                                   moe_dtype out_dtype, void *workspace, size_t workspace_bytes,
@@ -147,9 +159,11 @@ MOE_API moe_status moe_mxfp4_grouped_gemm(const uint16_t *act, int64_t rows, int
  *
  *  gu     device [rows, 2*I], f32 or bf16 (in_dtype), 16-byte aligned.
  *  h      device bf16 [rows, I] out, 16-byte aligned.
+ *  h_layout  order of h's columns (K8-interleaved needs I % 8 == 0), so that h
+ *         can feed the next grouped GEMM directly.
  */
 MOE_API moe_status moe_swiglu(const void *gu, moe_dtype in_dtype, int64_t rows, int32_t I, uint16_t *h,
-                      void *stream);
+                      moe_act_layout h_layout, void *stream);
 
 /*
  * moe_combine — deterministic top-k weighted unpermute ([Pocket]: expert
@@ -172,7 +186,8 @@ MOE_API moe_status moe_combine(const float *y, const int32_t *slot_to_row, const
 /*
  * moe_layer_forward — the whole routed-expert path in one call:
  * route_sort (with gather) -> w13 grouped GEMM -> SwiGLU -> w2 grouped GEMM ->
- * combine, each stage as described above, all on `stream`.
+ * combine, each stage as described above, all on `stream`.  x_sorted and h
+ * are written in the K8-interleaved order.
  *
  *  x            device bf16 [T, hidden]; topk_ids int32 [T, k]; topk_w f32 [T, k].
  *  w13_codes/scales  [E, 2*inter, hidden/2] / [E, 2*inter, hidden/32]

@@ -38,16 +38,37 @@ def _tol_check(gpu, ref, mag, rel=1e-5, abs_=1e-6, extra=None, what=""):
     return float(np.max(diff / bound)) if diff.size else 0.0
 
 
+def k8_interleave(a):
+    """Natural k order -> the K8-interleaved order [0,4,1,5,2,6,3,7] per group of 8."""
+    a = np.ascontiguousarray(a)
+    K = a.shape[-1]
+    return a.reshape(*a.shape[:-1], K // 8, 2, 4).swapaxes(-1, -2).reshape(a.shape)
+
+
+def k8_deinterleave(a):
+    a = np.ascontiguousarray(a)
+    K = a.shape[-1]
+    return a.reshape(*a.shape[:-1], K // 8, 4, 2).swapaxes(-1, -2).reshape(a.shape)
+
+
+def test_k8_helpers_are_inverse_and_match_header_order():
+    a = np.arange(16).reshape(1, 16)
+    assert k8_interleave(a).tolist() == [[0, 4, 1, 5, 2, 6, 3, 7, 8, 12, 9, 13, 10, 14, 11, 15]]
+    np.testing.assert_array_equal(k8_deinterleave(k8_interleave(a)), a)
+
+
 def _bf16_ulp(x):
     a = np.abs(np.asarray(x, np.float64))
     e = np.floor(np.log2(np.maximum(a, 2.0 ** -133)))
     return np.ldexp(1.0, (np.maximum(e, -126) - 7).astype(np.int64))
 
 
-def _gemm_gpu(B, act, codes, scales, gs, out_dtype=torch.float32):
+def _gemm_gpu(B, act, codes, scales, gs, out_dtype=torch.float32, k8=False):
     ws = B.make_workspace(0, 1, 1, DEV)
-    out = B.grouped_gemm(B.bf16_from_bits(act, DEV), B.to_device(codes, DEV), B.to_device(scales, DEV),
-                         B.to_device(np.asarray(gs, np.int32), DEV), out_dtype=out_dtype, workspace=ws)
+    a = k8_interleave(act) if k8 else act
+    out = B.grouped_gemm(B.bf16_from_bits(a, DEV), B.to_device(codes, DEV), B.to_device(scales, DEV),
+                         B.to_device(np.asarray(gs, np.int32), DEV), out_dtype=out_dtype, workspace=ws,
+                         act_layout=B.MOE_ACT_K8_INTERLEAVED if k8 else B.MOE_ACT_ROW_MAJOR)
     st = B.read_status(ws)
     assert st == B.MOE_OK, B.status_string(st)
     if out_dtype == torch.bfloat16:
@@ -69,21 +90,24 @@ ROUTE_CASES = [
 ]
 
 
+@pytest.mark.parametrize("k8", [False, True], ids=["row_major", "k8"])
 @pytest.mark.parametrize("name,make", ROUTE_CASES, ids=[c[0] for c in ROUTE_CASES])
-def test_route_sort_bit_exact(B, name, make):
+def test_route_sort_bit_exact(B, name, make, k8):
     ids, E = make()
     T, k = ids.shape
     hidden = 64
     x = inputs.normal_bf16(1, 99, (T, hidden))
     ws = B.make_workspace(T, k, E, DEV)
-    gs, off, ss, s2r, xs = B.route_sort(B.to_device(ids, DEV), E, B.bf16_from_bits(x, DEV), ws)
+    gs, off, ss, s2r, xs = B.route_sort(B.to_device(ids, DEV), E, B.bf16_from_bits(x, DEV), ws,
+                                        x_layout=B.MOE_ACT_K8_INTERLEAVED if k8 else B.MOE_ACT_ROW_MAJOR)
     assert B.read_status(ws) == B.MOE_OK
     o_gs, o_off, o_ss, o_s2r = oracle.route_sort(ids, E)
     np.testing.assert_array_equal(gs.cpu().numpy(), o_gs)
     np.testing.assert_array_equal(off.cpu().numpy(), o_off)
     np.testing.assert_array_equal(ss.cpu().numpy(), o_ss)
     np.testing.assert_array_equal(s2r.cpu().numpy(), o_s2r)
-    np.testing.assert_array_equal(B.bits_from_bf16(xs), oracle.gather(x, o_ss, k))
+    got = B.bits_from_bf16(xs)
+    np.testing.assert_array_equal(k8_deinterleave(got) if k8 else got, oracle.gather(x, o_ss, k))
 
 
 def test_route_sort_repeatable_and_flags_bad_ids(B):
@@ -165,10 +189,11 @@ GEMM_CASES = {
 }
 
 
+@pytest.mark.parametrize("k8", [False, True], ids=["row_major", "k8"])
 @pytest.mark.parametrize("name", sorted(GEMM_CASES))
-def test_gemm_matches_oracle(B, name):
+def test_gemm_matches_oracle(B, name, k8):
     act, codes, scales, gs = GEMM_CASES[name]()
-    out = _gemm_gpu(B, act, codes, scales, gs)
+    out = _gemm_gpu(B, act, codes, scales, gs, k8=k8)
     ref, mag = oracle.grouped_gemm(act, codes, scales, gs)
     _tol_check(out, ref, mag, what=name)
 
@@ -280,13 +305,16 @@ def test_layer_size_gemms_sampled(B):
 
 # ------------------------------------------------------------ SwiGLU, combine
 
-@pytest.mark.parametrize("dtype,I", [(torch.float32, 2048), (torch.bfloat16, 512), (torch.float32, 40),
-                                     (torch.bfloat16, 12)])
-def test_swiglu_within_one_ulp(B, dtype, I):
+@pytest.mark.parametrize("dtype,I,k8", [(torch.float32, 2048, False), (torch.bfloat16, 512, False),
+                                        (torch.float32, 40, False), (torch.bfloat16, 12, False),
+                                        (torch.float32, 2048, True), (torch.bfloat16, 64, True)])
+def test_swiglu_within_one_ulp(B, dtype, I, k8):
     gu = inputs.gate_up_f32(4, 300, I)
     gu[0, :4] = [0.0, -100.0, 95.0, -88.7]
     t = torch.from_numpy(gu).to(DEV).to(dtype)
-    h = B.bits_from_bf16(B.swiglu(t))
+    h = B.bits_from_bf16(B.swiglu(t, layout=B.MOE_ACT_K8_INTERLEAVED if k8 else B.MOE_ACT_ROW_MAJOR))
+    if k8:
+        h = k8_deinterleave(h)
     ref = oracle.swiglu(t.float().cpu().numpy().astype(np.float64))
     assert np.abs(h.astype(np.int64) - ref.astype(np.int64)).max() <= 1
 
@@ -321,12 +349,13 @@ def test_layer_forward_stagewise(B):
     gs, off, ss, s2r = oracle.route_sort(c["ids"], E)
     np.testing.assert_array_equal(bufs.slot_to_row.cpu().numpy(), s2r)
     xs = oracle.gather(c["x"], ss, k)
-    np.testing.assert_array_equal(B.bits_from_bf16(bufs.x_sorted), xs)
+    np.testing.assert_array_equal(k8_deinterleave(B.bits_from_bf16(bufs.x_sorted)), xs)
     y13, m13 = oracle.grouped_gemm(xs, c["w13_codes"], c["w13_scales"], gs)
     _tol_check(bufs.y13.cpu().numpy(), y13, m13, what="w13")
     href = oracle.swiglu(bufs.y13.cpu().numpy().astype(np.float64))
-    assert np.abs(B.bits_from_bf16(bufs.h).astype(np.int64) - href.astype(np.int64)).max() <= 1
-    y2, m2 = oracle.grouped_gemm(B.bits_from_bf16(bufs.h), c["w2_codes"], c["w2_scales"], gs)
+    h_nat = k8_deinterleave(B.bits_from_bf16(bufs.h))
+    assert np.abs(h_nat.astype(np.int64) - href.astype(np.int64)).max() <= 1
+    y2, m2 = oracle.grouped_gemm(h_nat, c["w2_codes"], c["w2_scales"], gs)
     _tol_check(bufs.y2.cpu().numpy(), y2, m2, what="w2")
     o, mo = oracle.combine(bufs.y2.cpu().numpy().astype(np.float64), s2r, c["topk_w"])
     _tol_check(out.cpu().numpy(), o, mo, rel=1e-6, what="combine")

@@ -56,16 +56,17 @@ def test_workspace_bytes(lib):
 def test_gemm_rejects_bad_arguments_on_host(lib):
     f = lib.moe_mxfp4_grouped_gemm
     P = C.c_void_p
-    f.argtypes = [P, C.c_int64, C.c_int32, P, P, P, C.c_int32, C.c_int32, P, C.c_int, P, C.c_size_t, P]
+    f.argtypes = [P, C.c_int, C.c_int64, C.c_int32, P, P, P, C.c_int32, C.c_int32, P, C.c_int, P,
+                  C.c_size_t, P]
     f.restype = C.c_int
     fake = P(4096)
-    ok = dict(act=fake, rows=32, K=256, codes=fake, scales=fake, gs=fake, E=8, N=512, out=fake,
+    ok = dict(act=fake, lay=0, rows=32, K=256, codes=fake, scales=fake, gs=fake, E=8, N=512, out=fake,
               dt=0, ws=fake, wsb=256, s=None)
 
     def call(**kw):
         a = dict(ok, **kw)
-        return f(a["act"], a["rows"], a["K"], a["codes"], a["scales"], a["gs"], a["E"], a["N"],
-                 a["out"], a["dt"], a["ws"], a["wsb"], a["s"])
+        return f(a["act"], a["lay"], a["rows"], a["K"], a["codes"], a["scales"], a["gs"], a["E"],
+                 a["N"], a["out"], a["dt"], a["ws"], a["wsb"], a["s"])
 
     INVALID = 1
     assert call(K=48) == INVALID            # K % 32
@@ -82,6 +83,7 @@ def test_gemm_rejects_bad_arguments_on_host(lib):
     assert call(act=P(4098)) == INVALID     # TMA needs 16-byte aligned bases
     assert call(codes=P(4104)) == INVALID
     assert call(dt=7) == INVALID
+    assert call(lay=2) == INVALID
     # Valid arguments get past the host checks; without a GPU the device query fails.
     assert call() in (2, 3)
 
@@ -89,10 +91,12 @@ def test_gemm_rejects_bad_arguments_on_host(lib):
 def test_route_sort_rejects_bad_arguments_on_host(lib):
     f = lib.moe_route_sort
     P = C.c_void_p
-    f.argtypes = [P, C.c_int32, C.c_int32, C.c_int32, P, P, P, P, P, C.c_int32, P, P, C.c_size_t, P]
+    f.argtypes = [P, C.c_int32, C.c_int32, C.c_int32, P, P, P, P, P, C.c_int32, P, C.c_int, P,
+                  C.c_size_t, P]
     f.restype = C.c_int
     fake = P(4096)
-    assert f(fake, 16, 7, 6, fake, fake, fake, fake, None, 0, None, fake, 1 << 20, None) == 1   # k > E
-    assert f(fake, 16, 2, 8, fake, fake, fake, fake, fake, 256, None, fake, 1 << 20, None) == 1  # x w/o x_sorted
-    assert f(fake, 16, 2, 8, fake, fake, fake, fake, fake, 12, fake, fake, 1 << 20, None) == 1   # hidden % 8
-    assert f(fake, 16, 2, 8, fake, fake, fake, fake, None, 0, None, fake, 100, None) == 1        # small workspace
+    assert f(fake, 16, 7, 6, fake, fake, fake, fake, None, 0, None, 0, fake, 1 << 20, None) == 1   # k > E
+    assert f(fake, 16, 2, 8, fake, fake, fake, fake, fake, 256, None, 0, fake, 1 << 20, None) == 1  # x, no x_sorted
+    assert f(fake, 16, 2, 8, fake, fake, fake, fake, fake, 12, fake, 0, fake, 1 << 20, None) == 1   # hidden % 8
+    assert f(fake, 16, 2, 8, fake, fake, fake, fake, None, 0, None, 0, fake, 100, None) == 1        # small ws
+    assert f(fake, 16, 2, 8, fake, fake, fake, fake, None, 0, None, 5, fake, 1 << 20, None) == 1    # bad layout
