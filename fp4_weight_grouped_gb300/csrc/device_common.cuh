@@ -51,16 +51,14 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  : "memory");
 }
 
-// Test the phase with the given parity; if it is not complete the thread may
-// sleep (up to about 20 us, woken early by completion) before the answer.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(20000u)
+        : "r"(smem_u32(bar)), "r"(parity)
         : "memory");
     return ok != 0;
 }
@@ -69,13 +67,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 // after `limit_ns` nanoseconds (then raises *abort_flag and records
 // MOE_ERR_TIMEOUT) or as soon as another thread raised *abort_flag.  Returns
 // true if the phase completed.  abort_flag may be null (drain waits).
+// max_sleep_ns > 0 lets the thread back off with __nanosleep (32 ns doubling up
+// to max_sleep_ns) so that waiting roles leave issue slots to working warps.
 __device__ __forceinline__ bool wait_bounded(uint64_t *bar, uint32_t parity,
                                              volatile int *abort_flag, int *status,
-                                             uint64_t limit_ns) {
+                                             uint64_t limit_ns, uint32_t max_sleep_ns = 0) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
+    uint32_t sleep_ns = 32;
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
+        if (max_sleep_ns) {
+            __nanosleep(sleep_ns);
+            if (sleep_ns < max_sleep_ns) sleep_ns <<= 1;
+        }
         if ((it & 7u) == 0) {
             if (abort_flag && *abort_flag) return false;
             if (globaltimer_ns() - t0 > limit_ns) {
@@ -87,12 +92,14 @@ __device__ __forceinline__ bool wait_bounded(uint64_t *bar, uint32_t parity,
     }
 }
 
-// Warp-uniform form: lane 0 waits, every lane gets the same answer.
+// Warp-uniform form: lane 0 waits, every lane gets the same answer.  Every lane
+// of the warp must call it (it ends with a full-warp shuffle).
 __device__ __forceinline__ bool warp_wait_bounded(uint64_t *bar, uint32_t parity,
                                                   volatile int *abort_flag, int *status,
-                                                  uint64_t limit_ns) {
+                                                  uint64_t limit_ns, uint32_t max_sleep_ns = 0) {
     int ok = 0;
-    if ((threadIdx.x & 31) == 0) ok = wait_bounded(bar, parity, abort_flag, status, limit_ns);
+    if ((threadIdx.x & 31) == 0)
+        ok = wait_bounded(bar, parity, abort_flag, status, limit_ns, max_sleep_ns);
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
@@ -178,6 +185,20 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16
         "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
         "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
         "r"(v[15])
+        : "memory");
+}
+
+// Each lane of the warp writes 32 consecutive 32-bit columns of its own TMEM lane.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+        "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
+        "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
+        "r"(v[29]), "r"(v[30]), "r"(v[31])
         : "memory");
 }
 

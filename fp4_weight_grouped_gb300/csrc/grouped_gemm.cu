@@ -7,30 +7,31 @@
 // the matmul, bf16 products are exact in f32 and accumulate in f32.
 //
 // How (GB300 design, not the page's TPU design):
-//  * Swap-AB: the decoded weight tile (128 output columns n x K) is the MMA's
-//    A operand (M = 128) and the band's token rows are the B operand (MMA N =
-//    16..128, rounded up to 16).  Decode-sized bands (a few rows per expert) thus
-//    fill the 128-wide tensor-core dimension with weights, not with padding.
-//  * TMA streams the packed 4-bit codes (128 rows x 64 bytes per stage, 64-byte
-//    swizzle) and the activation rows (64-element boxes, 128-byte swizzle) into
-//    two shared-memory rings.
-//  * Two converter warpgroups (alternate K stages) decode codes x 2^k into bf16
-//    and write them straight into tensor memory with tcgen05.st; tcgen05.mma
-//    then reads A from tensor memory (no shared-memory round trip for the
-//    decoded weights, which would exceed the SM's shared-memory bandwidth at
-//    HBM rate).
-//  * One thread issues tcgen05.mma kind::f16 into one of two TMEM accumulators
-//    (128 columns each), so the epilogue of one work item overlaps the main
-//    loop of the next.
-//  * Four epilogue warps read the accumulator with tcgen05.ld (lane = output
-//    column n, column = token) and store rows of out with coalesced 128-byte
-//    writes, masking rows outside the band and columns >= N.
-//  * Persistent CTAs (one per SM) walk a static list of work items
-//    (expert, 128-token chunk, 128-column tile) built on the device from
-//    group_sizes; empty experts contribute no items and their weights are
-//    never read.
-//  * Every barrier wait is bounded; on timeout the kernel records
-//    MOE_ERR_TIMEOUT, drains its own copies and MMAs, frees TMEM and returns.
+//  * Swap-AB: the decoded weight tile (128 output columns n x K) is the MMA's A
+//    operand, held in tensor memory; the band's token rows are the B operand
+//    in shared memory (MMA N = 16..128).  Decode-sized bands thus fill the
+//    128-wide tensor-core dimension with weights, not with padding.
+//  * TMA streams the packed codes in 256-k stages (128 rows x 128 bytes,
+//    128-byte swizzle: wide rows move at about twice the rate of 64-byte
+//    ones) and the activation rows (64-element boxes) into shared memory.
+//  * Four converter warpgroups each own every 4th 64-k decode stage: they read
+//    their 32 code bytes per row, decode them to bf16 pairs and write them into
+//    one of eight tensor-memory A slots with tcgen05.st.  A slot and the
+//    activation tile of the same stage are released together by one
+//    tcgen05.commit.
+//  * Split mode (every band <= 32 rows): two issuer threads on different SM
+//    sub-partitions (one thread issues a small MMA only every ~50 cycles) each
+//    take every 2nd stage, accumulating into four per-warpgroup K-partial
+//    accumulators that the epilogue adds in a fixed order.  Single mode
+//    (wider bands): one issuer, one accumulator; N up to 128 keeps the tensor
+//    core busy.  Accumulators are double-buffered so the epilogue of one work
+//    item overlaps the next.
+//  * Persistent CTAs (one per SM) walk a static list of work items (expert,
+//    128-token chunk, 128-column tile) built on the device from group_sizes;
+//    empty experts contribute no items and their weights are never read.
+//  * Every wait is bounded (no unbounded barrier inside the pipeline); on
+//    timeout the kernel records MOE_ERR_TIMEOUT, drains its own copies and
+//    MMAs, frees tensor memory and returns.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -44,36 +45,35 @@
 namespace moe {
 namespace gemm {
 
-constexpr int kThreads = 512;                 // 16 warps
+constexpr int kThreads = 768;                 // 24 warps
+constexpr int kConvWG = 4;                    // converter warpgroups (warps 4..19)
+constexpr int kEpiWarp0 = 4 + 4 * kConvWG;    // epilogue warps 20..23
 constexpr int kBN = 128;                      // output columns per tile (MMA M)
-constexpr int kKS = 128;                      // K per pipeline stage
 constexpr int kMaxNT = 128;                   // tokens per work item (MMA N)
-constexpr int kCodeStages = 10;               // must be even (WG parity)
-constexpr int kActStages = 4;
-constexpr int kAStages = 4;                   // TMEM decoded-weight stages (even)
-constexpr int kCodeStageBytes = kBN * kKS / 2;            // 8 KB
-constexpr int kActHalfBytes = kMaxNT * 128;               // 64 bf16 per row
-constexpr int kActStageBytes = 2 * kActHalfBytes;         // 32 KB
+constexpr int kStageK = 64;                   // K per decode / MMA stage
+constexpr int kSlots = 8;                     // A slots in TMEM (+ activation slots in smem)
+constexpr int kCodeK = 256;                   // K per code stage (4 decode stages)
+constexpr int kCodeStageBytes = kBN * kCodeK / 2;         // 16 KB
+constexpr int kCodeStagesMax = 8;
+constexpr int kRingBytes = 192 * 1024;        // code ring + activation slots
 constexpr int kTmemCols = 512;
-constexpr int kAccCols = 128;
-constexpr int kACol0 = 2 * kAccCols;                      // A stages after the two accumulators
-constexpr int kAColsPerStage = kKS / 2;                   // bf16 pairs
+constexpr int kAccCols = 128;                 // per accumulator buffer
+constexpr int kACol0 = 2 * kAccCols;          // A slots after the two accumulator buffers
+constexpr int kAColsPerSlot = kStageK / 2;    // bf16 pairs: 32 columns
 constexpr int kMaxE = 1024;
 
 constexpr int kOffCode = 0;
-constexpr int kOffAct = kOffCode + kCodeStages * kCodeStageBytes;
-constexpr int kOffLut = kOffAct + kActStages * kActStageBytes;
-constexpr int kOffRowOff = kOffLut;
+constexpr int kOffRowOff = kOffCode + kRingBytes;
 constexpr int kOffItemOff = kOffRowOff + (kMaxE + 1) * 4;
 constexpr int kOffBars = (kOffItemOff + (kMaxE + 1) * 4 + 7) & ~7;
-constexpr int kNumBars = 2 * kCodeStages + 2 * kActStages + 2 * kAStages + 2 * 2 + 1;
+constexpr int kNumBars = 2 * kCodeStagesMax + 3 * kSlots + 2 * 2 + 2;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 64 + 1024;          // + alignment slack
 
-static_assert(kCodeStages % 2 == 0 && kAStages % 2 == 0, "WG parity needs even ring sizes");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kOffBars % 8 == 0, "barrier alignment");
-static_assert(kACol0 + kAStages * kAColsPerStage <= kTmemCols, "TMEM budget");
+static_assert(kACol0 + kSlots * kAColsPerSlot <= kTmemCols, "TMEM budget");
+static_assert(kSlots % kConvWG == 0, "each slot belongs to one warpgroup");
 
 struct Params {
     const uint8_t *scales;
@@ -83,9 +83,9 @@ struct Params {
     int rows, K, N, E;
     int out_bf16;
     int n_tiles;       // ceil(N / 128)
-    int k_stages;      // ceil(K / 128)
+    int k_stages;      // 64-k stages per item: 4 * ceil(K / 256)
     int scale_row;     // K / 32
-    int scale_vec4;    // scale rows 4-byte aligned: load 4 scale bytes at once
+    int scale_vec2;    // scale rows 2-byte aligned: load a stage's 2 scale bytes at once
     int act_k8;        // activations already in the K8-interleaved order
     uint64_t wait_limit_ns;
 };
@@ -125,17 +125,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
     int *ioff = reinterpret_cast<int *>(smem + kOffItemOff);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBars);
     uint64_t *code_full = bars;
-    uint64_t *code_empty = code_full + kCodeStages;
-    uint64_t *act_full = code_empty + kCodeStages;
-    uint64_t *act_empty = act_full + kActStages;
-    uint64_t *a_full = act_empty + kActStages;
-    uint64_t *a_empty = a_full + kAStages;
-    uint64_t *acc_full = a_empty + kAStages;
+    uint64_t *code_empty = code_full + kCodeStagesMax;
+    uint64_t *a_full = code_empty + kCodeStagesMax;     // converters -> issuer (4 warps)
+    uint64_t *act_full = a_full + kSlots;                // TMA -> issuer
+    uint64_t *slot_empty = act_full + kSlots;            // MMA commit -> converters, act producer
+    uint64_t *acc_full = slot_empty + kSlots;
     uint64_t *acc_empty = acc_full + 2;
-    uint64_t *final_bar = acc_empty + 2;
+    uint64_t *final_bar = acc_empty + 2;                 // one per issuer thread
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 8);
     int *bad_flag = reinterpret_cast<int *>(smem + kOffMisc + 16);
+    int *nt_max_slot = reinterpret_cast<int *>(smem + kOffMisc + 24);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -149,9 +149,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
     }
     __syncthreads();
     // Row offsets and work-item offsets: exclusive prefix sums over experts,
-    // done by warp 0 in chunks of 32 (E <= 1024).
+    // done by warp 0 in chunks of 32 (E <= 1024); also the widest work item.
     if (warp == 0) {
-        int run_rows = 0, run_items = 0;
+        int run_rows = 0, run_items = 0, nt_max = 0;
         for (int base = 0; base < E; base += 32) {
             const int e = base + lane;
             int gs = 0;
@@ -161,6 +161,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
             }
             const int g = gs > 0 ? gs : 0;
             const int items = ((g + kMaxNT - 1) / kMaxNT) * p.n_tiles;
+            nt_max = max(nt_max, min(kMaxNT, (g + 15) & ~15));
             int incl_r = g, incl_i = items;
 #pragma unroll
             for (int d = 1; d < 32; d <<= 1) {
@@ -178,9 +179,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
             run_rows += __shfl_sync(0xffffffffu, incl_r, 31);
             run_items += __shfl_sync(0xffffffffu, incl_i, 31);
         }
+        nt_max = __reduce_max_sync(0xffffffffu, nt_max);
         if (lane == 0) {
             roff[E] = run_rows;
             ioff[E] = run_items;
+            *nt_max_slot = nt_max;
             if (run_rows != p.rows) *bad_flag = 1;
         }
     }
@@ -192,26 +195,33 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
     const int total_items = ioff[E];
     if (static_cast<int>(blockIdx.x) >= total_items) return;
     const int my_items = (total_items - static_cast<int>(blockIdx.x) + gridDim.x - 1) / gridDim.x;
+    const int KT = p.k_stages;
+    const uint32_t total = static_cast<uint32_t>(my_items) * KT;   // decode stages of this CTA
+    // Split mode: every band <= 32 rows.  Activation slots are sized for the
+    // widest band; the code ring takes the rest of the 192 KB (at most 8).
+    const int nt_max = *nt_max_slot;
+    const bool split = nt_max <= 32;
+    const uint32_t act_stage_bytes = static_cast<uint32_t>(nt_max) * 128u;
+    const uint32_t CS = min(static_cast<uint32_t>(kCodeStagesMax),
+                            (kRingBytes - kSlots * act_stage_bytes) / kCodeStageBytes);
+    const uint32_t act_off = CS * kCodeStageBytes;
 
     if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
     if (tid == 0) {
-        for (int i = 0; i < kCodeStages; ++i) {
+        for (uint32_t i = 0; i < CS; ++i) {
             mbar_init(&code_full[i], 1);
-            mbar_init(&code_empty[i], 4);
+            mbar_init(&code_empty[i], 4 * kConvWG);
         }
-        for (int i = 0; i < kActStages; ++i) {
-            mbar_init(&act_full[i], 1);
-            mbar_init(&act_empty[i], 1);
-        }
-        for (int i = 0; i < kAStages; ++i) {
+        for (int i = 0; i < kSlots; ++i) {
             mbar_init(&a_full[i], 4);
-            mbar_init(&a_empty[i], 1);
+            mbar_init(&act_full[i], 1);
+            mbar_init(&slot_empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_full[i], split ? kConvWG : 1);
             mbar_init(&acc_empty[i], 4);
         }
-        mbar_init(final_bar, 1);
+        for (int i = 0; i < 2; ++i) mbar_init(&final_bar[i], 1);
         mbar_fence_init();
     }
     tc_fence_before();
@@ -219,36 +229,34 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const uint32_t code_smem = smem_u32(smem + kOffCode);
-    const uint32_t act_smem = smem_u32(smem + kOffAct);
-    const int KT = p.k_stages;
+    const uint32_t act_smem = smem_u32(smem + act_off);
     const uint64_t lim = p.wait_limit_ns;
 
     if (warp == 0) {
         // ------------------------------------------------------ code producer
         if (lane == 0) {
             tma_prefetch_map(&tm_codes);
-            uint32_t g = 0;
+            uint32_t c = 0;
             bool ok = true;
             for (int i = 0; i < my_items && ok; ++i) {
                 const Item it = decode_item(blockIdx.x + i * gridDim.x, roff, ioff, E, p.n_tiles);
                 const int y = it.e * p.N + it.n0;
-                for (int ks = 0; ks < KT; ++ks, ++g) {
-                    const uint32_t slot = g % kCodeStages;
-                    if (!wait_bounded(&code_empty[slot], ((g / kCodeStages) & 1u) ^ 1u, abort_flag,
-                                      p.status, lim)) {
+                for (int kc = 0; kc < KT / 4; ++kc, ++c) {
+                    const uint32_t slot = c % CS;
+                    if (!wait_bounded(&code_empty[slot], ((c / CS) & 1u) ^ 1u, abort_flag, p.status,
+                                      lim, 128)) {
                         ok = false;
                         break;
                     }
                     mbar_arrive_expect_tx(&code_full[slot], kCodeStageBytes);
-                    tma_load_2d(code_smem + slot * kCodeStageBytes, &tm_codes, ks * (kKS / 2), y,
+                    tma_load_2d(code_smem + slot * kCodeStageBytes, &tm_codes, kc * 128, y,
                                 &code_full[slot]);
                 }
             }
             if (!ok) {   // drain: every issued copy must land before the CTA exits
-                const uint32_t first = g > kCodeStages ? g - kCodeStages : 0;
-                for (uint32_t h = first; h < g; ++h)
-                    wait_bounded(&code_full[h % kCodeStages], (h / kCodeStages) & 1u, nullptr,
-                                 p.status, lim);
+                const uint32_t first = c > CS ? c - CS : 0;
+                for (uint32_t h = first; h < c; ++h)
+                    wait_bounded(&code_full[h % CS], (h / CS) & 1u, nullptr, p.status, lim);
             }
         }
     } else if (warp == 2) {
@@ -260,89 +268,92 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
             for (int i = 0; i < my_items && ok; ++i) {
                 const Item it = decode_item(blockIdx.x + i * gridDim.x, roff, ioff, E, p.n_tiles);
                 for (int ks = 0; ks < KT; ++ks, ++g) {
-                    const uint32_t slot = g % kActStages;
-                    if (!wait_bounded(&act_empty[slot], ((g / kActStages) & 1u) ^ 1u, abort_flag,
-                                      p.status, lim)) {
+                    const uint32_t slot = g % kSlots;
+                    if (!wait_bounded(&slot_empty[slot], ((g / kSlots) & 1u) ^ 1u, abort_flag,
+                                      p.status, lim, 128)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&act_full[slot], static_cast<uint32_t>(it.nt) * 256u);
-                    const uint32_t dst = act_smem + slot * kActStageBytes;
-                    for (int h = 0; h < 2; ++h)
-                        for (int grp = 0; grp < it.nt / 16; ++grp)
-                            tma_load_2d(dst + h * kActHalfBytes + grp * 2048, &tm_act,
-                                        ks * kKS + h * 64, it.row0 + grp * 16, &act_full[slot]);
+                    mbar_arrive_expect_tx(&act_full[slot], static_cast<uint32_t>(it.nt) * 128u);
+                    const uint32_t dst = act_smem + slot * act_stage_bytes;
+                    for (int grp = 0; grp < it.nt / 16; ++grp)
+                        tma_load_2d(dst + grp * 2048, &tm_act, ks * kStageK, it.row0 + grp * 16,
+                                    &act_full[slot]);
                 }
             }
             if (!ok) {
-                const uint32_t first = g > kActStages ? g - kActStages : 0;
+                const uint32_t first = g > kSlots ? g - kSlots : 0;
                 for (uint32_t h = first; h < g; ++h)
-                    wait_bounded(&act_full[h % kActStages], (h / kActStages) & 1u, nullptr,
-                                 p.status, lim);
+                    wait_bounded(&act_full[h % kSlots], (h / kSlots) & 1u, nullptr, p.status, lim);
             }
         }
-    } else if (warp == 1) {
-        // --------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            uint32_t g = 0;
+    } else if (warp == 1 || warp == 3) {
+        // ----------------------------------------------------------- MMA issuers
+        // Single mode: warp 1 issues every stage into one accumulator.  Split
+        // mode: warp 1 takes the even stages, warp 3 the odd ones; each stage's
+        // MMAs go into its warpgroup's K-partial accumulator.
+        const int issuer = warp == 1 ? 0 : 1;
+        if (lane == 0 && (split || issuer == 0)) {
+            const uint32_t step = split ? 2u : 1u;
+            int cur_item = -1;
+            Item it{};
             bool ok = true;
-            for (int i = 0; i < my_items && ok; ++i) {
-                const Item it = decode_item(blockIdx.x + i * gridDim.x, roff, ioff, E, p.n_tiles);
-                const uint32_t accslot = i & 1;
-                if (!wait_bounded(&acc_empty[accslot], ((i >> 1) & 1) ^ 1, abort_flag, p.status,
-                                  lim)) {
+            for (uint32_t g = split ? issuer : 0; g < total && ok; g += step) {
+                const int i = static_cast<int>(g / KT);
+                const int ks = static_cast<int>(g - static_cast<uint32_t>(i) * KT);
+                if (i != cur_item) {
+                    it = decode_item(blockIdx.x + i * gridDim.x, roff, ioff, E, p.n_tiles);
+                    cur_item = i;
+                }
+                const uint32_t buf = i & 1;
+                const int wg = ks & 3;
+                const bool first = split ? ks < kConvWG : ks == 0;
+                const bool last = split ? ks + kConvWG >= KT : ks == KT - 1;
+                if (first) {
+                    ok = wait_bounded(&acc_empty[buf], ((i >> 1) & 1) ^ 1, abort_flag, p.status, lim,
+                                      64);
+                    if (!ok) break;
+                }
+                const uint32_t slot = g % kSlots;
+                if (!wait_bounded(&a_full[slot], (g / kSlots) & 1u, abort_flag, p.status, lim, 32) ||
+                    !wait_bounded(&act_full[slot], (g / kSlots) & 1u, abort_flag, p.status, lim, 32)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
+                const uint32_t d_tmem = tmem_base + buf * kAccCols + (split ? wg * 32 : 0);
+                const uint32_t a_col = tmem_base + kACol0 + slot * kAColsPerSlot;
+                const uint64_t b0 = smem_desc_sw128(act_smem + slot * act_stage_bytes);
                 const uint32_t idesc = idesc_bf16_f32(128, it.nt);
-                const uint32_t d_tmem = tmem_base + accslot * kAccCols;
-                for (int ks = 0; ks < KT; ++ks, ++g) {
-                    const uint32_t aslot = g % kAStages;
-                    const uint32_t xslot = g % kActStages;
-                    if (!wait_bounded(&a_full[aslot], (g / kAStages) & 1u, abort_flag, p.status,
-                                      lim) ||
-                        !wait_bounded(&act_full[xslot], (g / kActStages) & 1u, abort_flag,
-                                      p.status, lim)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t a_col = tmem_base + kACol0 + aslot * kAColsPerStage;
-                    const uint32_t b_base = act_smem + xslot * kActStageBytes;
+                const uint32_t acc0 = first ? 0u : 1u;
 #pragma unroll
-                    for (int kk = 0; kk < kKS / 16; ++kk) {
-                        const uint64_t bdesc =
-                            smem_desc_sw128(b_base + (kk >> 2) * kActHalfBytes + (kk & 3) * 32);
-                        mma_bf16_ts(d_tmem, a_col + kk * 8, bdesc, idesc, (ks | kk) != 0);
-                    }
-                    mma_commit(&a_empty[aslot]);
-                    mma_commit(&act_empty[xslot]);
-                }
-                if (ok) mma_commit(&acc_full[accslot]);
+                for (int kk = 0; kk < kStageK / 16; ++kk)
+                    mma_bf16_ts(d_tmem, a_col + kk * 8, b0 + static_cast<uint64_t>(kk * 2), idesc,
+                                acc0 | static_cast<uint32_t>(kk));
+                mma_commit(&slot_empty[slot]);
+                if (last) mma_commit(&acc_full[buf]);
             }
             // All MMAs issued by this thread must finish before TMEM is freed.
-            mma_commit(final_bar);
-            wait_bounded(final_bar, 0, nullptr, p.status, lim);
+            mma_commit(&final_bar[issuer]);
+            wait_bounded(&final_bar[issuer], 0, nullptr, p.status, lim);
         }
-    } else if (warp >= 4 && warp < 12) {
+    } else if (warp >= 4 && warp < kEpiWarp0) {
         // ----------------------------------------------------------- converters
-        // Warpgroup wg handles the stages g with g % 2 == wg.  Thread `row` owns
-        // weight row n0 + row (TMEM lane row) and decodes its 128 codes of the
-        // stage into 64 bf16 pairs (reduction order of the K8 interleave).  For
-        // activations given in natural order the warpgroup also interleaves the
-        // stage's activation tile in shared memory before the MMA reads it.
+        // Warpgroup wg handles the stages g with g % 4 == wg.  Thread `row` owns
+        // weight row n0 + row (TMEM lane row) and decodes its 64 codes of the
+        // stage into 32 bf16 pairs (reduction order of the K8 interleave).  For
+        // activations given in natural order the warpgroup also interleaves
+        // the stage's activation tile in shared memory before the MMA reads it.
         const int wg = (warp - 4) >> 2;
         const int wtid = tid - 128 * (wg + 1);     // 0..127 within the warpgroup
-        const int q = warp & 3;                    // TMEM lane quarter
+        const int q = warp & 3;                    // TMEM lane quarter = warp within the group
         const int row = q * 32 + lane;
         const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-        const bool vec4 = p.scale_vec4 != 0;
-        const uint32_t total = static_cast<uint32_t>(my_items) * KT;
         int bad_scale = 0;
-        int pf_item = -1, cur_item = -1, cur_nt = 16;
+        int pf_item = -1, cur_item = -1;
+        Item cur{};
         const uint8_t *srow = nullptr;
-        // Scale bytes of this row for stage g (four 32-element blocks); the
+        // Scale bytes of this row for stage g (two 32-element blocks); the
         // row's scale pointer is looked up once per work item.
         auto load_scales = [&](uint32_t g) -> uint32_t {
             const int i = static_cast<int>(g / KT), ks = static_cast<int>(g - i * KT);
@@ -353,36 +364,33 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
                                : nullptr;
                 pf_item = i;
             }
-            if (!srow) return 0x7F7F7F7Fu;
-            if (vec4) return __ldg(reinterpret_cast<const uint32_t *>(srow + ks * 4));
-            uint32_t sw = 0;
-            for (int b = 0; b < 4; ++b) {
-                const int blk = ks * 4 + b;
-                sw |= (blk < p.scale_row ? static_cast<uint32_t>(__ldg(srow + blk)) : 127u) << (8 * b);
-            }
-            return sw;
+            const int blk = ks * 2;
+            if (!srow || blk >= p.scale_row) return 0x7F7Fu;       // beyond K: zero codes
+            if (p.scale_vec2) return __ldg(reinterpret_cast<const uint16_t *>(srow + blk));
+            const uint32_t s0 = __ldg(srow + blk);
+            const uint32_t s1 = blk + 1 < p.scale_row ? static_cast<uint32_t>(__ldg(srow + blk + 1)) : 127u;
+            return s0 | (s1 << 8);
         };
         uint32_t sw_next = wg < static_cast<int>(total) ? load_scales(wg) : 0u;
-        for (uint32_t g = wg; g < total; g += 2) {
+        for (uint32_t g = wg; g < total; g += kConvWG) {
             const uint32_t sw = sw_next;
-            if (g + 2 < total) sw_next = load_scales(g + 2);   // one stage ahead
-            if (!p.act_k8) {
-                const int i = static_cast<int>(g / KT);
-                if (i != cur_item) {
-                    cur_nt = decode_item(blockIdx.x + i * gridDim.x, roff, ioff, E, p.n_tiles).nt;
-                    cur_item = i;
-                }
+            if (g + kConvWG < total) sw_next = load_scales(g + kConvWG);   // one stage ahead
+            const int i = static_cast<int>(g / KT);
+            if (i != cur_item) {
+                cur = decode_item(blockIdx.x + i * gridDim.x, roff, ioff, E, p.n_tiles);
+                cur_item = i;
             }
-            const uint32_t cslot = g % kCodeStages;
-            if (!warp_wait_bounded(&code_full[cslot], (g / kCodeStages) & 1u, abort_flag, p.status,
-                                   lim))
+            const uint32_t cstage = g >> 2;         // this group's quarter of a code stage
+            const uint32_t cslot = cstage % CS;
+            if (!warp_wait_bounded(&code_full[cslot], (cstage / CS) & 1u, abort_flag, p.status, lim))
                 break;
-            // This row's 64 code bytes (4 chunks of 16, 64-byte swizzle).
-            uint32_t cw[4][4];
-            const uint8_t *crow = smem + kOffCode + cslot * kCodeStageBytes + row * 64;
+            // This row's 32 code bytes of the quarter (2 chunks of 16, 128-byte swizzle).
+            uint32_t cw[2][4];
+            const uint8_t *crow = smem + kOffCode + cslot * kCodeStageBytes + row * 128;
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
-                const uint4 v = *reinterpret_cast<const uint4 *>(crow + ((ch ^ ((row >> 1) & 3)) << 4));
+            for (int ch = 0; ch < 2; ++ch) {
+                const uint4 v = *reinterpret_cast<const uint4 *>(
+                    crow + (((2 * wg + ch) ^ (row & 7)) << 4));
                 cw[ch][0] = v.x;
                 cw[ch][1] = v.y;
                 cw[ch][2] = v.z;
@@ -390,53 +398,44 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&code_empty[cslot]);
+            const uint32_t slot = g % kSlots;
             if (!p.act_k8) {
                 // Interleave every 16-byte chunk of the stage's activation rows in
                 // place (the permutation stays inside a chunk, so the swizzle of
                 // the tile does not matter).
-                const uint32_t xslot = g % kActStages;
-                if (!warp_wait_bounded(&act_full[xslot], (g / kActStages) & 1u, abort_flag,
-                                       p.status, lim))
+                if (!warp_wait_bounded(&act_full[slot], (g / kSlots) & 1u, abort_flag, p.status, lim))
                     break;
-                uint8_t *abase = smem + kOffAct + xslot * kActStageBytes;
-                const int chunks = cur_nt * 8;          // per half: nt rows x 128 bytes
-                for (int c = wtid; c < 2 * chunks; c += 128) {
-                    const int h = c >= chunks;
-                    uint4 *ptr = reinterpret_cast<uint4 *>(abase + h * kActHalfBytes +
-                                                           (c - h * chunks) * 16);
-                    *ptr = interleave8(*ptr);
-                }
+                uint4 *abase = reinterpret_cast<uint4 *>(smem + act_off + slot * act_stage_bytes);
+                for (int c = wtid; c < cur.nt * 8; c += 128) abase[c] = interleave8(abase[c]);
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             }
             // Scale bytes 0..128 take one bf16 FMA, 129..252 two, 253..255 are
             // errors; the warp agrees on the path.
-            const bool any_big = __any_sync(0xffffffffu, __vcmpgtu4(sw, 0x80808080u) != 0);
-            const bool any_bad = __any_sync(0xffffffffu, __vcmpgtu4(sw, 0xFCFCFCFCu) != 0);
-            const uint32_t aslot = g % kAStages;
-            if (!warp_wait_bounded(&a_empty[aslot], ((g / kAStages) & 1u) ^ 1u, abort_flag, p.status,
-                                   lim))
-                break;
-            tc_fence_after();
-            const uint32_t a_addr = lane_base + kACol0 + aslot * kAColsPerStage;
-            uint32_t o[64];
+            const bool any_big = __any_sync(0xffffffffu, __vcmpgtu4(sw, 0x8080u) != 0);
+            const bool any_bad = __any_sync(0xffffffffu, __vcmpgtu4(sw, 0xFCFCu) != 0);
+            uint32_t o[32];
             if (!any_big && !any_bad) {
 #pragma unroll
-                for (int ch = 0; ch < 4; ++ch)
+                for (int ch = 0; ch < 2; ++ch)
                     decode32_single(cw[ch], scale_pair_single((sw >> (8 * ch)) & 0xFFu), &o[16 * ch]);
             } else {
 #pragma unroll
-                for (int ch = 0; ch < 4; ++ch)
+                for (int ch = 0; ch < 2; ++ch)
                     if (!decode32_any(cw[ch], (sw >> (8 * ch)) & 0xFFu, &o[16 * ch])) bad_scale = 1;
             }
+            if (!warp_wait_bounded(&slot_empty[slot], ((g / kSlots) & 1u) ^ 1u, abort_flag, p.status,
+                                   lim))
+                break;
+            tc_fence_after();
             __syncwarp();
-            tmem_st64(a_addr, o);
+            tmem_st32(lane_base + kACol0 + slot * kAColsPerSlot, o);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&a_full[aslot]);
+            if (lane == 0) mbar_arrive(&a_full[slot]);
         }
         if (bad_scale) set_status(p.status, MOE_ERR_DATA);
-    } else if (warp >= 12) {
+    } else if (warp >= kEpiWarp0) {
         // ------------------------------------------------------------- epilogue
         const int q = warp & 3;
         const int row = q * 32 + lane;
@@ -444,7 +443,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
         for (int i = 0; i < my_items; ++i) {
             const Item it = decode_item(blockIdx.x + i * gridDim.x, roff, ioff, E, p.n_tiles);
             const uint32_t accslot = i & 1;
-            if (!warp_wait_bounded(&acc_full[accslot], (i >> 1) & 1, abort_flag, p.status, lim))
+            if (!warp_wait_bounded(&acc_full[accslot], (i >> 1) & 1, abort_flag, p.status, lim, 128))
                 break;
             tc_fence_after();
             const int n = it.n0 + row;
@@ -452,7 +451,20 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
             for (int c = 0; c < it.nt / 16; ++c) {
                 uint32_t v[16];
                 __syncwarp();
-                tmem_ld16(lane_base + accslot * kAccCols + c * 16, v);
+                const uint32_t col = lane_base + accslot * kAccCols + c * 16;
+                tmem_ld16(col, v);
+                if (split) {
+                    // Partial sums of the four warpgroups' K stages, added in order.
+#pragma unroll
+                    for (int j = 1; j < kConvWG; ++j) {
+                        uint32_t u[16];
+                        tmem_ld16(col + 32 * j, u);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int t = 0; t < 16; ++t)
+                            v[t] = __float_as_uint(__uint_as_float(v[t]) + __uint_as_float(u[t]));
+                    }
+                }
                 tmem_ld_wait();
                 if (col_ok) {
 #pragma unroll
@@ -557,10 +569,10 @@ moe_status launch_grouped_gemm(const uint16_t *act, int rows, int K, const uint8
         cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2),
                               static_cast<cuuint64_t>(E) * static_cast<cuuint64_t>(N)};
         cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
-        cuuint32_t box[2] = {64, 128};
+        cuuint32_t box[2] = {128, 128};
         cuuint32_t estr[2] = {1, 1};
         if (encode(&tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(codes), dims,
-                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return MOE_ERR_CUDA;
@@ -576,12 +588,14 @@ moe_status launch_grouped_gemm(const uint16_t *act, int rows, int K, const uint8
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return MOE_ERR_CUDA;
     }
-    static bool attr_set = false;
-    if (!attr_set) {
+    static uint64_t attr_dev_mask = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (!(attr_dev_mask & (1ull << (dev & 63)))) {
         if (cudaFuncSetAttribute(grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kSmemBytes) != cudaSuccess)
             return MOE_ERR_CUDA;
-        attr_set = true;
+        attr_dev_mask |= 1ull << (dev & 63);
     }
     Params p;
     p.scales = scales;
@@ -594,9 +608,9 @@ moe_status launch_grouped_gemm(const uint16_t *act, int rows, int K, const uint8
     p.E = E;
     p.out_bf16 = out_bf16;
     p.n_tiles = (N + kBN - 1) / kBN;
-    p.k_stages = (K + kKS - 1) / kKS;
+    p.k_stages = 4 * ((K + kCodeK - 1) / kCodeK);
     p.scale_row = K / 32;
-    p.scale_vec4 = ((K / 32) % 4 == 0) && ((reinterpret_cast<uintptr_t>(scales) & 3) == 0);
+    p.scale_vec2 = ((K / 32) % 2 == 0) && ((reinterpret_cast<uintptr_t>(scales) & 1) == 0);
     p.wait_limit_ns = wait_limit_ns;
     p.act_k8 = act_k8;
     grouped_gemm_kernel<<<num_sms, kThreads, kSmemBytes, stream>>>(tm_codes, tm_act, p);

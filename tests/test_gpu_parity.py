@@ -149,21 +149,41 @@ def test_decode_flags_out_of_range_scale(B):
     assert torch.isnan(out[3, 32:].float()).all() and not torch.isnan(out[3, :32].float()).any()
 
 
-def test_gemm_identity_activations_expose_decoded_weights(B):
-    # act = I_K: out[k, n] = w[n, k] exactly, so the converter's decode is checked bit for bit.
+@pytest.mark.parametrize("scale_range", [(2, 128), (2, 252), (120, 135)],
+                         ids=["one_fma_path", "split_path", "path_boundary"])
+@pytest.mark.parametrize("k8", [False, True], ids=["row_major", "k8"])
+def test_gemm_identity_activations_expose_decoded_weights(B, scale_range, k8):
+    # act = I_K: out[k, n] = w[n, k] exactly, so the converter's decode is checked
+    # bit for bit inside the GEMM.  Scale bytes >= 2 keep every weight an f32
+    # normal number (subnormal products may be flushed by the tensor pipe; the
+    # decode entry point covers scale bytes 0 and 1 bit for bit).
     rng = np.random.default_rng(8)
     K, N = 256, 384
     codes = rng.integers(0, 256, (1, N, K // 2), dtype=np.uint8)
-    scales = rng.integers(0, 253, (1, N, K // 32), dtype=np.uint8)
-    scales[0, :, 0] = 0
-    scales[0, :, 1] = 1
-    scales[0, :, 2] = 252
+    scales = rng.integers(scale_range[0], scale_range[1] + 1, (1, N, K // 32), dtype=np.uint8)
     one = inputs.f32_to_bf16_bits(np.ones(1, np.float32))[0]
     act = np.zeros((K, K), np.uint16)
     act[np.arange(K), np.arange(K)] = one
-    out = _gemm_gpu(B, act, codes, scales, [K])
+    out = _gemm_gpu(B, act, codes, scales, [K], k8=k8)
     dec = inputs.bf16_bits_to_f32(oracle.decode_expert_bf16(codes, scales, 0))
     np.testing.assert_array_equal(out, dec.T)
+
+
+@pytest.mark.parametrize("scale_range", [(2, 128), (2, 252)], ids=["one_fma_path", "split_path"])
+def test_gemm_split_mode_exposes_decoded_weights(B, scale_range):
+    # 16 experts x 32 rows, K = 512: row r of expert e is one-hot at k = 32e + r, so
+    # out[row, n] = w_e[n, 32e + r] exactly; bands <= 32 rows select the split mode.
+    rng = np.random.default_rng(9)
+    E, K, N = 16, 512, 256
+    codes = rng.integers(0, 256, (E, N, K // 2), dtype=np.uint8)
+    scales = rng.integers(scale_range[0], scale_range[1] + 1, (E, N, K // 32), dtype=np.uint8)
+    one = inputs.f32_to_bf16_bits(np.ones(1, np.float32))[0]
+    act = np.zeros((E * 32, K), np.uint16)
+    act[np.arange(E * 32), np.arange(E * 32)] = one
+    out = _gemm_gpu(B, act, codes, scales, np.full(E, 32, np.int32))
+    for e in range(E):
+        dec = inputs.bf16_bits_to_f32(oracle.decode_expert_bf16(codes, scales, e))
+        np.testing.assert_array_equal(out[32 * e:32 * e + 32], dec[:, 32 * e:32 * e + 32].T)
 
 
 # ---------------------------------------------------------------- grouped GEMM
@@ -186,6 +206,12 @@ GEMM_CASES = {
     "few_rows": lambda: _explicit([3, 0, 2], 256, 128),
     "one_expert_long_band": lambda: _explicit([700], 256, 128),
     "many_items": lambda: _explicit(np.random.default_rng(3).integers(0, 40, 64), 512, 512),
+    # every band <= 32 rows: the split-accumulator mode
+    "split_small_bands": lambda: _explicit([0, 1, 7, 16, 0, 3, 32, 12, 17, 31], 1024, 384),
+    "split_k_tail_640": lambda: _explicit([5, 0, 16, 9], 640, 200),      # last 64-k stages all zero
+    "split_k_tail_544": lambda: _explicit([2, 11, 0, 30], 544, 136),     # K/32 = 17 scale bytes per row
+    "split_k_96": lambda: _explicit([3, 0, 8], 96, 128),                 # one partial code stage
+    "split_one_row_experts": lambda: _explicit(np.ones(40, np.int32), 2048, 256),
 }
 
 
