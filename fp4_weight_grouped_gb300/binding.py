@@ -13,7 +13,9 @@ import torch
 
 from . import build_lib
 
-MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_DATA, MOE_ERR_TIMEOUT = range(6)
+(MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_DATA, MOE_ERR_TIMEOUT,
+ MOE_ERR_CAPACITY) = range(7)
+MOE_ROUTE_SORT_NOALLOC_SCRATCH_BYTES = 512 * 1024
 MOE_F32, MOE_BF16 = 0, 1
 MOE_ACT_ROW_MAJOR, MOE_ACT_K8_INTERLEAVED = 0, 1
 
@@ -21,6 +23,7 @@ SYMBOLS = (
     "moe_status_string", "moe_workspace_bytes", "moe_clear_status", "moe_read_status",
     "moe_route_sort", "moe_mxfp4_grouped_gemm", "moe_swiglu", "moe_combine", "moe_layer_forward",
     "moe_mxfp4_decode_expert", "moe_debug_bounded_wait", "moe_last_launch_count",
+    "moe_route_sort_noalloc",
 )
 
 _lock = threading.Lock()
@@ -53,6 +56,8 @@ def load(path: str | None = None):
                 "moe_clear_status": ([P, P], C.c_int),
                 "moe_read_status": ([P, P], C.c_int),
                 "moe_route_sort": ([P, I32, I32, I32, P, P, P, P, P, I32, P, C.c_int, P, SZ, P], C.c_int),
+                "moe_route_sort_noalloc": ([P, I32, I32, I32, P, P, P, P, P, I32, P, C.c_int, P],
+                                           C.c_int),
                 "moe_mxfp4_grouped_gemm": ([P, C.c_int, I64, I32, P, P, P, I32, I32, P, C.c_int, P, SZ,
                                             P], C.c_int),
                 "moe_swiglu": ([P, C.c_int, I64, I32, P, C.c_int, P], C.c_int),
@@ -150,6 +155,24 @@ def route_sort(topk_ids: torch.Tensor, E: int, x: torch.Tensor | None = None,
                                workspace.numel(), _stream(stream))
     _check(rc, "moe_route_sort")
     return gs, off, ss, s2r, xs
+
+
+def route_sort_noalloc(topk_ids: torch.Tensor, E: int, out, x: torch.Tensor | None = None,
+                       stream=None, x_layout: int = MOE_ACT_ROW_MAJOR):
+    """Route sort through the fixed-capacity entry point, for callers that must
+    not allocate at the point of the call.  `out` = (group_sizes, group_offsets,
+    sorted_slot, slot_to_row, x_sorted or None) must already exist: this wrapper
+    creates no tensor, and the library call uses its own static scratch instead
+    of a workspace.  Raises MoeError(MOE_ERR_CAPACITY) when the problem needs
+    more than MOE_ROUTE_SORT_NOALLOC_SCRATCH_BYTES of scratch."""
+    T, k = topk_ids.shape
+    gs, off, ss, s2r, xs = out
+    hidden = 0 if x is None else x.shape[1]
+    rc = load().moe_route_sort_noalloc(_ptr(topk_ids), T, k, E, _ptr(gs), _ptr(off), _ptr(ss),
+                                       _ptr(s2r), _ptr(x), hidden, _ptr(xs), x_layout,
+                                       _stream(stream))
+    _check(rc, "moe_route_sort_noalloc")
+    return out
 
 
 def grouped_gemm(act: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor,

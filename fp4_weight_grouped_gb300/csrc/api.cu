@@ -93,6 +93,7 @@ const char *moe_status_string(moe_status s) {
         case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
         case MOE_ERR_DATA: return "MOE_ERR_DATA";
         case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+        case MOE_ERR_CAPACITY: return "MOE_ERR_CAPACITY";
     }
     return "MOE_ERR_UNKNOWN";
 }
@@ -139,6 +140,35 @@ moe_status moe_route_sort(const int32_t *topk_ids, int32_t T, int32_t k, int32_t
                                 static_cast<uint8_t *>(workspace) + kStatusBytes,
                                 status_word(workspace), static_cast<cudaStream_t>(stream),
                                 &launches);
+    g_last_launches = launches;
+    return st;
+}
+
+moe_status moe_route_sort_noalloc(const int32_t *topk_ids, int32_t T, int32_t k, int32_t E,
+                                  int32_t *group_sizes, int32_t *group_offsets,
+                                  int32_t *sorted_slot, int32_t *slot_to_row, const uint16_t *x,
+                                  int32_t hidden, uint16_t *x_sorted,
+                                  moe_act_layout x_sorted_layout, void *stream) {
+    // The checks of moe_route_sort that do not concern the workspace.
+    if (T < 0 || E <= 0 || E > kMaxE || k <= 0 || k > E) return MOE_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(T) * k > INT32_MAX) return MOE_ERR_INVALID_ARG;
+    if (!group_sizes || !group_offsets) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!topk_ids || !sorted_slot || !slot_to_row)) return MOE_ERR_INVALID_ARG;
+    if ((x == nullptr) != (x_sorted == nullptr)) return MOE_ERR_INVALID_ARG;
+    if (x_sorted_layout != MOE_ACT_ROW_MAJOR && x_sorted_layout != MOE_ACT_K8_INTERLEAVED)
+        return MOE_ERR_INVALID_ARG;
+    if (x && (hidden <= 0 || hidden % 8 != 0 || !aligned(x, 16) || !aligned(x_sorted, 16)))
+        return MOE_ERR_INVALID_ARG;
+    if (moe::route_sort_scratch_bytes(T, k, E) > MOE_ROUTE_SORT_NOALLOC_SCRATCH_BYTES)
+        return MOE_ERR_CAPACITY;
+    int sms = 0;
+    moe_status st = current_device(&sms);
+    if (st != MOE_OK) return st;
+    int launches = 0;
+    st = moe::launch_route_sort_noalloc(topk_ids, T, k, E, group_sizes, group_offsets,
+                                        sorted_slot, slot_to_row, x, hidden, x_sorted,
+                                        x_sorted_layout == MOE_ACT_K8_INTERLEAVED,
+                                        static_cast<cudaStream_t>(stream), &launches);
     g_last_launches = launches;
     return st;
 }

@@ -17,6 +17,12 @@ moe_status launch_route_sort(const int32_t *ids, int T, int k, int E, int32_t *g
                              const uint16_t *x, int hidden, uint16_t *x_sorted, int x_k8,
                              void *scratch, int *status, cudaStream_t stream, int *launches);
 
+moe_status launch_route_sort_noalloc(const int32_t *ids, int T, int k, int E,
+                                     int32_t *group_sizes, int32_t *offsets,
+                                     int32_t *sorted_slot, int32_t *slot_to_row,
+                                     const uint16_t *x, int hidden, uint16_t *x_sorted, int x_k8,
+                                     cudaStream_t stream, int *launches);
+
 moe_status launch_grouped_gemm(const uint16_t *act, int rows, int K, const uint8_t *codes,
                                const uint8_t *scales, const int32_t *group_sizes, int E, int N,
                                void *out, int out_bf16, int act_k8, int *status,

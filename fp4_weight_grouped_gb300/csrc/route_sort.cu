@@ -18,6 +18,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "device_common.cuh"
 #include "launch.h"
 #include "mxfp4_decode.cuh"
@@ -192,6 +194,53 @@ moe_status launch_route_sort(const int32_t *ids, int T, int k, int E, int32_t *g
         ++*launches;
     }
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------
+// Fixed-capacity variant: the same three kernels with their scratch in static
+// device storage, for callers that cannot allocate or pass a workspace at the
+// point of the call.  Layout of the array: the status word in the first 256
+// bytes, then the scratch exactly as launch_route_sort lays it out.  The
+// chunk totals and ranks are written in full before they are read; only the
+// status word needs clearing, which every call does on its stream.
+
+constexpr size_t kNoAllocStatusBytes = 256;
+
+static __device__ __align__(256) uint8_t
+    noalloc_area[kNoAllocStatusBytes + MOE_ROUTE_SORT_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex noalloc_mutex;
+void *noalloc_base[kMaxDevices];   // device address of noalloc_area, per device
+}  // namespace
+
+moe_status launch_route_sort_noalloc(const int32_t *ids, int T, int k, int E,
+                                     int32_t *group_sizes, int32_t *offsets,
+                                     int32_t *sorted_slot, int32_t *slot_to_row,
+                                     const uint16_t *x, int hidden, uint16_t *x_sorted, int x_k8,
+                                     cudaStream_t stream, int *launches) {
+    *launches = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+    void *base = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(noalloc_mutex);
+        if (!noalloc_base[dev]) {
+            // The device is current; the address is valid for this device only.
+            if (cudaGetSymbolAddress(&noalloc_base[dev], noalloc_area) != cudaSuccess) {
+                noalloc_base[dev] = nullptr;
+                return MOE_ERR_CUDA;
+            }
+        }
+        base = noalloc_base[dev];
+    }
+    int *status = static_cast<int *>(base);
+    if (cudaMemsetAsync(status, 0, sizeof(int), stream) != cudaSuccess) return MOE_ERR_CUDA;
+    return launch_route_sort(ids, T, k, E, group_sizes, offsets, sorted_slot, slot_to_row, x,
+                             hidden, x_sorted, x_k8,
+                             static_cast<uint8_t *>(base) + kNoAllocStatusBytes, status, stream,
+                             launches);
 }
 
 }  // namespace moe

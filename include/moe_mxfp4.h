@@ -21,7 +21,8 @@
  * Conventions for every call:
  *  - Pointers named as device buffers must be device memory of the current
  *    CUDA device; the caller owns all of them.  The library allocates nothing
- *    and keeps no state between calls.
+ *    and keeps no state between calls, apart from the fixed scratch array of
+ *    moe_route_sort_noalloc.
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *    Every call only enqueues work on it and returns; results are ready when
  *    the stream reaches that point.
@@ -58,7 +59,9 @@ typedef enum {
     MOE_ERR_CUDA = 3,        /* a CUDA runtime/driver call or launch failed */
     MOE_ERR_DATA = 4,        /* device-side: id out of range, sum(group_sizes) != rows,
                                 negative group size, or scale byte > 252 */
-    MOE_ERR_TIMEOUT = 5      /* device-side: a pipeline wait exceeded its bound */
+    MOE_ERR_TIMEOUT = 5,     /* device-side: a pipeline wait exceeded its bound */
+    MOE_ERR_CAPACITY = 6     /* host check: the problem needs more scratch than a
+                                fixed-capacity entry point holds */
 } moe_status;
 
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
@@ -115,6 +118,58 @@ MOE_API moe_status moe_route_sort(const int32_t *topk_ids, int32_t T, int32_t k,
                           int32_t *slot_to_row, const uint16_t *x, int32_t hidden,
                           uint16_t *x_sorted, moe_act_layout x_sorted_layout, void *workspace,
                           size_t workspace_bytes, void *stream);
+
+/* Size of the fixed scratch array behind moe_route_sort_noalloc (512 KiB). */
+#define MOE_ROUTE_SORT_NOALLOC_SCRATCH_BYTES (512u * 1024u)
+
+/*
+ * moe_route_sort_noalloc — moe_route_sort for callers that cannot supply a
+ * workspace.  The pages have no counterpart of this call; it is an addition of
+ * this library.
+ *
+ * Who needs it: a caller that must not allocate device memory at the point of
+ * the call.  Examples are a token-by-token decode loop, where cudaMalloc or
+ * cudaFree (directly, or inside a framework's caching allocator when its pool
+ * runs dry) may synchronise the device and stall every stream, and an operator
+ * with a fixed signature that has no argument through which a scratch buffer
+ * could be passed.  This call therefore allocates nothing: no cudaMalloc, no
+ * cudaFree, no allocating call into CUDA libraries or into torch.  The counting
+ * sort's scratch (per-chunk expert totals and per-slot ranks) and its status
+ * word sit in one array of static device storage inside the library, one copy
+ * per device.
+ *
+ * Arguments are those of moe_route_sort without workspace and workspace_bytes,
+ * and the results are identical to it on the same inputs.
+ *
+ * Capacity: the array holds MOE_ROUTE_SORT_NOALLOC_SCRATCH_BYTES of scratch.
+ * When moe_workspace_bytes(T, k, E) - 256 exceeds it, the call returns
+ * MOE_ERR_CAPACITY and enqueues nothing.  For scale: T*k = 65536 routed slots
+ * with E = 256 need 320 KiB.
+ *
+ * First call: on each device, the first call looks up the device address of
+ * the array (cudaGetSymbolAddress, with that device current) and sets a kernel
+ * attribute; the lookup may make the driver load the library's device code.
+ * Make one call on every device before any stream capture begins.
+ *
+ * Overlap: every call on a device shares the one array.  Two calls whose kernels
+ * can run at the same time (streams with no ordering between them, or host
+ * threads launching concurrently) race on it and produce wrong results; the
+ * caller must order them, e.g. by issuing them on one stream.
+ *
+ * Zeroing: the chunk totals and ranks are written in full before they are
+ * read, so they need no clearing.  The status word must start at zero; each
+ * call clears it with a stream-ordered cudaMemsetAsync before its kernels.
+ *
+ * Errors: host checks as in moe_route_sort, then the capacity check.  No
+ * status word is exposed: a slot whose id lies outside [0, E) is left out of
+ * every band, so group_offsets[E] < T*k tells the caller that it happened.
+ */
+MOE_API moe_status moe_route_sort_noalloc(const int32_t *topk_ids, int32_t T, int32_t k,
+                                          int32_t E, int32_t *group_sizes,
+                                          int32_t *group_offsets, int32_t *sorted_slot,
+                                          int32_t *slot_to_row, const uint16_t *x,
+                                          int32_t hidden, uint16_t *x_sorted,
+                                          moe_act_layout x_sorted_layout, void *stream);
 
 /*
  * moe_mxfp4_grouped_gemm — W4A16 grouped matmul over expert row bands ([TPU]
