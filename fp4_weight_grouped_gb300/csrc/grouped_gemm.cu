@@ -45,35 +45,42 @@
 namespace moe {
 namespace gemm {
 
-constexpr int kThreads = 768;                 // 24 warps
-constexpr int kConvWG = 4;                    // converter warpgroups (warps 4..19)
-constexpr int kEpiWarp0 = 4 + 4 * kConvWG;    // epilogue warps 20..23
+constexpr int kIssuerWarps = 4;               // warps 0..3: MMA issuers (lane 0)
+constexpr int kConvWG = 4;                    // converter warpgroups: warps 4..19
+constexpr int kConvWarp0 = kIssuerWarps;
+constexpr int kCodeWarp = kConvWarp0 + 4 * kConvWG;   // warp 20: code producer
+constexpr int kActWarp = kCodeWarp + 1;               // warp 21: activation producer
+constexpr int kThreads = 32 * (kActWarp + 1);         // 704
 constexpr int kBN = 128;                      // output columns per tile (MMA M)
 constexpr int kMaxNT = 128;                   // tokens per work item (MMA N)
 constexpr int kStageK = 64;                   // K per decode / MMA stage
 constexpr int kSlots = 8;                     // A slots in TMEM (+ activation slots in smem)
 constexpr int kCodeK = 256;                   // K per code stage (4 decode stages)
 constexpr int kCodeStageBytes = kBN * kCodeK / 2;         // 16 KB
-constexpr int kCodeStagesMax = 8;
-constexpr int kRingBytes = 192 * 1024;        // code ring + activation slots
+constexpr int kCodeStagesMax = 12;
+constexpr int kRingBytes = 216 * 1024;        // code ring + activation tiles
 constexpr int kTmemCols = 512;
 constexpr int kAccCols = 128;                 // per accumulator buffer
 constexpr int kACol0 = 2 * kAccCols;          // A slots after the two accumulator buffers
 constexpr int kAColsPerSlot = kStageK / 2;    // bf16 pairs: 32 columns
+constexpr int kPartCols = 32;                 // split mode: columns of one K-partial
 constexpr int kMaxE = 1024;
 
 constexpr int kOffCode = 0;
 constexpr int kOffRowOff = kOffCode + kRingBytes;
 constexpr int kOffItemOff = kOffRowOff + (kMaxE + 1) * 4;
 constexpr int kOffBars = (kOffItemOff + (kMaxE + 1) * 4 + 7) & ~7;
-constexpr int kNumBars = 2 * kCodeStagesMax + 3 * kSlots + 2 * 2 + 2;
+constexpr int kNumBars = 2 * kCodeStagesMax + 3 * kSlots + 2 * 2 + kIssuerWarps;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 64 + 1024;          // + alignment slack
 
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kCodeStageBytes % 1024 == 0, "ring slots keep the 1024-byte swizzle alignment");
 static_assert(kOffBars % 8 == 0, "barrier alignment");
 static_assert(kACol0 + kSlots * kAColsPerSlot <= kTmemCols, "TMEM budget");
-static_assert(kSlots % kConvWG == 0, "each slot belongs to one warpgroup");
+static_assert(kSlots == 2 * kConvWG, "each warpgroup alternates between two A slots");
+static_assert(kConvWG * kPartCols <= kAccCols, "split-mode partials fit one buffer");
+static_assert(kCodeK / kStageK == kConvWG, "one code stage = one decode stage per warpgroup");
 
 struct Params {
     const uint8_t *scales;
@@ -115,6 +122,60 @@ __device__ __forceinline__ Item decode_item(int j, const int *roff, const int *i
     return it;
 }
 
+// Position in a ring of `n` mbarrier-guarded slots: slot index and the parity
+// of the phase the current use waits for.  Advancing flips the parity on wrap.
+struct Ring {
+    uint32_t slot = 0, phase = 0;
+    __device__ __forceinline__ void next(uint32_t n) {
+        if (++slot == n) {
+            slot = 0;
+            phase ^= 1u;
+        }
+    }
+};
+
+// Epilogue of one work item for converter warpgroup `wg`: the warpgroup writes
+// its quarter of the item's token columns.  In split mode the four K-partials
+// are added in warpgroup order (deterministic); f32 or bf16 output.
+__device__ __forceinline__ void store_item(const Params &p, const Item &it, uint32_t acc_base,
+                                           int wg, int row, bool split) {
+    const int n = it.n0 + row;
+    const int qc = it.nt >> 2;                 // columns per warpgroup (multiple of 4)
+    for (int c = wg * qc; c < (wg + 1) * qc; c += 4) {
+        uint32_t v[4];
+        __syncwarp();
+        tmem_ld4(acc_base + c, v);
+        if (split) {
+            uint32_t u1[4], u2[4], u3[4];
+            tmem_ld4(acc_base + kPartCols + c, u1);
+            tmem_ld4(acc_base + 2 * kPartCols + c, u2);
+            tmem_ld4(acc_base + 3 * kPartCols + c, u3);
+            tmem_ld_wait();
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+                v[t] = __float_as_uint(((__uint_as_float(v[t]) + __uint_as_float(u1[t])) +
+                                        __uint_as_float(u2[t])) +
+                                       __uint_as_float(u3[t]));
+        } else {
+            tmem_ld_wait();
+        }
+        if (n < p.N) {
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const int tok = c + t;
+                if (tok < it.nvalid) {
+                    const size_t off = static_cast<size_t>(it.row0 + tok) * p.N + n;
+                    if (p.out_bf16)
+                        reinterpret_cast<__nv_bfloat16 *>(p.out)[off] =
+                            __float2bfloat16_rn(__uint_as_float(v[t]));
+                    else
+                        reinterpret_cast<float *>(p.out)[off] = __uint_as_float(v[t]);
+                }
+            }
+        }
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
                     const __grid_constant__ CUtensorMap tm_act, const Params p) {
@@ -124,13 +185,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
     int *roff = reinterpret_cast<int *>(smem + kOffRowOff);
     int *ioff = reinterpret_cast<int *>(smem + kOffItemOff);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBars);
-    uint64_t *code_full = bars;
-    uint64_t *code_empty = code_full + kCodeStagesMax;
-    uint64_t *a_full = code_empty + kCodeStagesMax;     // converters -> issuer (4 warps)
+    uint64_t *code_full = bars;                          // TMA -> converters (+ issuers, split)
+    uint64_t *code_empty = code_full + kCodeStagesMax;   // 16 converter warps (+ 4 commits, split)
+    uint64_t *a_full = code_empty + kCodeStagesMax;      // converters -> issuer (4 warps)
     uint64_t *act_full = a_full + kSlots;                // TMA -> issuer
     uint64_t *slot_empty = act_full + kSlots;            // MMA commit -> converters, act producer
-    uint64_t *acc_full = slot_empty + kSlots;
-    uint64_t *acc_empty = acc_full + 2;
+    uint64_t *acc_full = slot_empty + kSlots;            // MMA commits -> epilogue
+    uint64_t *acc_empty = acc_full + 2;                  // epilogue (16 warps) -> issuers
     uint64_t *final_bar = acc_empty + 2;                 // one per issuer thread
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 8);
@@ -195,22 +256,29 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
     const int total_items = ioff[E];
     if (static_cast<int>(blockIdx.x) >= total_items) return;
     const int my_items = (total_items - static_cast<int>(blockIdx.x) + gridDim.x - 1) / gridDim.x;
-    const int KT = p.k_stages;
-    const uint32_t total = static_cast<uint32_t>(my_items) * KT;   // decode stages of this CTA
-    // Split mode: every band <= 32 rows.  Activation slots are sized for the
-    // widest band; the code ring takes the rest of the 192 KB (at most 8).
+    const int KT = p.k_stages;                  // multiple of 4
+    // Split mode: every band <= 32 rows.  Four issuers, one per converter
+    // warpgroup, each accumulating its warpgroup's stages into its own
+    // K-partial.  The activation tile of a code stage (the band's rows x 256 k,
+    // four 64-k boxes) travels in the same ring slot as the codes, so it is
+    // fetched as far ahead as the codes; a slot is free again once the 16
+    // converter warps have read the codes and the 4 issuers' MMAs are done.
+    // Single mode (wider bands): the code ring holds codes only and the
+    // activations use eight 64-k slots of their own, released with the A
+    // slot of the same stage.
     const int nt_max = *nt_max_slot;
-    const bool split = nt_max <= 32;
-    const uint32_t act_stage_bytes = static_cast<uint32_t>(nt_max) * 128u;
+    const bool split = nt_max <= kPartCols;
+    const uint32_t act_stage_bytes = static_cast<uint32_t>(nt_max) * 128u;   // one 64-k box
+    const uint32_t ring_stage_bytes = kCodeStageBytes + (split ? 4u * act_stage_bytes : 0u);
     const uint32_t CS = min(static_cast<uint32_t>(kCodeStagesMax),
-                            (kRingBytes - kSlots * act_stage_bytes) / kCodeStageBytes);
-    const uint32_t act_off = CS * kCodeStageBytes;
+                            (kRingBytes - (split ? 0u : kSlots * act_stage_bytes)) / ring_stage_bytes);
+    const uint32_t act_off = CS * ring_stage_bytes;     // single mode: activation slots
 
-    if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+    if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
     if (tid == 0) {
         for (uint32_t i = 0; i < CS; ++i) {
             mbar_init(&code_full[i], 1);
-            mbar_init(&code_empty[i], 4 * kConvWG);
+            mbar_init(&code_empty[i], 4 * kConvWG + (split ? kIssuerWarps : 0));
         }
         for (int i = 0; i < kSlots; ++i) {
             mbar_init(&a_full[i], 4);
@@ -218,10 +286,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
             mbar_init(&slot_empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&acc_full[i], split ? kConvWG : 1);
-            mbar_init(&acc_empty[i], 4);
+            mbar_init(&acc_full[i], split ? kIssuerWarps : 1);
+            mbar_init(&acc_empty[i], 4 * kConvWG);
         }
-        for (int i = 0; i < 2; ++i) mbar_init(&final_bar[i], 1);
+        for (int i = 0; i < kIssuerWarps; ++i) mbar_init(&final_bar[i], 1);
         mbar_fence_init();
     }
     tc_fence_before();
@@ -232,267 +300,277 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
     const uint32_t act_smem = smem_u32(smem + act_off);
     const uint64_t lim = p.wait_limit_ns;
 
-    if (warp == 0) {
-        // ------------------------------------------------------ code producer
-        if (lane == 0) {
-            tma_prefetch_map(&tm_codes);
-            uint32_t c = 0;
-            bool ok = true;
-            for (int i = 0; i < my_items && ok; ++i) {
-                const Item it = decode_item(blockIdx.x + i * gridDim.x, roff, ioff, E, p.n_tiles);
-                const int y = it.e * p.N + it.n0;
-                for (int kc = 0; kc < KT / 4; ++kc, ++c) {
-                    const uint32_t slot = c % CS;
-                    if (!wait_bounded(&code_empty[slot], ((c / CS) & 1u) ^ 1u, abort_flag, p.status,
-                                      lim, 128)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(&code_full[slot], kCodeStageBytes);
-                    tma_load_2d(code_smem + slot * kCodeStageBytes, &tm_codes, kc * 128, y,
-                                &code_full[slot]);
-                }
-            }
-            if (!ok) {   // drain: every issued copy must land before the CTA exits
-                const uint32_t first = c > CS ? c - CS : 0;
-                for (uint32_t h = first; h < c; ++h)
-                    wait_bounded(&code_full[h % CS], (h / CS) & 1u, nullptr, p.status, lim);
-            }
-        }
-    } else if (warp == 2) {
-        // ---------------------------------------------------- activation producer
-        if (lane == 0) {
-            tma_prefetch_map(&tm_act);
-            uint32_t g = 0;
-            bool ok = true;
-            for (int i = 0; i < my_items && ok; ++i) {
-                const Item it = decode_item(blockIdx.x + i * gridDim.x, roff, ioff, E, p.n_tiles);
-                for (int ks = 0; ks < KT; ++ks, ++g) {
-                    const uint32_t slot = g % kSlots;
-                    if (!wait_bounded(&slot_empty[slot], ((g / kSlots) & 1u) ^ 1u, abort_flag,
-                                      p.status, lim, 128)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(&act_full[slot], static_cast<uint32_t>(it.nt) * 128u);
-                    const uint32_t dst = act_smem + slot * act_stage_bytes;
-                    for (int grp = 0; grp < it.nt / 16; ++grp)
-                        tma_load_2d(dst + grp * 2048, &tm_act, ks * kStageK, it.row0 + grp * 16,
-                                    &act_full[slot]);
-                }
-            }
-            if (!ok) {
-                const uint32_t first = g > kSlots ? g - kSlots : 0;
-                for (uint32_t h = first; h < g; ++h)
-                    wait_bounded(&act_full[h % kSlots], (h / kSlots) & 1u, nullptr, p.status, lim);
-            }
-        }
-    } else if (warp == 1 || warp == 3) {
+    if (warp < kIssuerWarps) {
         // ----------------------------------------------------------- MMA issuers
-        // Single mode: warp 1 issues every stage into one accumulator.  Split
-        // mode: warp 1 takes the even stages, warp 3 the odd ones; each stage's
-        // MMAs go into its warpgroup's K-partial accumulator.
-        const int issuer = warp == 1 ? 0 : 1;
-        if (lane == 0 && (split || issuer == 0)) {
-            const uint32_t step = split ? 2u : 1u;
-            int cur_item = -1;
-            Item it{};
+        // Split mode: issuer w issues the stages of converter warpgroup w
+        // (every 4th stage) into K-partial w.  Single mode: issuer 0 issues
+        // every stage into one accumulator.
+        const int w = warp;
+        if (lane == 0 && (split || w == 0)) {
+            const uint32_t step = split ? kConvWG : 1u;
+            uint32_t g = split ? w : 0;       // global stage index of this CTA
+            int ks = static_cast<int>(g);     // stage within the item
+            Item it = decode_item(blockIdx.x, roff, ioff, E, p.n_tiles);
+            uint32_t idesc = idesc_bf16_f32(128, it.nt);
+            Ring ring;                        // split mode: code stage of this issuer's stage
             bool ok = true;
-            for (uint32_t g = split ? issuer : 0; g < total && ok; g += step) {
-                const int i = static_cast<int>(g / KT);
-                const int ks = static_cast<int>(g - static_cast<uint32_t>(i) * KT);
-                if (i != cur_item) {
-                    it = decode_item(blockIdx.x + i * gridDim.x, roff, ioff, E, p.n_tiles);
-                    cur_item = i;
-                }
+            for (int i = 0; i < my_items && ok;) {
                 const uint32_t buf = i & 1;
-                const int wg = ks & 3;
-                const bool first = split ? ks < kConvWG : ks == 0;
-                const bool last = split ? ks + kConvWG >= KT : ks == KT - 1;
-                if (first) {
-                    ok = wait_bounded(&acc_empty[buf], ((i >> 1) & 1) ^ 1, abort_flag, p.status, lim,
-                                      64);
-                    if (!ok) break;
+                if (ks < static_cast<int>(step)) {      // first stage of the item
+                    if (!wait_bounded(&acc_empty[buf], ((i >> 1) & 1) ^ 1, abort_flag, p.status,
+                                      lim, 64)) {
+                        ok = false;
+                        break;
+                    }
                 }
-                const uint32_t slot = g % kSlots;
-                if (!wait_bounded(&a_full[slot], (g / kSlots) & 1u, abort_flag, p.status, lim, 32) ||
-                    !wait_bounded(&act_full[slot], (g / kSlots) & 1u, abort_flag, p.status, lim, 32)) {
+                const uint32_t slot = g & (kSlots - 1), par = (g / kSlots) & 1u;
+                if (!wait_bounded(&a_full[slot], par, abort_flag, p.status, lim, 32) ||
+                    !(split ? wait_bounded(&code_full[ring.slot], ring.phase, abort_flag, p.status,
+                                           lim, 32)
+                            : wait_bounded(&act_full[slot], par, abort_flag, p.status, lim, 32))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + buf * kAccCols + (split ? wg * 32 : 0);
+                const uint32_t d_tmem = tmem_base + buf * kAccCols + (split ? w * kPartCols : 0);
                 const uint32_t a_col = tmem_base + kACol0 + slot * kAColsPerSlot;
-                const uint64_t b0 = smem_desc_sw128(act_smem + slot * act_stage_bytes);
-                const uint32_t idesc = idesc_bf16_f32(128, it.nt);
-                const uint32_t acc0 = first ? 0u : 1u;
+                const uint64_t b0 = smem_desc_sw128(
+                    split ? code_smem + ring.slot * ring_stage_bytes + kCodeStageBytes +
+                                w * act_stage_bytes
+                          : act_smem + slot * act_stage_bytes);
+                const uint32_t acc0 = ks < static_cast<int>(step) ? 0u : 1u;
 #pragma unroll
                 for (int kk = 0; kk < kStageK / 16; ++kk)
                     mma_bf16_ts(d_tmem, a_col + kk * 8, b0 + static_cast<uint64_t>(kk * 2), idesc,
                                 acc0 | static_cast<uint32_t>(kk));
                 mma_commit(&slot_empty[slot]);
-                if (last) mma_commit(&acc_full[buf]);
+                if (split) {
+                    mma_commit(&code_empty[ring.slot]);
+                    ring.next(CS);
+                }
+                g += step;
+                ks += static_cast<int>(step);
+                if (ks >= KT) {                         // last stage of the item
+                    mma_commit(&acc_full[buf]);
+                    ks -= KT;
+                    if (++i < my_items) {
+                        it = decode_item(blockIdx.x + i * gridDim.x, roff, ioff, E, p.n_tiles);
+                        idesc = idesc_bf16_f32(128, it.nt);
+                    }
+                }
             }
             // All MMAs issued by this thread must finish before TMEM is freed.
-            mma_commit(&final_bar[issuer]);
-            wait_bounded(&final_bar[issuer], 0, nullptr, p.status, lim);
+            mma_commit(&final_bar[w]);
+            wait_bounded(&final_bar[w], 0, nullptr, p.status, lim);
         }
-    } else if (warp >= 4 && warp < kEpiWarp0) {
-        // ----------------------------------------------------------- converters
-        // Warpgroup wg handles the stages g with g % 4 == wg.  Thread `row` owns
-        // weight row n0 + row (TMEM lane row) and decodes its 64 codes of the
-        // stage into 32 bf16 pairs (reduction order of the K8 interleave).  For
-        // activations given in natural order the warpgroup also interleaves
-        // the stage's activation tile in shared memory before the MMA reads it.
-        const int wg = (warp - 4) >> 2;
-        const int wtid = tid - 128 * (wg + 1);     // 0..127 within the warpgroup
+    } else if (warp == kCodeWarp) {
+        // ------------------------------------------------------ code producer
+        if (lane == 0) {
+            tma_prefetch_map(&tm_codes);
+            Ring r;
+            uint32_t issued = 0;
+            bool ok = true;
+            for (int i = 0; i < my_items && ok; ++i) {
+                const Item it = decode_item(blockIdx.x + i * gridDim.x, roff, ioff, E, p.n_tiles);
+                const int y = it.e * p.N + it.n0;
+                for (int kc = 0; kc < KT / 4; ++kc, r.next(CS), ++issued) {
+                    if (!wait_bounded(&code_empty[r.slot], r.phase ^ 1u, abort_flag, p.status, lim,
+                                      128)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t dst = code_smem + r.slot * ring_stage_bytes;
+                    mbar_arrive_expect_tx(&code_full[r.slot],
+                                          kCodeStageBytes + (split ? it.nt * 512u : 0u));
+                    tma_load_2d(dst, &tm_codes, kc * 128, y, &code_full[r.slot]);
+                    if (split) {
+                        for (int sub = 0; sub < 4; ++sub)
+                            for (int grp = 0; grp < it.nt / 16; ++grp)
+                                tma_load_2d(dst + kCodeStageBytes + sub * act_stage_bytes +
+                                                grp * 2048,
+                                            &tm_act, kc * kCodeK + sub * kStageK,
+                                            it.row0 + grp * 16, &code_full[r.slot]);
+                    }
+                }
+            }
+            if (!ok) {   // drain: every issued copy must land before the CTA exits
+                const uint32_t first = issued > CS ? issued - CS : 0;
+                for (uint32_t h = first; h < issued; ++h)
+                    wait_bounded(&code_full[h % CS], (h / CS) & 1u, nullptr, p.status, lim);
+            }
+        }
+    } else if (warp == kActWarp) {
+        // ------------------------------------- activation producer (single mode)
+        if (lane == 0 && !split) {
+            tma_prefetch_map(&tm_act);
+            Ring r;
+            uint32_t issued = 0;
+            bool ok = true;
+            for (int i = 0; i < my_items && ok; ++i) {
+                const Item it = decode_item(blockIdx.x + i * gridDim.x, roff, ioff, E, p.n_tiles);
+                for (int ks = 0; ks < KT; ++ks, r.next(kSlots), ++issued) {
+                    if (!wait_bounded(&slot_empty[r.slot], r.phase ^ 1u, abort_flag, p.status, lim,
+                                      128)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&act_full[r.slot], static_cast<uint32_t>(it.nt) * 128u);
+                    const uint32_t dst = act_smem + r.slot * act_stage_bytes;
+                    for (int grp = 0; grp < it.nt / 16; ++grp)
+                        tma_load_2d(dst + grp * 2048, &tm_act, ks * kStageK, it.row0 + grp * 16,
+                                    &act_full[r.slot]);
+                }
+            }
+            if (!ok) {
+                const uint32_t first = issued > kSlots ? issued - kSlots : 0;
+                for (uint32_t h = first; h < issued; ++h)
+                    wait_bounded(&act_full[h % kSlots], (h / kSlots) & 1u, nullptr, p.status, lim);
+            }
+        }
+    } else {
+        // ------------------------------------------------ converters + epilogue
+        // Warpgroup wg handles the stages with index = wg (mod 4): for each, a
+        // thread reads the 32 code bytes of its weight row (TMEM lane), decodes
+        // them into 32 bf16 pairs (K8-interleaved reduction order) and stores
+        // them into the warpgroup's A slot for that stage.  The warpgroup also
+        // writes the output of item i - 2 when it starts item i (both
+        // accumulator buffers in flight), and of the last two items at the end.
+        const int wg = (warp - kConvWarp0) >> 2;
+        const int wtid = tid - 32 * kConvWarp0 - 128 * wg;   // 0..127 within the warpgroup
         const int q = warp & 3;                    // TMEM lane quarter = warp within the group
         const int row = q * 32 + lane;
-        const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+        const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+        const uint32_t a_base = tmem_base + lane_off + kACol0;
+        const int KT4 = KT / 4;
         int bad_scale = 0;
-        int pf_item = -1, cur_item = -1;
-        Item cur{};
-        const uint8_t *srow = nullptr;
-        // Scale bytes of this row for stage g (two 32-element blocks); the
-        // row's scale pointer is looked up once per work item.
-        auto load_scales = [&](uint32_t g) -> uint32_t {
-            const int i = static_cast<int>(g / KT), ks = static_cast<int>(g - i * KT);
-            if (i != pf_item) {
-                const Item it = decode_item(blockIdx.x + i * gridDim.x, roff, ioff, E, p.n_tiles);
-                const int n = it.n0 + row;
-                srow = n < p.N ? p.scales + (static_cast<size_t>(it.e) * p.N + n) * p.scale_row
-                               : nullptr;
-                pf_item = i;
-            }
+        bool ok = true;
+        Ring code;
+        uint32_t j = 0;                            // warpgroup-local stage counter
+        Item prev1{}, prev2{};                     // items i-1 and i-2
+        auto scale_row_ptr = [&](const Item &it) -> const uint8_t * {
+            const int n = it.n0 + row;
+            return n < p.N ? p.scales + (static_cast<size_t>(it.e) * p.N + n) * p.scale_row
+                           : nullptr;
+        };
+        // Scale bytes of this row for item stage ks (two 32-element blocks).
+        auto load_scales = [&](const uint8_t *srow, int ks) -> uint32_t {
             const int blk = ks * 2;
-            if (!srow || blk >= p.scale_row) return 0x7F7Fu;       // beyond K: zero codes
+            if (!srow || blk >= p.scale_row) return 0x7F7Fu;   // beyond K: zero codes
             if (p.scale_vec2) return __ldg(reinterpret_cast<const uint16_t *>(srow + blk));
             const uint32_t s0 = __ldg(srow + blk);
-            const uint32_t s1 = blk + 1 < p.scale_row ? static_cast<uint32_t>(__ldg(srow + blk + 1)) : 127u;
+            const uint32_t s1 =
+                blk + 1 < p.scale_row ? static_cast<uint32_t>(__ldg(srow + blk + 1)) : 127u;
             return s0 | (s1 << 8);
         };
-        uint32_t sw_next = wg < static_cast<int>(total) ? load_scales(wg) : 0u;
-        for (uint32_t g = wg; g < total; g += kConvWG) {
-            const uint32_t sw = sw_next;
-            if (g + kConvWG < total) sw_next = load_scales(g + kConvWG);   // one stage ahead
-            const int i = static_cast<int>(g / KT);
-            if (i != cur_item) {
-                cur = decode_item(blockIdx.x + i * gridDim.x, roff, ioff, E, p.n_tiles);
-                cur_item = i;
-            }
-            const uint32_t cstage = g >> 2;         // this group's quarter of a code stage
-            const uint32_t cslot = cstage % CS;
-            if (!warp_wait_bounded(&code_full[cslot], (cstage / CS) & 1u, abort_flag, p.status, lim))
-                break;
-            // This row's 32 code bytes of the quarter (2 chunks of 16, 128-byte swizzle).
-            uint32_t cw[2][4];
-            const uint8_t *crow = smem + kOffCode + cslot * kCodeStageBytes + row * 128;
-#pragma unroll
-            for (int ch = 0; ch < 2; ++ch) {
-                const uint4 v = *reinterpret_cast<const uint4 *>(
-                    crow + (((2 * wg + ch) ^ (row & 7)) << 4));
-                cw[ch][0] = v.x;
-                cw[ch][1] = v.y;
-                cw[ch][2] = v.z;
-                cw[ch][3] = v.w;
-            }
+        auto epilogue = [&](int i, const Item &it) -> bool {
+            const uint32_t buf = i & 1;
+            if (!warp_wait_bounded(&acc_full[buf], (i >> 1) & 1, abort_flag, p.status, lim, 64))
+                return false;
+            tc_fence_after();
+            store_item(p, it, tmem_base + lane_off + buf * kAccCols, wg, row, split);
+            tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&code_empty[cslot]);
-            const uint32_t slot = g % kSlots;
-            if (!p.act_k8) {
-                // Interleave every 16-byte chunk of the stage's activation rows in
-                // place (the permutation stays inside a chunk, so the swizzle of
-                // the tile does not matter).
-                if (!warp_wait_bounded(&act_full[slot], (g / kSlots) & 1u, abort_flag, p.status, lim))
+            if (lane == 0) mbar_arrive(&acc_empty[buf]);
+            return true;
+        };
+        Item cur = decode_item(blockIdx.x, roff, ioff, E, p.n_tiles);
+        const uint8_t *srow = scale_row_ptr(cur);
+        uint32_t sw_next = load_scales(srow, wg);
+        for (int i = 0; i < my_items && ok; ++i) {
+            if (i >= 2 && !epilogue(i - 2, prev2)) {
+                ok = false;
+                break;
+            }
+            prev2 = prev1;
+            prev1 = cur;
+            const Item nxt = i + 1 < my_items
+                                 ? decode_item(blockIdx.x + (i + 1) * gridDim.x, roff, ioff, E,
+                                               p.n_tiles)
+                                 : cur;
+            const uint8_t *srow_next = i + 1 < my_items ? scale_row_ptr(nxt) : nullptr;
+            for (int m = 0; m < KT4; ++m, ++j, code.next(CS)) {
+                const uint32_t sw = sw_next;
+                // Scales one stage ahead (the next item's first stage at the end).
+                sw_next = m + 1 < KT4 ? load_scales(srow, 4 * (m + 1) + wg)
+                                      : load_scales(srow_next, wg);
+                if (!warp_wait_bounded(&code_full[code.slot], code.phase, abort_flag, p.status,
+                                       lim)) {
+                    ok = false;
                     break;
-                uint4 *abase = reinterpret_cast<uint4 *>(smem + act_off + slot * act_stage_bytes);
-                for (int c = wtid; c < cur.nt * 8; c += 128) abase[c] = interleave8(abase[c]);
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            }
-            // Scale bytes 0..128 take one bf16 FMA, 129..252 two, 253..255 are
-            // errors; the warp agrees on the path.
-            const bool any_big = __any_sync(0xffffffffu, __vcmpgtu4(sw, 0x8080u) != 0);
-            const bool any_bad = __any_sync(0xffffffffu, __vcmpgtu4(sw, 0xFCFCu) != 0);
-            uint32_t o[32];
-            if (!any_big && !any_bad) {
+                }
+                // This row's 32 code bytes of the stage (2 chunks of 16, 128-byte swizzle).
+                uint32_t cw[2][4];
+                const uint8_t *crow = smem + kOffCode + code.slot * ring_stage_bytes + row * 128;
 #pragma unroll
-                for (int ch = 0; ch < 2; ++ch)
-                    decode32_single(cw[ch], scale_pair_single((sw >> (8 * ch)) & 0xFFu), &o[16 * ch]);
-            } else {
-#pragma unroll
-                for (int ch = 0; ch < 2; ++ch)
-                    if (!decode32_any(cw[ch], (sw >> (8 * ch)) & 0xFFu, &o[16 * ch])) bad_scale = 1;
-            }
-            if (!warp_wait_bounded(&slot_empty[slot], ((g / kSlots) & 1u) ^ 1u, abort_flag, p.status,
-                                   lim))
-                break;
-            tc_fence_after();
-            __syncwarp();
-            tmem_st32(lane_base + kACol0 + slot * kAColsPerSlot, o);
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&a_full[slot]);
-        }
-        if (bad_scale) set_status(p.status, MOE_ERR_DATA);
-    } else if (warp >= kEpiWarp0) {
-        // ------------------------------------------------------------- epilogue
-        const int q = warp & 3;
-        const int row = q * 32 + lane;
-        const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-        for (int i = 0; i < my_items; ++i) {
-            const Item it = decode_item(blockIdx.x + i * gridDim.x, roff, ioff, E, p.n_tiles);
-            const uint32_t accslot = i & 1;
-            if (!warp_wait_bounded(&acc_full[accslot], (i >> 1) & 1, abort_flag, p.status, lim, 128))
-                break;
-            tc_fence_after();
-            const int n = it.n0 + row;
-            const bool col_ok = n < p.N;
-            for (int c = 0; c < it.nt / 16; ++c) {
-                uint32_t v[16];
+                for (int ch = 0; ch < 2; ++ch) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(
+                        crow + (((2 * wg + ch) ^ (row & 7)) << 4));
+                    cw[ch][0] = v.x;
+                    cw[ch][1] = v.y;
+                    cw[ch][2] = v.z;
+                    cw[ch][3] = v.w;
+                }
                 __syncwarp();
-                const uint32_t col = lane_base + accslot * kAccCols + c * 16;
-                tmem_ld16(col, v);
-                if (split) {
-                    // Partial sums of the four warpgroups' K stages, added in order.
-#pragma unroll
-                    for (int j = 1; j < kConvWG; ++j) {
-                        uint32_t u[16];
-                        tmem_ld16(col + 32 * j, u);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int t = 0; t < 16; ++t)
-                            v[t] = __float_as_uint(__uint_as_float(v[t]) + __uint_as_float(u[t]));
+                if (lane == 0) mbar_arrive(&code_empty[code.slot]);
+                const uint32_t slot = static_cast<uint32_t>(wg) + ((j & 1u) ? 4u : 0u);
+                const uint32_t spar = (j >> 1) & 1u;
+                if (!p.act_k8) {
+                    // Interleave every 16-byte chunk of the stage's activation rows in
+                    // place (the permutation stays inside a chunk, so the swizzle of
+                    // the tile does not matter).
+                    if (!split &&
+                        !warp_wait_bounded(&act_full[slot], spar, abort_flag, p.status, lim)) {
+                        ok = false;
+                        break;
                     }
+                    uint4 *abase = reinterpret_cast<uint4 *>(
+                        split ? smem + kOffCode + code.slot * ring_stage_bytes + kCodeStageBytes +
+                                    wg * act_stage_bytes
+                              : smem + act_off + slot * act_stage_bytes);
+                    for (int c = wtid; c < cur.nt * 8; c += 128) abase[c] = interleave8(abase[c]);
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 }
-                tmem_ld_wait();
-                if (col_ok) {
+                // Scale bytes 0..128 take one bf16 FMA, 129..252 two, 253..255 are
+                // errors; the warp agrees on the path.
+                const bool slow = __any_sync(0xffffffffu, __vcmpgtu4(sw, 0x8080u) != 0);
+                uint32_t o[32];
+                if (!slow) {
 #pragma unroll
-                    for (int t = 0; t < 16; ++t) {
-                        const int tok = c * 16 + t;
-                        if (tok < it.nvalid) {
-                            const size_t off = static_cast<size_t>(it.row0 + tok) * p.N + n;
-                            if (p.out_bf16) {
-                                const float f = __uint_as_float(v[t]);
-                                reinterpret_cast<__nv_bfloat16 *>(p.out)[off] = __float2bfloat16_rn(f);
-                            } else {
-                                reinterpret_cast<float *>(p.out)[off] = __uint_as_float(v[t]);
-                            }
-                        }
-                    }
+                    for (int ch = 0; ch < 2; ++ch)
+                        decode32_single(cw[ch], scale_pair_single((sw >> (8 * ch)) & 0xFFu),
+                                        &o[16 * ch]);
+                } else {
+#pragma unroll
+                    for (int ch = 0; ch < 2; ++ch)
+                        if (!decode32_any(cw[ch], (sw >> (8 * ch)) & 0xFFu, &o[16 * ch]))
+                            bad_scale = 1;
                 }
+                if (!warp_wait_bounded(&slot_empty[slot], spar ^ 1u, abort_flag, p.status, lim)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                __syncwarp();
+                tmem_st32(a_base + slot * kAColsPerSlot, o);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&a_full[slot]);
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[accslot]);
+            cur = nxt;
+            srow = srow_next;
         }
+        // Outputs of the last two items.
+        if (ok && my_items >= 2 && !epilogue(my_items - 2, prev2)) ok = false;
+        if (ok && !epilogue(my_items - 1, prev1)) ok = false;
+        if (bad_scale) set_status(p.status, MOE_ERR_DATA);
     }
 
     // ---------------------------------------------------------------- teardown
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) {
+    if (warp == 0) {
         __syncwarp();
         tmem_dealloc(tmem_base, kTmemCols);
     }
