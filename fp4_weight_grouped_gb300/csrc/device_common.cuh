@@ -63,31 +63,42 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait that lets the hardware suspend the calling thread until the phase
+// completes or about `hint_ns` nanoseconds have passed, so a waiting thread
+// takes no issue slots from the warps that do the work.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t *bar, uint32_t parity,
+                                                      uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+constexpr uint32_t kSuspendHintNs = 10000;
+
 // Wait until the barrier phase with the given parity has completed.  Gives up
 // after `limit_ns` nanoseconds (then raises *abort_flag and records
 // MOE_ERR_TIMEOUT) or as soon as another thread raised *abort_flag.  Returns
-// true if the phase completed.  abort_flag may be null (drain waits).
-// max_sleep_ns > 0 lets the thread back off with __nanosleep (32 ns doubling up
-// to max_sleep_ns) so that waiting roles leave issue slots to working warps.
+// true if the phase completed.  abort_flag may be null (drain waits).  Between
+// checks of the clock and the abort flag the thread sleeps in try_wait for at
+// most kSuspendHintNs.
 __device__ __forceinline__ bool wait_bounded(uint64_t *bar, uint32_t parity,
                                              volatile int *abort_flag, int *status,
-                                             uint64_t limit_ns, uint32_t max_sleep_ns = 0) {
+                                             uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    uint32_t sleep_ns = 32;
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (max_sleep_ns) {
-            __nanosleep(sleep_ns);
-            if (sleep_ns < max_sleep_ns) sleep_ns <<= 1;
-        }
-        if ((it & 7u) == 0) {
-            if (abort_flag && *abort_flag) return false;
-            if (globaltimer_ns() - t0 > limit_ns) {
-                if (abort_flag) *abort_flag = 1;
-                set_status(status, MOE_ERR_TIMEOUT);
-                return false;
-            }
+    for (;;) {
+        if (mbar_try_wait_suspend(bar, parity, kSuspendHintNs)) return true;
+        if (abort_flag && *abort_flag) return false;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            if (abort_flag) *abort_flag = 1;
+            set_status(status, MOE_ERR_TIMEOUT);
+            return false;
         }
     }
 }
@@ -96,11 +107,24 @@ __device__ __forceinline__ bool wait_bounded(uint64_t *bar, uint32_t parity,
 // of the warp must call it (it ends with a full-warp shuffle).
 __device__ __forceinline__ bool warp_wait_bounded(uint64_t *bar, uint32_t parity,
                                                   volatile int *abort_flag, int *status,
-                                                  uint64_t limit_ns, uint32_t max_sleep_ns = 0) {
+                                                  uint64_t limit_ns) {
+    // Fast path: every lane probes the barrier once and the warp agrees.
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
     int ok = 0;
-    if ((threadIdx.x & 31) == 0)
-        ok = wait_bounded(bar, parity, abort_flag, status, limit_ns, max_sleep_ns);
+    if ((threadIdx.x & 31) == 0) ok = wait_bounded(bar, parity, abort_flag, status, limit_ns);
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// One lane of the (converged) warp gets true; the warp stays converged, so
+// values computed by every lane can stay in the warp-uniform datapath.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "elect.sync _|P, 0xffffffff;\n\t"
+        "selp.b32 %0, 1, 0, P;\n\t}"
+        : "+r"(pred));
+    return pred != 0;
 }
 
 // ------------------------------------------------------------------------ TMA
@@ -117,6 +141,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// 3-D tiled load of one box into shared memory (x innermost, then y, then z).
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int32_t x,
+                                            int32_t y, int32_t z, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
         : "memory");
 }
 

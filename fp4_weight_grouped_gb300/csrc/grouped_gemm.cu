@@ -48,13 +48,14 @@ namespace gemm {
 constexpr int kIssuerWarps = 4;               // warps 0..3: MMA issuers (lane 0)
 constexpr int kConvWG = 4;                    // converter warpgroups: warps 4..19
 constexpr int kConvWarp0 = kIssuerWarps;
-constexpr int kCodeWarp = kConvWarp0 + 4 * kConvWG;   // warp 20: code producer
-constexpr int kActWarp = kCodeWarp + 1;               // warp 21: activation producer
-constexpr int kThreads = 32 * (kActWarp + 1);         // 704
+constexpr int kActWarp = kConvWarp0 + 4 * kConvWG;    // warp 20: activation producer
+constexpr int kCodeWarp = kActWarp + 1;               // warp 21: code producer
+constexpr int kThreads = 32 * (kCodeWarp + 1);        // 704
 constexpr int kBN = 128;                      // output columns per tile (MMA M)
 constexpr int kMaxNT = 128;                   // tokens per work item (MMA N)
 constexpr int kStageK = 64;                   // K per decode / MMA stage
 constexpr int kSlots = 8;                     // A slots in TMEM (+ activation slots in smem)
+constexpr int kSlotsMax = 12;                 // bands <= 16 rows: three A slots per warpgroup
 constexpr int kCodeK = 256;                   // K per code stage (4 decode stages)
 constexpr int kCodeStageBytes = kBN * kCodeK / 2;         // 16 KB
 constexpr int kCodeStagesMax = 12;
@@ -70,7 +71,7 @@ constexpr int kOffCode = 0;
 constexpr int kOffRowOff = kOffCode + kRingBytes;
 constexpr int kOffItemOff = kOffRowOff + (kMaxE + 1) * 4;
 constexpr int kOffBars = (kOffItemOff + (kMaxE + 1) * 4 + 7) & ~7;
-constexpr int kNumBars = 2 * kCodeStagesMax + 3 * kSlots + 2 * 2 + kIssuerWarps;
+constexpr int kNumBars = 2 * kCodeStagesMax + 3 * kSlotsMax + 2 * 2 + kIssuerWarps;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 64 + 1024;          // + alignment slack
 
@@ -80,6 +81,8 @@ static_assert(kOffBars % 8 == 0, "barrier alignment");
 static_assert(kACol0 + kSlots * kAColsPerSlot <= kTmemCols, "TMEM budget");
 static_assert(kSlots == 2 * kConvWG, "each warpgroup alternates between two A slots");
 static_assert(kConvWG * kPartCols <= kAccCols, "split-mode partials fit one buffer");
+static_assert(2 * kConvWG * (kPartCols / 2) + kSlotsMax * kAColsPerSlot <= kTmemCols,
+              "narrow layout: 16-column partials, twelve A slots");
 static_assert(kCodeK / kStageK == kConvWG, "one code stage = one decode stage per warpgroup");
 
 struct Params {
@@ -93,7 +96,9 @@ struct Params {
     int k_stages;      // 64-k stages per item: 4 * ceil(K / 256)
     int scale_row;     // K / 32
     int scale_vec2;    // scale rows 2-byte aligned: load a stage's 2 scale bytes at once
+    int scale_full;    // scale_vec2 and K % 256 == 0: every stage has both scale bytes
     int act_k8;        // activations already in the K8-interleaved order
+    int act3d;         // K % 256 == 0: one 3-D box fetches a band's 256-k activation tile
     uint64_t wait_limit_ns;
 };
 
@@ -138,7 +143,7 @@ struct Ring {
 // its quarter of the item's token columns.  In split mode the four K-partials
 // are added in warpgroup order (deterministic); f32 or bf16 output.
 __device__ __forceinline__ void store_item(const Params &p, const Item &it, uint32_t acc_base,
-                                           int wg, int row, bool split) {
+                                           int wg, int row, bool split, uint32_t part_cols) {
     const int n = it.n0 + row;
     const int qc = it.nt >> 2;                 // columns per warpgroup (multiple of 4)
     for (int c = wg * qc; c < (wg + 1) * qc; c += 4) {
@@ -147,9 +152,9 @@ __device__ __forceinline__ void store_item(const Params &p, const Item &it, uint
         tmem_ld4(acc_base + c, v);
         if (split) {
             uint32_t u1[4], u2[4], u3[4];
-            tmem_ld4(acc_base + kPartCols + c, u1);
-            tmem_ld4(acc_base + 2 * kPartCols + c, u2);
-            tmem_ld4(acc_base + 3 * kPartCols + c, u3);
+            tmem_ld4(acc_base + part_cols + c, u1);
+            tmem_ld4(acc_base + 2 * part_cols + c, u2);
+            tmem_ld4(acc_base + 3 * part_cols + c, u3);
             tmem_ld_wait();
 #pragma unroll
             for (int t = 0; t < 4; ++t)
@@ -178,7 +183,8 @@ __device__ __forceinline__ void store_item(const Params &p, const Item &it, uint
 
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
-                    const __grid_constant__ CUtensorMap tm_act, const Params p) {
+                    const __grid_constant__ CUtensorMap tm_act,
+                    const __grid_constant__ CUtensorMap tm_act3, const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -188,9 +194,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
     uint64_t *code_full = bars;                          // TMA -> converters (+ issuers, split)
     uint64_t *code_empty = code_full + kCodeStagesMax;   // 16 converter warps (+ 4 commits, split)
     uint64_t *a_full = code_empty + kCodeStagesMax;      // converters -> issuer (4 warps)
-    uint64_t *act_full = a_full + kSlots;                // TMA -> issuer
-    uint64_t *slot_empty = act_full + kSlots;            // MMA commit -> converters, act producer
-    uint64_t *acc_full = slot_empty + kSlots;            // MMA commits -> epilogue
+    uint64_t *act_full = a_full + kSlotsMax;             // TMA -> issuer (single mode)
+    uint64_t *slot_empty = act_full + kSlotsMax;         // MMA commit -> converters, act producer
+    uint64_t *acc_full = slot_empty + kSlotsMax;         // MMA commits -> epilogue
     uint64_t *acc_empty = acc_full + 2;                  // epilogue (16 warps) -> issuers
     uint64_t *final_bar = acc_empty + 2;                 // one per issuer thread
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
@@ -273,6 +279,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
     const uint32_t CS = min(static_cast<uint32_t>(kCodeStagesMax),
                             (kRingBytes - (split ? 0u : kSlots * act_stage_bytes)) / ring_stage_bytes);
     const uint32_t act_off = CS * ring_stage_bytes;     // single mode: activation slots
+    // TMEM columns: two accumulator buffers, then the A slots.  With every band
+    // <= 16 rows the K-partials need 16 columns each, which leaves room for
+    // three A slots per warpgroup (more decode ahead of the MMAs); otherwise two.
+    const bool narrow = split && nt_max <= 16;
+    const uint32_t per_wg = narrow ? 3u : 2u;              // A slots per warpgroup
+    const uint32_t nslots = narrow ? kSlotsMax : kSlots;
+    const uint32_t part_cols = narrow ? kPartCols / 2 : kPartCols;
+    const uint32_t acc_cols = split ? kConvWG * part_cols : kAccCols;
+    const uint32_t acol0 = 2 * acc_cols;
 
     if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
     if (tid == 0) {
@@ -280,7 +295,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
             mbar_init(&code_full[i], 1);
             mbar_init(&code_empty[i], 4 * kConvWG + (split ? kIssuerWarps : 0));
         }
-        for (int i = 0; i < kSlots; ++i) {
+        for (int i = 0; i < kSlotsMax; ++i) {
             mbar_init(&a_full[i], 4);
             mbar_init(&act_full[i], 1);
             mbar_init(&slot_empty[i], 1);
@@ -304,54 +319,59 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
         // ----------------------------------------------------------- MMA issuers
         // Split mode: issuer w issues the stages of converter warpgroup w
         // (every 4th stage) into K-partial w.  Single mode: issuer 0 issues
-        // every stage into one accumulator.
+        // every stage into one accumulator.  The whole warp runs the loop (its
+        // values stay warp-uniform); one elected lane issues the MMAs and the
+        // commits, always the same lane, so each commit covers its MMAs.
         const int w = warp;
-        if (lane == 0 && (split || w == 0)) {
+        if (split || w == 0) {
             const uint32_t step = split ? kConvWG : 1u;
             uint32_t g = split ? w : 0;       // global stage index of this CTA
             int ks = static_cast<int>(g);     // stage within the item
             Item it = decode_item(blockIdx.x, roff, ioff, E, p.n_tiles);
             uint32_t idesc = idesc_bf16_f32(128, it.nt);
             Ring ring;                        // split mode: code stage of this issuer's stage
+            const uint32_t d_part = split ? w * part_cols : 0;
+            Ring sr;                          // this issuer's A-slot sequence
+            const uint32_t b_part = code_smem + kCodeStageBytes + w * act_stage_bytes;
             bool ok = true;
             for (int i = 0; i < my_items && ok;) {
                 const uint32_t buf = i & 1;
-                if (ks < static_cast<int>(step)) {      // first stage of the item
-                    if (!wait_bounded(&acc_empty[buf], ((i >> 1) & 1) ^ 1, abort_flag, p.status,
-                                      lim, 64)) {
-                        ok = false;
-                        break;
-                    }
+                const bool first = ks < static_cast<int>(step);
+                if (first && !warp_wait_bounded(&acc_empty[buf], ((i >> 1) & 1) ^ 1, abort_flag,
+                                                p.status, lim)) {
+                    ok = false;
+                    break;
                 }
-                const uint32_t slot = g & (kSlots - 1), par = (g / kSlots) & 1u;
-                if (!wait_bounded(&a_full[slot], par, abort_flag, p.status, lim, 32) ||
-                    !(split ? wait_bounded(&code_full[ring.slot], ring.phase, abort_flag, p.status,
-                                           lim, 32)
-                            : wait_bounded(&act_full[slot], par, abort_flag, p.status, lim, 32))) {
+                const uint32_t slot = split ? w + kConvWG * sr.slot : sr.slot, par = sr.phase;
+                if (!warp_wait_bounded(&a_full[slot], par, abort_flag, p.status, lim) ||
+                    !(split ? warp_wait_bounded(&code_full[ring.slot], ring.phase, abort_flag,
+                                                p.status, lim)
+                            : warp_wait_bounded(&act_full[slot], par, abort_flag, p.status,
+                                                lim))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + buf * kAccCols + (split ? w * kPartCols : 0);
-                const uint32_t a_col = tmem_base + kACol0 + slot * kAColsPerSlot;
-                const uint64_t b0 = smem_desc_sw128(
-                    split ? code_smem + ring.slot * ring_stage_bytes + kCodeStageBytes +
-                                w * act_stage_bytes
-                          : act_smem + slot * act_stage_bytes);
-                const uint32_t acc0 = ks < static_cast<int>(step) ? 0u : 1u;
+                const uint32_t d_tmem = tmem_base + buf * acc_cols + d_part;
+                const uint32_t a_col = tmem_base + acol0 + slot * kAColsPerSlot;
+                const uint64_t b0 = smem_desc_sw128(split ? b_part + ring.slot * ring_stage_bytes
+                                                          : act_smem + slot * act_stage_bytes);
+                const bool last = ks + static_cast<int>(step) >= KT;
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < kStageK / 16; ++kk)
-                    mma_bf16_ts(d_tmem, a_col + kk * 8, b0 + static_cast<uint64_t>(kk * 2), idesc,
-                                acc0 | static_cast<uint32_t>(kk));
-                mma_commit(&slot_empty[slot]);
-                if (split) {
-                    mma_commit(&code_empty[ring.slot]);
-                    ring.next(CS);
+                    for (int kk = 0; kk < kStageK / 16; ++kk)
+                        mma_bf16_ts(d_tmem, a_col + kk * 8, b0 + static_cast<uint64_t>(kk * 2),
+                                    idesc, (first && kk == 0) ? 0u : 1u);
+                    mma_commit(&slot_empty[slot]);
+                    if (split) mma_commit(&code_empty[ring.slot]);
+                    if (last) mma_commit(&acc_full[buf]);
                 }
+                __syncwarp();
+                if (split) ring.next(CS);
+                sr.next(split ? per_wg : kSlots);
                 g += step;
                 ks += static_cast<int>(step);
-                if (ks >= KT) {                         // last stage of the item
-                    mma_commit(&acc_full[buf]);
+                if (last) {
                     ks -= KT;
                     if (++i < my_items) {
                         it = decode_item(blockIdx.x + i * gridDim.x, roff, ioff, E, p.n_tiles);
@@ -359,45 +379,62 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
                     }
                 }
             }
-            // All MMAs issued by this thread must finish before TMEM is freed.
-            mma_commit(&final_bar[w]);
-            wait_bounded(&final_bar[w], 0, nullptr, p.status, lim);
+            // All MMAs issued by the elected lane must finish before TMEM is freed.
+            if (elect_one()) mma_commit(&final_bar[w]);
+            __syncwarp();
+            warp_wait_bounded(&final_bar[w], 0, nullptr, p.status, lim);
         }
     } else if (warp == kCodeWarp) {
         // ------------------------------------------------------ code producer
+        // Converged warp, one elected lane issues the copies.  Split mode: the
+        // band's activation tile of the code stage rides along; with bands of
+        // <= 16 rows and K % 256 == 0 it is one 3-D box (16 rows x 4 x 64 k,
+        // stored as four 64-k tiles), else 2-D boxes of 16 rows x 64 k.
+        const bool use3d = p.act3d && narrow;    // one 16-row group per code stage
         if (lane == 0) {
             tma_prefetch_map(&tm_codes);
-            Ring r;
-            uint32_t issued = 0;
-            bool ok = true;
-            for (int i = 0; i < my_items && ok; ++i) {
-                const Item it = decode_item(blockIdx.x + i * gridDim.x, roff, ioff, E, p.n_tiles);
-                const int y = it.e * p.N + it.n0;
-                for (int kc = 0; kc < KT / 4; ++kc, r.next(CS), ++issued) {
-                    if (!wait_bounded(&code_empty[r.slot], r.phase ^ 1u, abort_flag, p.status, lim,
-                                      128)) {
-                        ok = false;
-                        break;
-                    }
+            if (split) tma_prefetch_map(use3d ? &tm_act3 : &tm_act);
+        }
+        __syncwarp();
+        Ring r;
+        uint32_t issued = 0;
+        bool ok = true;
+        for (int i = 0; i < my_items && ok; ++i) {
+            const Item it = decode_item(blockIdx.x + i * gridDim.x, roff, ioff, E, p.n_tiles);
+            const int y = it.e * p.N + it.n0;
+            for (int kc = 0; kc < KT / 4; ++kc, r.next(CS), ++issued) {
+                if (!warp_wait_bounded(&code_empty[r.slot], r.phase ^ 1u, abort_flag, p.status,
+                                       lim)) {
+                    ok = false;
+                    break;
+                }
+                if (elect_one()) {
                     const uint32_t dst = code_smem + r.slot * ring_stage_bytes;
                     mbar_arrive_expect_tx(&code_full[r.slot],
                                           kCodeStageBytes + (split ? it.nt * 512u : 0u));
                     tma_load_2d(dst, &tm_codes, kc * 128, y, &code_full[r.slot]);
                     if (split) {
-                        for (int sub = 0; sub < 4; ++sub)
-                            for (int grp = 0; grp < it.nt / 16; ++grp)
-                                tma_load_2d(dst + kCodeStageBytes + sub * act_stage_bytes +
-                                                grp * 2048,
-                                            &tm_act, kc * kCodeK + sub * kStageK,
-                                            it.row0 + grp * 16, &code_full[r.slot]);
+                        for (int grp = 0; grp < it.nt / 16; ++grp) {
+                            if (use3d) {
+                                tma_load_3d(dst + kCodeStageBytes + grp * 2048, &tm_act3, 0,
+                                            it.row0 + grp * 16, kc * 4, &code_full[r.slot]);
+                            } else {
+                                for (int sub = 0; sub < 4; ++sub)
+                                    tma_load_2d(dst + kCodeStageBytes + sub * act_stage_bytes +
+                                                    grp * 2048,
+                                                &tm_act, kc * kCodeK + sub * kStageK,
+                                                it.row0 + grp * 16, &code_full[r.slot]);
+                            }
+                        }
                     }
                 }
+                __syncwarp();
             }
-            if (!ok) {   // drain: every issued copy must land before the CTA exits
-                const uint32_t first = issued > CS ? issued - CS : 0;
-                for (uint32_t h = first; h < issued; ++h)
-                    wait_bounded(&code_full[h % CS], (h / CS) & 1u, nullptr, p.status, lim);
-            }
+        }
+        if (!ok && lane == 0) {   // drain: every issued copy must land before the CTA exits
+            const uint32_t first = issued > CS ? issued - CS : 0;
+            for (uint32_t h = first; h < issued; ++h)
+                wait_bounded(&code_full[h % CS], (h / CS) & 1u, nullptr, p.status, lim);
         }
     } else if (warp == kActWarp) {
         // ------------------------------------- activation producer (single mode)
@@ -409,8 +446,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
             for (int i = 0; i < my_items && ok; ++i) {
                 const Item it = decode_item(blockIdx.x + i * gridDim.x, roff, ioff, E, p.n_tiles);
                 for (int ks = 0; ks < KT; ++ks, r.next(kSlots), ++issued) {
-                    if (!wait_bounded(&slot_empty[r.slot], r.phase ^ 1u, abort_flag, p.status, lim,
-                                      128)) {
+                    if (!wait_bounded(&slot_empty[r.slot], r.phase ^ 1u, abort_flag, p.status, lim)) {
                         ok = false;
                         break;
                     }
@@ -440,59 +476,53 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
         const int q = warp & 3;                    // TMEM lane quarter = warp within the group
         const int row = q * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-        const uint32_t a_base = tmem_base + lane_off + kACol0;
+        const uint32_t a_base = tmem_base + lane_off + acol0;
         const int KT4 = KT / 4;
         int bad_scale = 0;
         bool ok = true;
         Ring code;
-        uint32_t j = 0;                            // warpgroup-local stage counter
-        Item prev1{}, prev2{};                     // items i-1 and i-2
-        auto scale_row_ptr = [&](const Item &it) -> const uint8_t * {
-            const int n = it.n0 + row;
-            return n < p.N ? p.scales + (static_cast<size_t>(it.e) * p.N + n) * p.scale_row
-                           : nullptr;
+        Ring sr;                                   // this warpgroup's A-slot sequence
+        // Scale bytes of item stage 4m + wg for this row: bytes 8m + 2wg and
+        // 8m + 2wg + 1 of the row.  A tile row beyond N reads row N - 1 (its
+        // codes are zero-filled, so the value never matters).
+        auto scale_base = [&](int j) -> const uint8_t * {
+            const Item it = decode_item(blockIdx.x + j * gridDim.x, roff, ioff, E, p.n_tiles);
+            const int n = min(it.n0 + row, p.N - 1);
+            return p.scales + (static_cast<size_t>(it.e) * p.N + n) * p.scale_row + 2 * wg;
         };
-        // Scale bytes of this row for item stage ks (two 32-element blocks).
-        auto load_scales = [&](const uint8_t *srow, int ks) -> uint32_t {
-            const int blk = ks * 2;
-            if (!srow || blk >= p.scale_row) return 0x7F7Fu;   // beyond K: zero codes
-            if (p.scale_vec2) return __ldg(reinterpret_cast<const uint16_t *>(srow + blk));
-            const uint32_t s0 = __ldg(srow + blk);
+        auto load_scales = [&](const uint8_t *sb, int m) -> uint32_t {
+            if (p.scale_full) return __ldg(reinterpret_cast<const uint16_t *>(sb + 8 * m));
+            const int blk = 8 * m + 2 * wg;
+            const uint32_t s0 = blk < p.scale_row ? static_cast<uint32_t>(__ldg(sb + 8 * m)) : 127u;
             const uint32_t s1 =
-                blk + 1 < p.scale_row ? static_cast<uint32_t>(__ldg(srow + blk + 1)) : 127u;
+                blk + 1 < p.scale_row ? static_cast<uint32_t>(__ldg(sb + 8 * m + 1)) : 127u;
             return s0 | (s1 << 8);
         };
-        auto epilogue = [&](int i, const Item &it) -> bool {
+        auto epilogue = [&](int i) -> bool {
             const uint32_t buf = i & 1;
-            if (!warp_wait_bounded(&acc_full[buf], (i >> 1) & 1, abort_flag, p.status, lim, 64))
+            if (!warp_wait_bounded(&acc_full[buf], (i >> 1) & 1, abort_flag, p.status, lim))
                 return false;
             tc_fence_after();
-            store_item(p, it, tmem_base + lane_off + buf * kAccCols, wg, row, split);
+            const Item it = decode_item(blockIdx.x + i * gridDim.x, roff, ioff, E, p.n_tiles);
+            store_item(p, it, tmem_base + lane_off + buf * acc_cols, wg, row, split, part_cols);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[buf]);
             return true;
         };
-        Item cur = decode_item(blockIdx.x, roff, ioff, E, p.n_tiles);
-        const uint8_t *srow = scale_row_ptr(cur);
-        uint32_t sw_next = load_scales(srow, wg);
+        int cur_nt = decode_item(blockIdx.x, roff, ioff, E, p.n_tiles).nt;
+        const uint8_t *sb = scale_base(0);
+        uint32_t sw_next = load_scales(sb, 0);
         for (int i = 0; i < my_items && ok; ++i) {
-            if (i >= 2 && !epilogue(i - 2, prev2)) {
+            if (i >= 2 && !epilogue(i - 2)) {
                 ok = false;
                 break;
             }
-            prev2 = prev1;
-            prev1 = cur;
-            const Item nxt = i + 1 < my_items
-                                 ? decode_item(blockIdx.x + (i + 1) * gridDim.x, roff, ioff, E,
-                                               p.n_tiles)
-                                 : cur;
-            const uint8_t *srow_next = i + 1 < my_items ? scale_row_ptr(nxt) : nullptr;
-            for (int m = 0; m < KT4; ++m, ++j, code.next(CS)) {
+            const uint8_t *sb_next = scale_base(i + 1 < my_items ? i + 1 : i);
+            for (int m = 0; m < KT4; ++m, sr.next(per_wg), code.next(CS)) {
                 const uint32_t sw = sw_next;
                 // Scales one stage ahead (the next item's first stage at the end).
-                sw_next = m + 1 < KT4 ? load_scales(srow, 4 * (m + 1) + wg)
-                                      : load_scales(srow_next, wg);
+                sw_next = m + 1 < KT4 ? load_scales(sb, m + 1) : load_scales(sb_next, 0);
                 if (!warp_wait_bounded(&code_full[code.slot], code.phase, abort_flag, p.status,
                                        lim)) {
                     ok = false;
@@ -512,8 +542,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&code_empty[code.slot]);
-                const uint32_t slot = static_cast<uint32_t>(wg) + ((j & 1u) ? 4u : 0u);
-                const uint32_t spar = (j >> 1) & 1u;
+                const uint32_t slot = static_cast<uint32_t>(wg) + kConvWG * sr.slot;
+                const uint32_t spar = sr.phase;
                 if (!p.act_k8) {
                     // Interleave every 16-byte chunk of the stage's activation rows in
                     // place (the permutation stays inside a chunk, so the swizzle of
@@ -527,23 +557,20 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
                         split ? smem + kOffCode + code.slot * ring_stage_bytes + kCodeStageBytes +
                                     wg * act_stage_bytes
                               : smem + act_off + slot * act_stage_bytes);
-                    for (int c = wtid; c < cur.nt * 8; c += 128) abase[c] = interleave8(abase[c]);
+                    for (int c = wtid; c < cur_nt * 8; c += 128) abase[c] = interleave8(abase[c]);
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 }
                 // Scale bytes 0..128 take one bf16 FMA, 129..252 two, 253..255 are
                 // errors; the warp agrees on the path.
-                const bool slow = __any_sync(0xffffffffu, __vcmpgtu4(sw, 0x8080u) != 0);
+                const uint32_t s_lo = sw & 0xFFu, s_hi = sw >> 8;
+                const bool slow = __any_sync(0xffffffffu, max(s_lo, s_hi) > 128u);
                 uint32_t o[32];
                 if (!slow) {
-#pragma unroll
-                    for (int ch = 0; ch < 2; ++ch)
-                        decode32_single(cw[ch], scale_pair_single((sw >> (8 * ch)) & 0xFFu),
-                                        &o[16 * ch]);
+                    decode32_single(cw[0], scale_pair_single(s_lo), &o[0]);
+                    decode32_single(cw[1], scale_pair_single(s_hi), &o[16]);
                 } else {
-#pragma unroll
-                    for (int ch = 0; ch < 2; ++ch)
-                        if (!decode32_any(cw[ch], (sw >> (8 * ch)) & 0xFFu, &o[16 * ch]))
-                            bad_scale = 1;
+                    if (!decode32_any(cw[0], s_lo, &o[0])) bad_scale = 1;
+                    if (!decode32_any(cw[1], s_hi, &o[16])) bad_scale = 1;
                 }
                 if (!warp_wait_bounded(&slot_empty[slot], spar ^ 1u, abort_flag, p.status, lim)) {
                     ok = false;
@@ -551,18 +578,21 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
                 }
                 tc_fence_after();
                 __syncwarp();
-                tmem_st32(a_base + slot * kAColsPerSlot, o);
+                tmem_st16(a_base + slot * kAColsPerSlot, *reinterpret_cast<uint32_t(*)[16]>(&o[0]));
+                tmem_st16(a_base + slot * kAColsPerSlot + 16,
+                          *reinterpret_cast<uint32_t(*)[16]>(&o[16]));
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&a_full[slot]);
             }
-            cur = nxt;
-            srow = srow_next;
+            if (!p.act_k8 && i + 1 < my_items)
+                cur_nt = decode_item(blockIdx.x + (i + 1) * gridDim.x, roff, ioff, E, p.n_tiles).nt;
+            sb = sb_next;
         }
         // Outputs of the last two items.
-        if (ok && my_items >= 2 && !epilogue(my_items - 2, prev2)) ok = false;
-        if (ok && !epilogue(my_items - 1, prev1)) ok = false;
+        if (ok && my_items >= 2 && !epilogue(my_items - 2)) ok = false;
+        if (ok && !epilogue(my_items - 1)) ok = false;
         if (bad_scale) set_status(p.status, MOE_ERR_DATA);
     }
 
@@ -642,7 +672,7 @@ moe_status launch_grouped_gemm(const uint16_t *act, int rows, int K, const uint8
     PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode_fn();
     if (!encode) return MOE_ERR_CUDA;
 
-    CUtensorMap tm_codes, tm_act;
+    CUtensorMap tm_codes, tm_act, tm_act3;
     {
         cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2),
                               static_cast<cuuint64_t>(E) * static_cast<cuuint64_t>(N)};
@@ -665,6 +695,22 @@ moe_status launch_grouped_gemm(const uint16_t *act, int rows, int K, const uint8
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return MOE_ERR_CUDA;
+    }
+    // The same activations seen as [K/64 chunks][rows][64]: one box holds 16
+    // rows x 4 chunks and lands as four consecutive 64-k tiles of 16 rows.
+    const int act3d = (K % kCodeK) == 0;
+    if (act3d) {
+        cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(K / 64)};
+        cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, 128};
+        cuuint32_t box[3] = {64, 16, 4};
+        cuuint32_t estr[3] = {1, 1, 1};
+        if (encode(&tm_act3, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t *>(act), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return MOE_ERR_CUDA;
+    } else {
+        tm_act3 = tm_act;
     }
     static uint64_t attr_dev_mask = 0;
     int dev = 0;
@@ -689,9 +735,11 @@ moe_status launch_grouped_gemm(const uint16_t *act, int rows, int K, const uint8
     p.k_stages = 4 * ((K + kCodeK - 1) / kCodeK);
     p.scale_row = K / 32;
     p.scale_vec2 = ((K / 32) % 2 == 0) && ((reinterpret_cast<uintptr_t>(scales) & 1) == 0);
+    p.scale_full = p.scale_vec2 && (K % kCodeK) == 0;
     p.wait_limit_ns = wait_limit_ns;
     p.act_k8 = act_k8;
-    grouped_gemm_kernel<<<num_sms, kThreads, kSmemBytes, stream>>>(tm_codes, tm_act, p);
+    p.act3d = act3d;
+    grouped_gemm_kernel<<<num_sms, kThreads, kSmemBytes, stream>>>(tm_codes, tm_act, tm_act3, p);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

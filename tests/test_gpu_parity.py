@@ -169,21 +169,25 @@ def test_gemm_identity_activations_expose_decoded_weights(B, scale_range, k8):
     np.testing.assert_array_equal(out, dec.T)
 
 
+@pytest.mark.parametrize("rows", [32, 16], ids=["bands32", "bands16"])
 @pytest.mark.parametrize("scale_range", [(2, 128), (2, 252)], ids=["one_fma_path", "split_path"])
-def test_gemm_split_mode_exposes_decoded_weights(B, scale_range):
-    # 16 experts x 32 rows, K = 512: row r of expert e is one-hot at k = 32e + r, so
-    # out[row, n] = w_e[n, 32e + r] exactly; bands <= 32 rows select the split mode.
+def test_gemm_split_mode_exposes_decoded_weights(B, scale_range, rows):
+    # 512 // rows experts x `rows` rows, K = 512: row r of expert e is one-hot at
+    # k = rows * e + r, so out[row, n] = w_e[n, rows * e + r] exactly.  Bands of
+    # <= 32 rows select the split-accumulator mode, <= 16 its narrow layout.
     rng = np.random.default_rng(9)
-    E, K, N = 16, 512, 256
+    K, N = 512, 256
+    E = K // rows
     codes = rng.integers(0, 256, (E, N, K // 2), dtype=np.uint8)
     scales = rng.integers(scale_range[0], scale_range[1] + 1, (E, N, K // 32), dtype=np.uint8)
     one = inputs.f32_to_bf16_bits(np.ones(1, np.float32))[0]
-    act = np.zeros((E * 32, K), np.uint16)
-    act[np.arange(E * 32), np.arange(E * 32)] = one
-    out = _gemm_gpu(B, act, codes, scales, np.full(E, 32, np.int32))
+    act = np.zeros((K, K), np.uint16)
+    act[np.arange(K), np.arange(K)] = one
+    out = _gemm_gpu(B, act, codes, scales, np.full(E, rows, np.int32))
     for e in range(E):
         dec = inputs.bf16_bits_to_f32(oracle.decode_expert_bf16(codes, scales, e))
-        np.testing.assert_array_equal(out[32 * e:32 * e + 32], dec[:, 32 * e:32 * e + 32].T)
+        np.testing.assert_array_equal(out[rows * e:rows * e + rows],
+                                      dec[:, rows * e:rows * e + rows].T)
 
 
 # ---------------------------------------------------------------- grouped GEMM
