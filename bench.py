@@ -52,8 +52,8 @@ FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
 # DRAM bytes (read + write) per launch of the w13 GEMM kernel measured by ncu for
 # each workload, with the hash of the kernel source they were taken on.  A
 # changed kernel reports traffic = null until re-measured.
-NCU_TRAFFIC = {}
-NCU_KERNEL_HASH = None
+NCU_TRAFFIC = {"decode_T64": 1785895000 + 9617920}   # profiles/grouped_gemm_decode_T64_w13.md
+NCU_KERNEL_HASH = "819b8d5e49eaf623"
 
 WEIGHT_BYTES_PER_ELEM = 17.0 / 32.0       # 4-bit code + one E8M0 byte per 32
 
@@ -80,6 +80,26 @@ def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return rank, world, local
+
+
+def reduce_max_over_ranks(values, device=None):
+    """Max of each value over all ranks (identity on one process).  Every rank
+    must call it; the replicas' step times are combined this way, so the job is
+    as fast as its slowest replica."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.cpu()]
+
+
+def whole_job_rate(work_per_rank_step: float, ms_per_step: float, world: int) -> float:
+    """Units per second of the whole job: every replica processes the same work
+    per step (weak scaling), timed by the slowest replica."""
+    return world * work_per_rank_step / (ms_per_step * 1e-3)
 
 
 def gemm_work(gs, K, N):
@@ -258,11 +278,7 @@ def run_ours(args, rank, world, local):
     d2h = hout.numel() * 4
 
     # ---- aggregate over ranks (max time)
-    ms_step = ms_total / K
-    if world > 1:
-        t = torch.tensor([ms_step, e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step, e2e_ms = float(t[0]), float(t[1])
+    ms_step, e2e_ms = reduce_max_over_ranks([ms_total / K, e2e_ms], device=dev)
     flops = f13 + f2
     hbm, bf16_burst, bf16_sus, peak_src = load_peaks()
     w13_avg_ms = statistics.fmean(w13_ms)
@@ -273,7 +289,7 @@ def run_ours(args, rank, world, local):
         traffic = NCU_TRAFFIC.get(args.workload)
     result = {
         "metric": METRIC,
-        "value": round(world * flops / (ms_step * 1e-3) / 1e12, 3),
+        "value": round(whole_job_rate(flops, ms_step, world) / 1e12, 3),
         "unit": "TFLOP/s",
         "n_gpus": world,
         "steps": K,
@@ -290,7 +306,7 @@ def run_ours(args, rank, world, local):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2: %.2f GB of touched MXFP4 weights per step vs 129 MB L2; "
                          "no flush" % ((b13 + b2) / 1e9)},
-        "weight_GBps": round(world * (b13 + b2) / (ms_step * 1e-3) / 1e9, 1),
+        "weight_GBps": round(whole_job_rate(b13 + b2, ms_step, world) / 1e9, 1),
         "gemm_flops_per_step": flops,
         "weight_bytes_per_step": b13 + b2,
         "roofline": {
@@ -308,7 +324,7 @@ def run_ours(args, rank, world, local):
             "avg_launch_ms": round(w13_avg_ms, 5),
             "roofline_frac_of_max": None,
         },
-        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+        "e2e": {"value": round(whole_job_rate(flops, e2e_ms, world) / 1e12, 3), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "api": "moe_layer_forward with pinned host copies"},
         "gpu_launches": launches_per_step * K,
@@ -324,22 +340,20 @@ def run_ours(args, rank, world, local):
 
 # --------------------------------------------------------------- CPU oracle arm
 
-def oracle_sample(workload: str, seed: int, max_experts: int):
-    """A bounded sample of the workload for the CPU oracle: the grouped GEMMs
+def oracle_sample(c, max_experts: int):
+    """A bounded sample of workload `c` for the CPU oracle: the grouped GEMMs
     of the first `max_experts` non-empty expert bands, SwiGLU on them and a
     combine over the same rows."""
     import numpy as np
 
-    from fp4_weight_grouped_gb300 import inputs
     import oracle
-    c = inputs.layer_workload(workload, seed)
     gs, off, ss, s2r = oracle.route_sort(c["ids"], c["E"])
     keep = np.nonzero(gs)[0][:max_experts]
     gs_s = np.zeros_like(gs)
     gs_s[keep] = gs[keep]
     rows_idx = np.concatenate([np.arange(off[e], off[e + 1]) for e in keep])
     xs = oracle.gather(c["x"], ss, c["k"])[rows_idx]
-    return c, gs_s, xs
+    return gs_s, xs
 
 
 def run_oracle_steps(c, gs_s, xs, steps):
@@ -362,9 +376,10 @@ def run_oracle_steps(c, gs_s, xs, steps):
 
 
 def cpu_baseline(workload: str, seed: int):
-    import numpy as np
+    from fp4_weight_grouped_gb300 import inputs
     n_exp = 64
-    c, gs_s, xs = oracle_sample(workload, seed, n_exp)
+    c = inputs.layer_workload(workload, seed)
+    gs_s, xs = oracle_sample(c, n_exp)
     flops, times, threads = run_oracle_steps(c, gs_s, xs, 1)
     return {"value": round(flops / times[0] / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
             "kind": "oracle",
@@ -373,20 +388,31 @@ def cpu_baseline(workload: str, seed: int):
                       f"({times[0]:.1f} s)"}
 
 
+REFERENCE_BUDGET_S = 150.0     # whole reference run (warm-up + timed steps)
+
+
 def run_reference(args, rank, world):
+    """The CPU oracle timed as the reference arm: `warmup` + `steps` steps, each
+    over the first n non-empty expert bands of the workload, with n chosen from
+    a one-band calibration so the run fits REFERENCE_BUDGET_S.  Rank 0 only."""
     if rank != 0:
         return None
-    n_exp = 16
-    c, gs_s, xs = oracle_sample(args.workload, args.seed, n_exp)
-    run_oracle_steps(c, gs_s, xs, args.warmup_ref)
-    flops, times, threads = run_oracle_steps(c, gs_s, xs, args.steps_ref)
+    from fp4_weight_grouped_gb300 import inputs
+    c = inputs.layer_workload(args.workload, args.seed)
+    gs1, xs1 = oracle_sample(c, 1)
+    _, t1, _ = run_oracle_steps(c, gs1, xs1, 1)
+    per_step = REFERENCE_BUDGET_S / (args.steps + args.warmup)
+    n_exp = int(max(1, min(64, per_step // max(t1[0], 1e-6))))
+    gs_s, xs = oracle_sample(c, n_exp)
+    run_oracle_steps(c, gs_s, xs, args.warmup)
+    flops, times, threads = run_oracle_steps(c, gs_s, xs, args.steps)
     ms = 1e3 * sum(times) / len(times)
     val = round(flops / (ms * 1e-3) / 1e12, 6)
     sample = (f"w13 + SwiGLU + w2 + combine over the first {n_exp} non-empty expert bands "
-              f"({int(gs_s.sum())} rows) of {args.workload}, fp64 C oracle")
+              f"({int(gs_s.sum())} rows) of {args.workload} per step, fp64 C oracle")
     return {
         "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": world,
-        "steps": args.steps_ref, "warmup": args.warmup_ref, "ms_per_step": round(ms, 3),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (same generator and seed as the GPU arm)",
         "config": {"workload": args.workload, "description": WORKLOADS[args.workload],
@@ -415,9 +441,6 @@ def main():
     rank, world, local = dist_env()
 
     if args.impl == "reference":
-        # The reference arm is the CPU oracle: bounded steps so the run stays short.
-        args.steps_ref = max(1, min(args.steps, 3))
-        args.warmup_ref = 1
         res = run_reference(args, rank, world)
         if res is not None:
             print(json.dumps(res), flush=True)

@@ -1,0 +1,62 @@
+"""Host logic of the multi-replica bench on CPU: two gloo ranks combine their
+step times with a max, the whole-job rate counts every replica's work, and the
+reference arm runs on rank 0 only."""
+import argparse
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        # rank r reports step time 1.5 + r ms and e2e time 10 - r ms
+        got = bench.reduce_max_over_ranks([1.5 + rank, 10.0 - rank])
+        q.put((rank, got))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_take_the_slowest_replica():
+    world = 2
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    results = dict(q.get(timeout=10) for _ in range(world))
+    for r in range(world):
+        assert results[r] == [2.5, 10.0]
+
+
+def test_single_process_reduce_is_identity():
+    assert bench.reduce_max_over_ranks([3.0, 4.0]) == [3.0, 4.0]
+
+
+def test_whole_job_rate_counts_every_replica():
+    # 2 replicas x 1e12 flop per step in 2 ms -> 1e15 flop/s
+    assert bench.whole_job_rate(1e12, 2.0, 2) == pytest.approx(1e15)
+    assert bench.whole_job_rate(5.0, 1.0, 1) == pytest.approx(5000.0)
+
+
+def test_reference_arm_runs_on_rank_zero_only():
+    args = argparse.Namespace(workload="decode_T64", seed=0, steps=2, warmup=3)
+    assert bench.run_reference(args, rank=1, world=2) is None
