@@ -59,6 +59,7 @@ constexpr int kSlotsMax = 12;                 // bands <= 16 rows: three A slots
 constexpr int kCodeK = 256;                   // K per code stage (4 decode stages)
 constexpr int kCodeStageBytes = kBN * kCodeK / 2;         // 16 KB
 constexpr int kCodeStagesMax = 12;
+constexpr int kScaleTileBytes = 128 * 16;     // scale bytes of two code stages (512 k) x 128 rows
 constexpr int kRingBytes = 216 * 1024;        // code ring + activation tiles
 constexpr int kTmemCols = 512;
 constexpr int kAccCols = 128;                 // per accumulator buffer
@@ -97,6 +98,7 @@ struct Params {
     int scale_row;     // K / 32
     int scale_vec2;    // scale rows 2-byte aligned: load a stage's 2 scale bytes at once
     int scale_full;    // scale_vec2 and K % 256 == 0: every stage has both scale bytes
+    int scale_tma;     // K % 512 == 0, 16-byte aligned scales: scale tiles ride in the ring
     int act_k8;        // activations already in the K8-interleaved order
     int act3d;         // K % 256 == 0: one 3-D box fetches a band's 256-k activation tile
     uint64_t wait_limit_ns;
@@ -184,7 +186,8 @@ __device__ __forceinline__ void store_item(const Params &p, const Item &it, uint
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
                     const __grid_constant__ CUtensorMap tm_act,
-                    const __grid_constant__ CUtensorMap tm_act3, const Params p) {
+                    const __grid_constant__ CUtensorMap tm_act3,
+                    const __grid_constant__ CUtensorMap tm_scales, const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -275,7 +278,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
     const int nt_max = *nt_max_slot;
     const bool split = nt_max <= kPartCols;
     const uint32_t act_stage_bytes = static_cast<uint32_t>(nt_max) * 128u;   // one 64-k box
-    const uint32_t ring_stage_bytes = kCodeStageBytes + (split ? 4u * act_stage_bytes : 0u);
+    // Ring slot: codes (16 KB), [split: activation tile], [scale tile, loaded
+    // with every even code stage for itself and the next one].
+    const uint32_t scale_off = kCodeStageBytes + (split ? 4u * act_stage_bytes : 0u);
+    const uint32_t ring_stage_bytes = scale_off + (p.scale_tma ? kScaleTileBytes : 0u);
     const uint32_t CS = min(static_cast<uint32_t>(kCodeStagesMax),
                             (kRingBytes - (split ? 0u : kSlots * act_stage_bytes)) / ring_stage_bytes);
     const uint32_t act_off = CS * ring_stage_bytes;     // single mode: activation slots
@@ -394,6 +400,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
         if (lane == 0) {
             tma_prefetch_map(&tm_codes);
             if (split) tma_prefetch_map(use3d ? &tm_act3 : &tm_act);
+            if (p.scale_tma) tma_prefetch_map(&tm_scales);
         }
         __syncwarp();
         Ring r;
@@ -410,9 +417,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
                 }
                 if (elect_one()) {
                     const uint32_t dst = code_smem + r.slot * ring_stage_bytes;
+                    const bool scales_here = p.scale_tma && (kc & 1) == 0;
                     mbar_arrive_expect_tx(&code_full[r.slot],
-                                          kCodeStageBytes + (split ? it.nt * 512u : 0u));
+                                          kCodeStageBytes + (split ? it.nt * 512u : 0u) +
+                                              (scales_here ? kScaleTileBytes : 0u));
                     tma_load_2d(dst, &tm_codes, kc * 128, y, &code_full[r.slot]);
+                    if (scales_here)
+                        tma_load_2d(dst + scale_off, &tm_scales, kc * 8, y, &code_full[r.slot]);
                     if (split) {
                         for (int grp = 0; grp < it.nt / 16; ++grp) {
                             if (use3d) {
@@ -512,21 +523,37 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
         };
         int cur_nt = decode_item(blockIdx.x, roff, ioff, E, p.n_tiles).nt;
         const uint8_t *sb = scale_base(0);
-        uint32_t sw_next = load_scales(sb, 0);
+        uint32_t sw_next = p.scale_tma ? 0u : load_scales(sb, 0);
+        uint32_t sw_stash = 0;
+        // Scale bytes that belong to a tile row beyond N (read with the tile) never
+        // count as errors: those rows are not part of the output.
+        bool row_ok = decode_item(blockIdx.x, roff, ioff, E, p.n_tiles).n0 + row < p.N;
         for (int i = 0; i < my_items && ok; ++i) {
             if (i >= 2 && !epilogue(i - 2)) {
                 ok = false;
                 break;
             }
-            const uint8_t *sb_next = scale_base(i + 1 < my_items ? i + 1 : i);
+            const uint8_t *sb_next = p.scale_tma ? sb : scale_base(i + 1 < my_items ? i + 1 : i);
             for (int m = 0; m < KT4; ++m, sr.next(per_wg), code.next(CS)) {
-                const uint32_t sw = sw_next;
+                uint32_t sw = sw_next;
                 // Scales one stage ahead (the next item's first stage at the end).
-                sw_next = m + 1 < KT4 ? load_scales(sb, m + 1) : load_scales(sb_next, 0);
+                if (!p.scale_tma)
+                    sw_next = m + 1 < KT4 ? load_scales(sb, m + 1) : load_scales(sb_next, 0);
                 if (!warp_wait_bounded(&code_full[code.slot], code.phase, abort_flag, p.status,
                                        lim)) {
                     ok = false;
                     break;
+                }
+                if (p.scale_tma) {
+                    // Even code stage: this row's scale bytes for it and the next.
+                    if ((m & 1) == 0) {
+                        const uint16_t *sp = reinterpret_cast<const uint16_t *>(
+                            smem + kOffCode + code.slot * ring_stage_bytes + scale_off + row * 16) + wg;
+                        sw = sp[0];
+                        sw_stash = sp[4];
+                    } else {
+                        sw = sw_stash;
+                    }
                 }
                 // This row's 32 code bytes of the stage (2 chunks of 16, 128-byte swizzle).
                 uint32_t cw[2][4];
@@ -569,8 +596,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
                     decode32_single(cw[0], scale_pair_single(s_lo), &o[0]);
                     decode32_single(cw[1], scale_pair_single(s_hi), &o[16]);
                 } else {
-                    if (!decode32_any(cw[0], s_lo, &o[0])) bad_scale = 1;
-                    if (!decode32_any(cw[1], s_hi, &o[16])) bad_scale = 1;
+                    if (!decode32_any(cw[0], s_lo, &o[0]) && row_ok) bad_scale = 1;
+                    if (!decode32_any(cw[1], s_hi, &o[16]) && row_ok) bad_scale = 1;
                 }
                 if (!warp_wait_bounded(&slot_empty[slot], spar ^ 1u, abort_flag, p.status, lim)) {
                     ok = false;
@@ -586,8 +613,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&a_full[slot]);
             }
-            if (!p.act_k8 && i + 1 < my_items)
-                cur_nt = decode_item(blockIdx.x + (i + 1) * gridDim.x, roff, ioff, E, p.n_tiles).nt;
+            if (i + 1 < my_items) {
+                const Item nx = decode_item(blockIdx.x + (i + 1) * gridDim.x, roff, ioff, E, p.n_tiles);
+                cur_nt = nx.nt;
+                row_ok = nx.n0 + row < p.N;
+            }
             sb = sb_next;
         }
         // Outputs of the last two items.
@@ -672,7 +702,7 @@ moe_status launch_grouped_gemm(const uint16_t *act, int rows, int K, const uint8
     PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode_fn();
     if (!encode) return MOE_ERR_CUDA;
 
-    CUtensorMap tm_codes, tm_act, tm_act3;
+    CUtensorMap tm_codes, tm_act, tm_act3, tm_scales;
     {
         cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2),
                               static_cast<cuuint64_t>(E) * static_cast<cuuint64_t>(N)};
@@ -712,6 +742,23 @@ moe_status launch_grouped_gemm(const uint16_t *act, int rows, int K, const uint8
     } else {
         tm_act3 = tm_act;
     }
+    // Scale tiles: [E*N rows][K/32 bytes], boxes of 16 bytes (two code stages) x
+    // 128 rows, when the row pitch and the base allow 16-byte TMA rows.
+    const int scale_tma = (K % 512) == 0 && (reinterpret_cast<uintptr_t>(scales) & 15) == 0;
+    if (scale_tma) {
+        cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 32),
+                              static_cast<cuuint64_t>(E) * static_cast<cuuint64_t>(N)};
+        cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 32)};
+        cuuint32_t box[2] = {16, 128};
+        cuuint32_t estr[2] = {1, 1};
+        if (encode(&tm_scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(scales), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return MOE_ERR_CUDA;
+    } else {
+        tm_scales = tm_codes;
+    }
     static uint64_t attr_dev_mask = 0;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
@@ -739,7 +786,9 @@ moe_status launch_grouped_gemm(const uint16_t *act, int rows, int K, const uint8
     p.wait_limit_ns = wait_limit_ns;
     p.act_k8 = act_k8;
     p.act3d = act3d;
-    grouped_gemm_kernel<<<num_sms, kThreads, kSmemBytes, stream>>>(tm_codes, tm_act, tm_act3, p);
+    p.scale_tma = scale_tma;
+    grouped_gemm_kernel<<<num_sms, kThreads, kSmemBytes, stream>>>(tm_codes, tm_act, tm_act3,
+                                                                   tm_scales, p);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -275,13 +275,29 @@ def test_gemm_flags_inconsistent_group_sizes(B):
     assert torch.isnan(out).all()
 
 
-def test_gemm_flags_out_of_range_scale(B):
-    act, codes, scales, gs = _explicit([20], 128, 128)
+@pytest.mark.parametrize("K", [128, 512], ids=["scales_ldg", "scales_tma"])
+def test_gemm_flags_out_of_range_scale(B, K):
+    act, codes, scales, gs = _explicit([20], K, 128)
     scales[0, 7, 2] = 255
     ws = B.make_workspace(0, 1, 1, DEV)
     B.grouped_gemm(B.bf16_from_bits(act, DEV), B.to_device(codes, DEV), B.to_device(scales, DEV),
                    B.to_device(gs, DEV), workspace=ws)
     assert B.read_status(ws) == B.MOE_ERR_DATA
+
+
+@pytest.mark.parametrize("K", [256, 1024], ids=["scales_ldg", "scales_tma"])
+def test_gemm_ignores_scales_of_rows_beyond_n(B, K):
+    # N = 72: the 128-row weight tile of expert 0 also spans rows of expert 1,
+    # which is empty and carries out-of-range scale bytes.  Those rows are not
+    # part of any output, so no error may be flagged and expert 0 stays exact.
+    act, codes, scales, gs = _explicit([9, 0], K, 72)
+    scales[1] = 255
+    ws = B.make_workspace(0, 1, 1, DEV)
+    out = B.grouped_gemm(B.bf16_from_bits(act, DEV), B.to_device(codes, DEV), B.to_device(scales, DEV),
+                         B.to_device(gs, DEV), workspace=ws)
+    assert B.read_status(ws) == B.MOE_OK
+    ref, mag = oracle.grouped_gemm(act, codes, scales, gs)
+    _tol_check(out.cpu().numpy(), ref, mag, what="rows beyond N")
 
 
 def _sample_pairs(gs, N, n=3000, seed=0):
