@@ -46,6 +46,7 @@ namespace moe {
 namespace gemm {
 
 constexpr int kIssuerWarps = 4;               // warps 0..3: MMA issuers (lane 0)
+constexpr int kSingleIssuers = 2;             // single mode: issuers splitting the token columns
 constexpr int kConvWG = 4;                    // converter warpgroups: warps 4..19
 constexpr int kConvWarp0 = kIssuerWarps;
 constexpr int kActWarp = kConvWarp0 + 4 * kConvWG;    // warp 20: activation producer
@@ -187,7 +188,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
                     const __grid_constant__ CUtensorMap tm_act,
                     const __grid_constant__ CUtensorMap tm_act3,
-                    const __grid_constant__ CUtensorMap tm_scales, const Params p) {
+                    const __grid_constant__ CUtensorMap tm_scales,
+                    const __grid_constant__ CUtensorMap tm_act64, const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -277,7 +279,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
     // slot of the same stage.
     const int nt_max = *nt_max_slot;
     const bool split = nt_max <= kPartCols;
-    const uint32_t act_stage_bytes = static_cast<uint32_t>(nt_max) * 128u;   // one 64-k box
+    // One 64-k activation tile: split mode nt_max rows (16-row boxes); single
+    // mode nt_max rounded up to 64 rows (64-row boxes, one or two copies a stage).
+    const uint32_t act_stage_bytes =
+        static_cast<uint32_t>(nt_max <= kPartCols ? nt_max : (nt_max + 63) & ~63) * 128u;
     // Ring slot: codes (16 KB), [split: activation tile], [scale tile, loaded
     // with every even code stage for itself and the next one].
     const uint32_t scale_off = kCodeStageBytes + (split ? 4u * act_stage_bytes : 0u);
@@ -304,10 +309,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
         for (int i = 0; i < kSlotsMax; ++i) {
             mbar_init(&a_full[i], 4);
             mbar_init(&act_full[i], 1);
-            mbar_init(&slot_empty[i], 1);
+            mbar_init(&slot_empty[i], split ? 1 : kSingleIssuers);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&acc_full[i], split ? kIssuerWarps : 1);
+            mbar_init(&acc_full[i], split ? kIssuerWarps : kSingleIssuers);
             mbar_init(&acc_empty[i], 4 * kConvWG);
         }
         for (int i = 0; i < kIssuerWarps; ++i) mbar_init(&final_bar[i], 1);
@@ -324,23 +329,96 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
     if (warp < kIssuerWarps) {
         // ----------------------------------------------------------- MMA issuers
         // Split mode: issuer w issues the stages of converter warpgroup w
-        // (every 4th stage) into K-partial w.  Single mode: issuer 0 issues
-        // every stage into one accumulator.  The whole warp runs the loop (its
+        // (every 4th stage) into K-partial w.  Single mode: issuers 0 and 1 issue
+        // every stage, each for its own part of the item's token columns (the
+        // first a multiple of 16, about half), into one accumulator.  The whole warp runs the loop (its
         // values stay warp-uniform); one elected lane issues the MMAs and the
         // commits, always the same lane, so each commit covers its MMAs.
         const int w = warp;
-        if (split || w == 0) {
+        if (split || w < kSingleIssuers) {
             const uint32_t step = split ? kConvWG : 1u;
             uint32_t g = split ? w : 0;       // global stage index of this CTA
             int ks = static_cast<int>(g);     // stage within the item
             Item it = decode_item(blockIdx.x, roff, ioff, E, p.n_tiles);
-            uint32_t idesc = idesc_bf16_f32(128, it.nt);
+            // This issuer's token columns [c0, c0 + cn) of the item (single mode).
+            auto my_cols = [&](int nt, uint32_t &c0, uint32_t &cn) {
+                if (split) {
+                    c0 = 0;
+                    cn = nt;
+                    return;
+                }
+                const uint32_t half = ((nt / 2) + 15) & ~15;
+                c0 = w == 0 ? 0u : half;
+                cn = w == 0 ? half : nt - half;
+            };
+            uint32_t c0, cn;
+            my_cols(it.nt, c0, cn);
+            uint32_t idesc = idesc_bf16_f32(128, cn ? cn : 16);
             Ring ring;                        // split mode: code stage of this issuer's stage
             const uint32_t d_part = split ? w * part_cols : 0;
             Ring sr;                          // this issuer's A-slot sequence
             const uint32_t b_part = code_smem + kCodeStageBytes + w * act_stage_bytes;
             bool ok = true;
-            for (int i = 0; i < my_items && ok;) {
+            // Single mode: stages come in groups of four (KT is a multiple of 4), and
+            // the eight barriers of a group are probed together, so the probe
+            // latency is paid once per group; the MMAs of the four stages follow,
+            // each stage's slot released by its own commit.
+            constexpr int kGroup = 4;
+            for (int i = 0; i < my_items && ok && !split; ++i) {
+                const uint32_t buf = i & 1;
+                for (int kp = 0; kp < KT; kp += kGroup) {
+                    if (kp == 0 && !warp_wait_bounded(&acc_empty[buf], ((i >> 1) & 1) ^ 1,
+                                                      abort_flag, p.status, lim)) {
+                        ok = false;
+                        break;
+                    }
+                    uint32_t sl[kGroup], ph[kGroup];
+                    bool ready = true;
+#pragma unroll
+                    for (int h = 0; h < kGroup; ++h) {
+                        sl[h] = sr.slot;
+                        ph[h] = sr.phase;
+                        sr.next(kSlots);
+                        ready = ready & mbar_try_wait(&a_full[sl[h]], ph[h]) &
+                                mbar_try_wait(&act_full[sl[h]], ph[h]);
+                    }
+                    if (!__all_sync(0xffffffffu, ready)) {
+#pragma unroll
+                        for (int h = 0; h < kGroup; ++h)
+                            if (ok && (!warp_wait_bounded(&a_full[sl[h]], ph[h], abort_flag,
+                                                          p.status, lim) ||
+                                       !warp_wait_bounded(&act_full[sl[h]], ph[h], abort_flag,
+                                                          p.status, lim)))
+                                ok = false;
+                        if (!ok) break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + buf * acc_cols + c0;
+                    if (elect_one()) {
+#pragma unroll
+                        for (int h = 0; h < kGroup; ++h) {
+                            const uint32_t a_col = tmem_base + acol0 + sl[h] * kAColsPerSlot;
+                            const uint64_t b0 =
+                                smem_desc_sw128(act_smem + sl[h] * act_stage_bytes + c0 * 128);
+                            if (cn > 0)
+#pragma unroll
+                            for (int kk = 0; kk < kStageK / 16; ++kk)
+                                mma_bf16_ts(d_tmem, a_col + kk * 8,
+                                            b0 + static_cast<uint64_t>(kk * 2), idesc,
+                                            (kp == 0 && h == 0 && kk == 0) ? 0u : 1u);
+                            mma_commit(&slot_empty[sl[h]]);
+                        }
+                        if (kp + kGroup >= KT) mma_commit(&acc_full[buf]);
+                    }
+                    __syncwarp();
+                }
+                if (ok && i + 1 < my_items) {
+                    it = decode_item(blockIdx.x + (i + 1) * gridDim.x, roff, ioff, E, p.n_tiles);
+                    my_cols(it.nt, c0, cn);
+                    idesc = idesc_bf16_f32(128, cn ? cn : 16);
+                }
+            }
+            for (int i = 0; i < my_items && ok && split;) {
                 const uint32_t buf = i & 1;
                 const bool first = ks < static_cast<int>(step);
                 if (first && !warp_wait_bounded(&acc_empty[buf], ((i >> 1) & 1) ^ 1, abort_flag,
@@ -358,12 +436,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + buf * acc_cols + d_part;
+                const uint32_t d_tmem = tmem_base + buf * acc_cols + d_part + c0;
                 const uint32_t a_col = tmem_base + acol0 + slot * kAColsPerSlot;
                 const uint64_t b0 = smem_desc_sw128(split ? b_part + ring.slot * ring_stage_bytes
-                                                          : act_smem + slot * act_stage_bytes);
+                                                          : act_smem + slot * act_stage_bytes + c0 * 128);
                 const bool last = ks + static_cast<int>(step) >= KT;
                 if (elect_one()) {
+                    if (cn > 0)
 #pragma unroll
                     for (int kk = 0; kk < kStageK / 16; ++kk)
                         mma_bf16_ts(d_tmem, a_col + kk * 8, b0 + static_cast<uint64_t>(kk * 2),
@@ -381,7 +460,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
                     ks -= KT;
                     if (++i < my_items) {
                         it = decode_item(blockIdx.x + i * gridDim.x, roff, ioff, E, p.n_tiles);
-                        idesc = idesc_bf16_f32(128, it.nt);
+                        my_cols(it.nt, c0, cn);
+                        idesc = idesc_bf16_f32(128, cn ? cn : 16);
                     }
                 }
             }
@@ -450,7 +530,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
     } else if (warp == kActWarp) {
         // ------------------------------------- activation producer (single mode)
         if (lane == 0 && !split) {
-            tma_prefetch_map(&tm_act);
+            tma_prefetch_map(&tm_act64);
             Ring r;
             uint32_t issued = 0;
             bool ok = true;
@@ -461,10 +541,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&act_full[r.slot], static_cast<uint32_t>(it.nt) * 128u);
+                    const int groups = (it.nt + 63) / 64;
+                    mbar_arrive_expect_tx(&act_full[r.slot], static_cast<uint32_t>(groups) * 8192u);
                     const uint32_t dst = act_smem + r.slot * act_stage_bytes;
-                    for (int grp = 0; grp < it.nt / 16; ++grp)
-                        tma_load_2d(dst + grp * 2048, &tm_act, ks * kStageK, it.row0 + grp * 16,
+                    for (int grp = 0; grp < groups; ++grp)
+                        tma_load_2d(dst + grp * 8192, &tm_act64, ks * kStageK, it.row0 + grp * 64,
                                     &act_full[r.slot]);
                 }
             }
@@ -702,7 +783,7 @@ moe_status launch_grouped_gemm(const uint16_t *act, int rows, int K, const uint8
     PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode_fn();
     if (!encode) return MOE_ERR_CUDA;
 
-    CUtensorMap tm_codes, tm_act, tm_act3, tm_scales;
+    CUtensorMap tm_codes, tm_act, tm_act3, tm_scales, tm_act64;
     {
         cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2),
                               static_cast<cuuint64_t>(E) * static_cast<cuuint64_t>(N)};
@@ -721,6 +802,17 @@ moe_status launch_grouped_gemm(const uint16_t *act, int rows, int K, const uint8
         cuuint32_t box[2] = {64, 16};
         cuuint32_t estr[2] = {1, 1};
         if (encode(&tm_act, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(act), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return MOE_ERR_CUDA;
+    }
+    {   // 64-row boxes for wide bands
+        cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+        cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+        cuuint32_t box[2] = {64, 64};
+        cuuint32_t estr[2] = {1, 1};
+        if (encode(&tm_act64, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(act), dims,
                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -788,7 +880,7 @@ moe_status launch_grouped_gemm(const uint16_t *act, int rows, int K, const uint8
     p.act3d = act3d;
     p.scale_tma = scale_tma;
     grouped_gemm_kernel<<<num_sms, kThreads, kSmemBytes, stream>>>(tm_codes, tm_act, tm_act3,
-                                                                   tm_scales, p);
+                                                                   tm_scales, tm_act64, p);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
