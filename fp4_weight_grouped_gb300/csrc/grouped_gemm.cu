@@ -294,7 +294,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
     // <= 16 rows the K-partials need 16 columns each, which leaves room for
     // three A slots per warpgroup (more decode ahead of the MMAs); otherwise two.
     const bool narrow = split && nt_max <= 16;
-    const uint32_t per_wg = narrow ? 3u : 2u;              // A slots per warpgroup
+    const uint32_t per_wg = 2u;                            // A-slot sets in flight
     const uint32_t nslots = narrow ? kSlotsMax : kSlots;
     const uint32_t part_cols = narrow ? kPartCols / 2 : kPartCols;
     const uint32_t acc_cols = split ? kConvWG * part_cols : kAccCols;
@@ -304,7 +304,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
     if (tid == 0) {
         for (uint32_t i = 0; i < CS; ++i) {
             mbar_init(&code_full[i], 1);
-            mbar_init(&code_empty[i], 4 * kConvWG + (split ? kIssuerWarps : 0));
+            mbar_init(&code_empty[i], 4 * kConvWG / 2 + (split ? kIssuerWarps : 0));
         }
         for (int i = 0; i < kSlotsMax; ++i) {
             mbar_init(&a_full[i], 4);
@@ -497,13 +497,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
                 }
                 if (elect_one()) {
                     const uint32_t dst = code_smem + r.slot * ring_stage_bytes;
-                    const bool scales_here = p.scale_tma && (kc & 1) == 0;
+                    const bool scales_here = p.scale_tma != 0;
                     mbar_arrive_expect_tx(&code_full[r.slot],
                                           kCodeStageBytes + (split ? it.nt * 512u : 0u) +
                                               (scales_here ? kScaleTileBytes : 0u));
                     tma_load_2d(dst, &tm_codes, kc * 128, y, &code_full[r.slot]);
-                    if (scales_here)
-                        tma_load_2d(dst + scale_off, &tm_scales, kc * 8, y, &code_full[r.slot]);
+                    if (scales_here)   // 16 bytes a row: this code stage and its even/odd twin
+                        tma_load_2d(dst + scale_off, &tm_scales, (kc & ~1) * 8, y,
+                                    &code_full[r.slot]);
                     if (split) {
                         for (int grp = 0; grp < it.nt / 16; ++grp) {
                             if (use3d) {
@@ -557,38 +558,50 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
         }
     } else {
         // ------------------------------------------------ converters + epilogue
-        // Warpgroup wg handles the stages with index = wg (mod 4): for each, a
-        // thread reads the 32 code bytes of its weight row (TMEM lane), decodes
-        // them into 32 bf16 pairs (K8-interleaved reduction order) and stores
-        // them into the warpgroup's A slot for that stage.  The warpgroup also
-        // writes the output of item i - 2 when it starts item i (both
-        // accumulator buffers in flight), and of the last two items at the end.
+        // The warpgroups work in pairs on alternate code stages: warpgroups 0 and
+        // 1 on the even ones, 2 and 3 on the odd ones, each taking one 128-k half
+        // (sub-stages 2h and 2h + 1).  A thread reads the 64 code bytes of its
+        // weight row (TMEM lane) in the half, decodes them into 64 bf16 pairs
+        // (K8-interleaved reduction order) and stores them, 32 columns at a
+        // time, into the warpgroup's two A slots 2wg and 2wg + 1; the slots are
+        // reused every other code stage of the warpgroup.  Every warpgroup also
+        // writes its quarter of the token columns of item i - 2 once it has gone
+        // past item i - 1, and of the remaining items at the end.
         const int wg = (warp - kConvWarp0) >> 2;
+        const int pair = wg >> 1;                  // code-stage parity of this warpgroup
+        const int half = wg & 1;                   // which 128-k half of the code stage
         const int wtid = tid - 32 * kConvWarp0 - 128 * wg;   // 0..127 within the warpgroup
         const int q = warp & 3;                    // TMEM lane quarter = warp within the group
         const int row = q * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-        const uint32_t a_base = tmem_base + lane_off + acol0;
+        const uint32_t slot0 = 2u * wg;            // A slots 2wg, 2wg + 1
+        const uint32_t a_base = tmem_base + lane_off + acol0 + slot0 * kAColsPerSlot;
         const int KT4 = KT / 4;
+        // This row's four swizzled 16-byte chunks of the half.
+        uint32_t chunk_off[4];
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch)
+            chunk_off[ch] = row * 128 + (((4 * half + ch) ^ (row & 7)) << 4);
         int bad_scale = 0;
         bool ok = true;
-        Ring code;
-        Ring sr;                                   // this warpgroup's A-slot sequence
-        // Scale bytes of item stage 4m + wg for this row: bytes 8m + 2wg and
-        // 8m + 2wg + 1 of the row.  A tile row beyond N reads row N - 1 (its
-        // codes are zero-filled, so the value never matters).
+        // Scale bytes of code stage m for this row and half: blocks 8m + 4h ..
+        // 8m + 4h + 3 of the row.  A tile row beyond N reads row N - 1 (its codes
+        // are zero-filled, so the value never matters).
         auto scale_base = [&](int j) -> const uint8_t * {
             const Item it = decode_item(blockIdx.x + j * gridDim.x, roff, ioff, E, p.n_tiles);
             const int n = min(it.n0 + row, p.N - 1);
-            return p.scales + (static_cast<size_t>(it.e) * p.N + n) * p.scale_row + 2 * wg;
+            return p.scales + (static_cast<size_t>(it.e) * p.N + n) * p.scale_row + 4 * half;
         };
         auto load_scales = [&](const uint8_t *sb, int m) -> uint32_t {
-            if (p.scale_full) return __ldg(reinterpret_cast<const uint16_t *>(sb + 8 * m));
-            const int blk = 8 * m + 2 * wg;
-            const uint32_t s0 = blk < p.scale_row ? static_cast<uint32_t>(__ldg(sb + 8 * m)) : 127u;
-            const uint32_t s1 =
-                blk + 1 < p.scale_row ? static_cast<uint32_t>(__ldg(sb + 8 * m + 1)) : 127u;
-            return s0 | (s1 << 8);
+            uint32_t v = 0;
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                const int blk = 8 * m + 4 * half + b;
+                const uint32_t sbyte =
+                    blk < p.scale_row ? static_cast<uint32_t>(__ldg(sb + 8 * m + b)) : 127u;
+                v |= sbyte << (8 * b);
+            }
+            return v;
         };
         auto epilogue = [&](int i) -> bool {
             const uint32_t buf = i & 1;
@@ -602,108 +615,129 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
             if (lane == 0) mbar_arrive(&acc_empty[buf]);
             return true;
         };
-        int cur_nt = decode_item(blockIdx.x, roff, ioff, E, p.n_tiles).nt;
-        const uint8_t *sb = scale_base(0);
-        uint32_t sw_next = p.scale_tma ? 0u : load_scales(sb, 0);
-        uint32_t sw_stash = 0;
-        // Scale bytes that belong to a tile row beyond N (read with the tile) never
-        // count as errors: those rows are not part of the output.
-        bool row_ok = decode_item(blockIdx.x, roff, ioff, E, p.n_tiles).n0 + row < p.N;
-        for (int i = 0; i < my_items && ok; ++i) {
-            if (i >= 2 && !epilogue(i - 2)) {
+        const uint32_t total_cs = static_cast<uint32_t>(my_items) * KT4;
+        Ring code;                                 // ring position of code stage c
+        if (pair) code.next(CS);
+        uint32_t sphase = 0;                       // A-slot phase: (c / 2) & 1
+        int i = pair / KT4, m = pair % KT4;        // item and code stage within it
+        int ep_next = 0;                           // next item whose output this warp writes
+        int cur_nt = 0;
+        bool row_ok = false;
+        const uint8_t *sb = nullptr;
+        auto enter_item = [&](int it_idx) {
+            const Item it = decode_item(blockIdx.x + it_idx * gridDim.x, roff, ioff, E, p.n_tiles);
+            cur_nt = it.nt;
+            // Scale bytes of a tile row beyond N (read with the tile) never count
+            // as errors: those rows are not part of the output.
+            row_ok = it.n0 + row < p.N;
+            if (!p.scale_tma) sb = scale_base(it_idx);
+        };
+        if (i < my_items) enter_item(i);
+        for (uint32_t c = pair; c < total_cs && ok; c += 2) {
+            // Probe the code stage and both A slots together (one round trip when
+            // all are ready, the usual case); wait for each otherwise.
+            const bool ready = __all_sync(
+                0xffffffffu, mbar_try_wait(&code_full[code.slot], code.phase) &
+                                 mbar_try_wait(&slot_empty[slot0], sphase ^ 1u) &
+                                 mbar_try_wait(&slot_empty[slot0 + 1], sphase ^ 1u));
+            if (!ready && !warp_wait_bounded(&code_full[code.slot], code.phase, abort_flag,
+                                             p.status, lim)) {
                 ok = false;
                 break;
             }
-            const uint8_t *sb_next = p.scale_tma ? sb : scale_base(i + 1 < my_items ? i + 1 : i);
-            for (int m = 0; m < KT4; ++m, sr.next(per_wg), code.next(CS)) {
-                uint32_t sw = sw_next;
-                // Scales one stage ahead (the next item's first stage at the end).
-                if (!p.scale_tma)
-                    sw_next = m + 1 < KT4 ? load_scales(sb, m + 1) : load_scales(sb_next, 0);
-                if (!warp_wait_bounded(&code_full[code.slot], code.phase, abort_flag, p.status,
-                                       lim)) {
+            uint8_t *slot_base = smem + kOffCode + code.slot * ring_stage_bytes;
+            const uint32_t sw =
+                p.scale_tma ? *reinterpret_cast<const uint32_t *>(slot_base + scale_off + row * 16 +
+                                                                  (m & 1) * 8 + 4 * half)
+                            : load_scales(sb, m);
+            uint32_t cw[4][4];
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                const uint4 v = *reinterpret_cast<const uint4 *>(slot_base + chunk_off[ch]);
+                cw[ch][0] = v.x;
+                cw[ch][1] = v.y;
+                cw[ch][2] = v.z;
+                cw[ch][3] = v.w;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&code_empty[code.slot]);
+            if (!p.act_k8) {
+                // Interleave every 16-byte chunk of the two sub-stages' activation
+                // rows in place (the permutation stays inside a chunk, so the
+                // swizzle of the tile does not matter).
+                if (!split &&
+                    (!warp_wait_bounded(&act_full[slot0], sphase, abort_flag, p.status, lim) ||
+                     !warp_wait_bounded(&act_full[slot0 + 1], sphase, abort_flag, p.status,
+                                        lim))) {
                     ok = false;
                     break;
                 }
-                if (p.scale_tma) {
-                    // Even code stage: this row's scale bytes for it and the next.
-                    if ((m & 1) == 0) {
-                        const uint16_t *sp = reinterpret_cast<const uint16_t *>(
-                            smem + kOffCode + code.slot * ring_stage_bytes + scale_off + row * 16) + wg;
-                        sw = sp[0];
-                        sw_stash = sp[4];
-                    } else {
-                        sw = sw_stash;
-                    }
-                }
-                // This row's 32 code bytes of the stage (2 chunks of 16, 128-byte swizzle).
-                uint32_t cw[2][4];
-                const uint8_t *crow = smem + kOffCode + code.slot * ring_stage_bytes + row * 128;
 #pragma unroll
-                for (int ch = 0; ch < 2; ++ch) {
-                    const uint4 v = *reinterpret_cast<const uint4 *>(
-                        crow + (((2 * wg + ch) ^ (row & 7)) << 4));
-                    cw[ch][0] = v.x;
-                    cw[ch][1] = v.y;
-                    cw[ch][2] = v.z;
-                    cw[ch][3] = v.w;
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&code_empty[code.slot]);
-                const uint32_t slot = static_cast<uint32_t>(wg) + kConvWG * sr.slot;
-                const uint32_t spar = sr.phase;
-                if (!p.act_k8) {
-                    // Interleave every 16-byte chunk of the stage's activation rows in
-                    // place (the permutation stays inside a chunk, so the swizzle of
-                    // the tile does not matter).
-                    if (!split &&
-                        !warp_wait_bounded(&act_full[slot], spar, abort_flag, p.status, lim)) {
-                        ok = false;
-                        break;
-                    }
+                for (int h = 0; h < 2; ++h) {
                     uint4 *abase = reinterpret_cast<uint4 *>(
-                        split ? smem + kOffCode + code.slot * ring_stage_bytes + kCodeStageBytes +
-                                    wg * act_stage_bytes
-                              : smem + act_off + slot * act_stage_bytes);
-                    for (int c = wtid; c < cur_nt * 8; c += 128) abase[c] = interleave8(abase[c]);
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                        split ? slot_base + kCodeStageBytes + (2 * half + h) * act_stage_bytes
+                              : smem + act_off + (slot0 + h) * act_stage_bytes);
+                    for (int cc = wtid; cc < cur_nt * 8; cc += 128)
+                        abase[cc] = interleave8(abase[cc]);
                 }
-                // Scale bytes 0..128 take one bf16 FMA, 129..252 two, 253..255 are
-                // errors; the warp agrees on the path.
-                const uint32_t s_lo = sw & 0xFFu, s_hi = sw >> 8;
-                const bool slow = __any_sync(0xffffffffu, max(s_lo, s_hi) > 128u);
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            }
+            // Scale bytes 0..128 take one bf16 FMA, 129..252 two, 253..255 are
+            // errors; the warp agrees on the path.  A byte is above 128 exactly
+            // when its top bit and one of its low seven bits are set.
+            const uint32_t big = sw & ((sw & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) & 0x80808080u;
+            const bool slow = __any_sync(0xffffffffu, big != 0);
+            if (!ready &&
+                (!warp_wait_bounded(&slot_empty[slot0], sphase ^ 1u, abort_flag, p.status, lim) ||
+                 !warp_wait_bounded(&slot_empty[slot0 + 1], sphase ^ 1u, abort_flag, p.status,
+                                    lim))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {          // sub-stage 2·half + h -> A slot slot0 + h
                 uint32_t o[32];
                 if (!slow) {
-                    decode32_single(cw[0], scale_pair_single(s_lo), &o[0]);
-                    decode32_single(cw[1], scale_pair_single(s_hi), &o[16]);
+                    decode32_single(cw[2 * h], scale_pair_single((sw >> (16 * h)) & 0xFFu), &o[0]);
+                    decode32_single(cw[2 * h + 1], scale_pair_single((sw >> (16 * h + 8)) & 0xFFu),
+                                    &o[16]);
                 } else {
-                    if (!decode32_any(cw[0], s_lo, &o[0]) && row_ok) bad_scale = 1;
-                    if (!decode32_any(cw[1], s_hi, &o[16]) && row_ok) bad_scale = 1;
+                    if (!decode32_any(cw[2 * h], (sw >> (16 * h)) & 0xFFu, &o[0]) && row_ok)
+                        bad_scale = 1;
+                    if (!decode32_any(cw[2 * h + 1], (sw >> (16 * h + 8)) & 0xFFu, &o[16]) && row_ok)
+                        bad_scale = 1;
                 }
-                if (!warp_wait_bounded(&slot_empty[slot], spar ^ 1u, abort_flag, p.status, lim)) {
-                    ok = false;
-                    break;
+                __syncwarp();
+                tmem_st32(a_base + h * kAColsPerSlot, o);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&a_full[slot0]);
+                mbar_arrive(&a_full[slot0 + 1]);
+            }
+            // Next code stage of this pair: c + 2.
+            code.next(CS);
+            code.next(CS);
+            sphase ^= 1u;
+            m += 2;
+            while (m >= KT4) {
+                m -= KT4;
+                ++i;
+                while (ok && ep_next <= i - 2) {
+                    if (!epilogue(ep_next)) ok = false;
+                    ++ep_next;
                 }
-                tc_fence_after();
-                __syncwarp();
-                tmem_st16(a_base + slot * kAColsPerSlot, *reinterpret_cast<uint32_t(*)[16]>(&o[0]));
-                tmem_st16(a_base + slot * kAColsPerSlot + 16,
-                          *reinterpret_cast<uint32_t(*)[16]>(&o[16]));
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&a_full[slot]);
+                if (i < my_items) enter_item(i);
             }
-            if (i + 1 < my_items) {
-                const Item nx = decode_item(blockIdx.x + (i + 1) * gridDim.x, roff, ioff, E, p.n_tiles);
-                cur_nt = nx.nt;
-                row_ok = nx.n0 + row < p.N;
-            }
-            sb = sb_next;
         }
-        // Outputs of the last two items.
-        if (ok && my_items >= 2 && !epilogue(my_items - 2)) ok = false;
-        if (ok && !epilogue(my_items - 1)) ok = false;
+        // Outputs of the items not written yet.
+        while (ok && ep_next < my_items) {
+            if (!epilogue(ep_next)) ok = false;
+            ++ep_next;
+        }
         if (bad_scale) set_status(p.status, MOE_ERR_DATA);
     }
 
