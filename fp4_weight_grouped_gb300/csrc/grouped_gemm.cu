@@ -426,12 +426,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
                     ok = false;
                     break;
                 }
-                const uint32_t slot = split ? w + kConvWG * sr.slot : sr.slot, par = sr.phase;
-                if (!warp_wait_bounded(&a_full[slot], par, abort_flag, p.status, lim) ||
-                    !(split ? warp_wait_bounded(&code_full[ring.slot], ring.phase, abort_flag,
-                                                p.status, lim)
-                            : warp_wait_bounded(&act_full[slot], par, abort_flag, p.status,
-                                                lim))) {
+                const uint32_t slot = w + kConvWG * sr.slot, par = sr.phase;
+                // One probe for both barriers (the usual case: both complete).
+                const bool ready =
+                    __all_sync(0xffffffffu, mbar_try_wait(&a_full[slot], par) &
+                                                mbar_try_wait(&code_full[ring.slot], ring.phase));
+                if (!ready &&
+                    (!warp_wait_bounded(&a_full[slot], par, abort_flag, p.status, lim) ||
+                     !warp_wait_bounded(&code_full[ring.slot], ring.phase, abort_flag, p.status,
+                                        lim))) {
                     ok = false;
                     break;
                 }
