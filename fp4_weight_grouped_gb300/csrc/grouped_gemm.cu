@@ -636,15 +636,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
             if (!p.scale_tma) sb = scale_base(it_idx);
         };
         if (i < my_items) enter_item(i);
+        // Barrier tests are issued ahead of their use (non-blocking), so their
+        // latency hides behind the decode: the next code stage's at the start of
+        // this stage's decode, this stage's A slots just before it.  A test that
+        // fails falls back to the bounded wait.
+        bool code_ready = false;
         for (uint32_t c = pair; c < total_cs && ok; c += 2) {
-            // Probe the code stage and both A slots together (one round trip when
-            // all are ready, the usual case); wait for each otherwise.
-            const bool ready = __all_sync(
-                0xffffffffu, mbar_try_wait(&code_full[code.slot], code.phase) &
-                                 mbar_try_wait(&slot_empty[slot0], sphase ^ 1u) &
-                                 mbar_try_wait(&slot_empty[slot0 + 1], sphase ^ 1u));
-            if (!ready && !warp_wait_bounded(&code_full[code.slot], code.phase, abort_flag,
-                                             p.status, lim)) {
+            if (!__all_sync(0xffffffffu, code_ready) &&
+                !warp_wait_bounded(&code_full[code.slot], code.phase, abort_flag, p.status,
+                                   lim)) {
                 ok = false;
                 break;
             }
@@ -685,12 +685,20 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
                 }
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             }
+            const bool slots_ready = mbar_test_wait(&slot_empty[slot0], sphase ^ 1u) &
+                                     mbar_test_wait(&slot_empty[slot0 + 1], sphase ^ 1u);
+            {
+                Ring nx = code;
+                nx.next(CS);
+                nx.next(CS);
+                code_ready = c + 2 < total_cs && mbar_test_wait(&code_full[nx.slot], nx.phase);
+            }
             // Scale bytes 0..128 take one bf16 FMA, 129..252 two, 253..255 are
             // errors; the warp agrees on the path.  A byte is above 128 exactly
             // when its top bit and one of its low seven bits are set.
             const uint32_t big = sw & ((sw & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) & 0x80808080u;
             const bool slow = __any_sync(0xffffffffu, big != 0);
-            if (!ready &&
+            if (!__all_sync(0xffffffffu, slots_ready) &&
                 (!warp_wait_bounded(&slot_empty[slot0], sphase ^ 1u, abort_flag, p.status, lim) ||
                  !warp_wait_bounded(&slot_empty[slot0 + 1], sphase ^ 1u, abort_flag, p.status,
                                     lim))) {
