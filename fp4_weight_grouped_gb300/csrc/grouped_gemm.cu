@@ -709,10 +709,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
 #pragma unroll
             for (int h = 0; h < 2; ++h) {          // sub-stage 2·half + h -> A slot slot0 + h
                 uint32_t o[32];
-                if (!slow) {
-                    decode32_single(cw[2 * h], scale_pair_single((sw >> (16 * h)) & 0xFFu), &o[0]);
-                    decode32_single(cw[2 * h + 1], scale_pair_single((sw >> (16 * h + 8)) & 0xFFu),
-                                    &o[16]);
+                if (__builtin_expect(!slow, 1)) {
+                    // Scale byte b of sw in both 16-bit halves, then 2^(s-1) as bf16x2.
+                    const uint32_t sp0 = prmt(sw, 0u, h ? 0x4242u : 0x4040u);
+                    const uint32_t sp1 = prmt(sw, 0u, h ? 0x4343u : 0x4141u);
+                    decode32_single(cw[2 * h], sp0 * 0x80u + 0x3F003F00u, &o[0]);
+                    decode32_single(cw[2 * h + 1], sp1 * 0x80u + 0x3F003F00u, &o[16]);
                 } else {
                     if (!decode32_any(cw[2 * h], (sw >> (16 * h)) & 0xFFu, &o[0]) && row_ok)
                         bad_scale = 1;
