@@ -45,13 +45,13 @@
 namespace moe {
 namespace gemm {
 
-constexpr int kIssuerWarps = 4;               // warps 0..3: MMA issuers (lane 0)
+constexpr int kIssuerWarps = 2;               // warps 0..1: MMA issuers (one elected lane each)
 constexpr int kSingleIssuers = 2;             // single mode: issuers splitting the token columns
-constexpr int kConvWG = 4;                    // converter warpgroups: warps 4..19
+constexpr int kConvWG = 4;                    // converter warpgroups: warps 2..17
 constexpr int kConvWarp0 = kIssuerWarps;
-constexpr int kActWarp = kConvWarp0 + 4 * kConvWG;    // warp 20: activation producer
-constexpr int kCodeWarp = kActWarp + 1;               // warp 21: code producer
-constexpr int kThreads = 32 * (kCodeWarp + 1);        // 704
+constexpr int kActWarp = kConvWarp0 + 4 * kConvWG;    // warp 18: activation producer
+constexpr int kCodeWarp = kActWarp + 1;               // warp 19: code producer
+constexpr int kThreads = 32 * (kCodeWarp + 1);        // 640
 constexpr int kBN = 128;                      // output columns per tile (MMA M)
 constexpr int kMaxNT = 128;                   // tokens per work item (MMA N)
 constexpr int kStageK = 64;                   // K per decode / MMA stage
@@ -154,16 +154,12 @@ __device__ __forceinline__ void store_item(const Params &p, const Item &it, uint
         __syncwarp();
         tmem_ld4(acc_base + c, v);
         if (split) {
-            uint32_t u1[4], u2[4], u3[4];
+            uint32_t u1[4];
             tmem_ld4(acc_base + part_cols + c, u1);
-            tmem_ld4(acc_base + 2 * part_cols + c, u2);
-            tmem_ld4(acc_base + 3 * part_cols + c, u3);
             tmem_ld_wait();
 #pragma unroll
             for (int t = 0; t < 4; ++t)
-                v[t] = __float_as_uint(((__uint_as_float(v[t]) + __uint_as_float(u1[t])) +
-                                        __uint_as_float(u2[t])) +
-                                       __uint_as_float(u3[t]));
+                v[t] = __float_as_uint(__uint_as_float(v[t]) + __uint_as_float(u1[t]));
         } else {
             tmem_ld_wait();
         }
@@ -297,7 +293,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
     const uint32_t per_wg = 2u;                            // A-slot sets in flight
     const uint32_t nslots = narrow ? kSlotsMax : kSlots;
     const uint32_t part_cols = narrow ? kPartCols / 2 : kPartCols;
-    const uint32_t acc_cols = split ? kConvWG * part_cols : kAccCols;
+    const uint32_t acc_cols = split ? kIssuerWarps * part_cols : kAccCols;
     const uint32_t acol0 = 2 * acc_cols;
 
     if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
@@ -336,9 +332,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
         // commits, always the same lane, so each commit covers its MMAs.
         const int w = warp;
         if (split || w < kSingleIssuers) {
-            const uint32_t step = split ? kConvWG : 1u;
-            uint32_t g = split ? w : 0;       // global stage index of this CTA
-            int ks = static_cast<int>(g);     // stage within the item
             Item it = decode_item(blockIdx.x, roff, ioff, E, p.n_tiles);
             // This issuer's token columns [c0, c0 + cn) of the item (single mode).
             auto my_cols = [&](int nt, uint32_t &c0, uint32_t &cn) {
@@ -357,7 +350,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
             Ring ring;                        // split mode: code stage of this issuer's stage
             const uint32_t d_part = split ? w * part_cols : 0;
             Ring sr;                          // this issuer's A-slot sequence
-            const uint32_t b_part = code_smem + kCodeStageBytes + w * act_stage_bytes;
             bool ok = true;
             // Single mode: stages come in groups of four (KT is a multiple of 4), and
             // the eight barriers of a group are probed together, so the probe
@@ -418,54 +410,57 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
                     idesc = idesc_bf16_f32(128, cn ? cn : 16);
                 }
             }
-            for (int i = 0; i < my_items && ok && split;) {
+            // Split mode: issuer w issues sub-stages 2w and 2w + 1 of every code
+            // stage (8 MMAs, in k order) into its K-partial w.
+            for (int i = 0; i < my_items && ok && split; ++i) {
                 const uint32_t buf = i & 1;
-                const bool first = ks < static_cast<int>(step);
-                if (first && !warp_wait_bounded(&acc_empty[buf], ((i >> 1) & 1) ^ 1, abort_flag,
-                                                p.status, lim)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t slot = w + kConvWG * sr.slot, par = sr.phase;
-                // One probe for both barriers (the usual case: both complete).
-                const bool ready =
-                    __all_sync(0xffffffffu, mbar_try_wait(&a_full[slot], par) &
-                                                mbar_try_wait(&code_full[ring.slot], ring.phase));
-                if (!ready &&
-                    (!warp_wait_bounded(&a_full[slot], par, abort_flag, p.status, lim) ||
-                     !warp_wait_bounded(&code_full[ring.slot], ring.phase, abort_flag, p.status,
-                                        lim))) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t d_tmem = tmem_base + buf * acc_cols + d_part + c0;
-                const uint32_t a_col = tmem_base + acol0 + slot * kAColsPerSlot;
-                const uint64_t b0 = smem_desc_sw128(split ? b_part + ring.slot * ring_stage_bytes
-                                                          : act_smem + slot * act_stage_bytes + c0 * 128);
-                const bool last = ks + static_cast<int>(step) >= KT;
-                if (elect_one()) {
-                    if (cn > 0)
-#pragma unroll
-                    for (int kk = 0; kk < kStageK / 16; ++kk)
-                        mma_bf16_ts(d_tmem, a_col + kk * 8, b0 + static_cast<uint64_t>(kk * 2),
-                                    idesc, (first && kk == 0) ? 0u : 1u);
-                    mma_commit(&slot_empty[slot]);
-                    if (split) mma_commit(&code_empty[ring.slot]);
-                    if (last) mma_commit(&acc_full[buf]);
-                }
-                __syncwarp();
-                if (split) ring.next(CS);
-                sr.next(split ? per_wg : kSlots);
-                g += step;
-                ks += static_cast<int>(step);
-                if (last) {
-                    ks -= KT;
-                    if (++i < my_items) {
-                        it = decode_item(blockIdx.x + i * gridDim.x, roff, ioff, E, p.n_tiles);
-                        my_cols(it.nt, c0, cn);
-                        idesc = idesc_bf16_f32(128, cn ? cn : 16);
+                for (int m = 0; m < KT / 4; ++m) {
+                    if (m == 0 && !warp_wait_bounded(&acc_empty[buf], ((i >> 1) & 1) ^ 1,
+                                                     abort_flag, p.status, lim)) {
+                        ok = false;
+                        break;
                     }
+                    const uint32_t s0 = 2u * w + 4u * sr.slot, par = sr.phase;   // sub-stage 2w at slot set
+                    // One probe for the three barriers (the usual case: all complete).
+                    const bool ready = __all_sync(
+                        0xffffffffu, mbar_try_wait(&a_full[s0], par) &
+                                         mbar_try_wait(&a_full[s0 + 1], par) &
+                                         mbar_try_wait(&code_full[ring.slot], ring.phase));
+                    if (!ready &&
+                        (!warp_wait_bounded(&a_full[s0], par, abort_flag, p.status, lim) ||
+                         !warp_wait_bounded(&a_full[s0 + 1], par, abort_flag, p.status, lim) ||
+                         !warp_wait_bounded(&code_full[ring.slot], ring.phase, abort_flag,
+                                            p.status, lim))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + buf * acc_cols + d_part;
+                    const uint32_t b_base = code_smem + ring.slot * ring_stage_bytes +
+                                            kCodeStageBytes + 2u * w * act_stage_bytes;
+                    if (elect_one()) {
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const uint32_t a_col = tmem_base + acol0 + (s0 + h) * kAColsPerSlot;
+                            const uint64_t b0 = smem_desc_sw128(b_base + h * act_stage_bytes);
+#pragma unroll
+                            for (int kk = 0; kk < kStageK / 16; ++kk)
+                                mma_bf16_ts(d_tmem, a_col + kk * 8,
+                                            b0 + static_cast<uint64_t>(kk * 2), idesc,
+                                            (m == 0 && h == 0 && kk == 0) ? 0u : 1u);
+                            mma_commit(&slot_empty[s0 + h]);
+                        }
+                        mma_commit(&code_empty[ring.slot]);
+                        if (m + 1 == KT / 4) mma_commit(&acc_full[buf]);
+                    }
+                    __syncwarp();
+                    ring.next(CS);
+                    sr.next(per_wg);
+                }
+                if (ok && i + 1 < my_items) {
+                    it = decode_item(blockIdx.x + (i + 1) * gridDim.x, roff, ioff, E, p.n_tiles);
+                    my_cols(it.nt, c0, cn);
+                    idesc = idesc_bf16_f32(128, cn ? cn : 16);
                 }
             }
             // All MMAs issued by the elected lane must finish before TMEM is freed.
