@@ -11,21 +11,23 @@
 //    operand, held in tensor memory; the band's token rows are the B operand
 //    in shared memory (MMA N = 16..128).  Decode-sized bands thus fill the
 //    128-wide tensor-core dimension with weights, not with padding.
-//  * TMA streams the packed codes in 256-k stages (128 rows x 128 bytes,
-//    128-byte swizzle: wide rows move at about twice the rate of 64-byte
-//    ones) and the activation rows (64-element boxes) into shared memory.
-//  * Four converter warpgroups each own every 4th 64-k decode stage: they read
-//    their 32 code bytes per row, decode them to bf16 pairs and write them into
-//    one of eight tensor-memory A slots with tcgen05.st.  A slot and the
-//    activation tile of the same stage are released together by one
-//    tcgen05.commit.
-//  * Split mode (every band <= 32 rows): two issuer threads on different SM
-//    sub-partitions (one thread issues a small MMA only every ~50 cycles) each
-//    take every 2nd stage, accumulating into four per-warpgroup K-partial
-//    accumulators that the epilogue adds in a fixed order.  Single mode
-//    (wider bands): one issuer, one accumulator; N up to 128 keeps the tensor
-//    core busy.  Accumulators are double-buffered so the epilogue of one work
-//    item overlaps the next.
+//  * A ring of code stages in shared memory, filled by TMA: each holds the
+//    codes of 128 rows x 256 k (128-byte swizzle), the block-scale bytes when
+//    K % 512 == 0, and for narrow bands the band's activation tile of the same
+//    256 k, so activations arrive as early as the codes.  Wider bands take
+//    their activations through eight 64-k slots of their own.
+//  * Four converter warpgroups decode in pairs on alternate code stages: each
+//    warpgroup takes one 128-k half; a thread reads the 64 code bytes of its
+//    weight row, decodes them to bf16 pairs on the ALU and FMA pipes and
+//    writes them into the warpgroup's two tensor-memory A slots (tcgen05.st).
+//  * Split mode (every band <= 32 rows): two issuer warps, each issuing two
+//    adjacent 64-k sub-stages of every code stage into its own K-partial
+//    accumulator; the epilogue adds the partials in a fixed order (one issuer
+//    thread issues a small MMA only about every 50 cycles, so the work is
+//    shared).  Single mode (wider bands): the two issuers split the token
+//    columns of one accumulator and take four stages per barrier probe.
+//    Accumulators are double-buffered so the epilogue of one work item (done
+//    by the converter warps) overlaps the next item.
 //  * Persistent CTAs (one per SM) walk a static list of work items (expert,
 //    128-token chunk, 128-column tile) built on the device from group_sizes;
 //    empty experts contribute no items and their weights are never read.
