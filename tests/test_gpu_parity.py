@@ -216,6 +216,10 @@ GEMM_CASES = {
     "split_k_tail_544": lambda: _explicit([2, 11, 0, 30], 544, 136),     # K/32 = 17 scale bytes per row
     "split_k_96": lambda: _explicit([3, 0, 8], 96, 128),                 # one partial code stage
     "split_one_row_experts": lambda: _explicit(np.ones(40, np.int32), 2048, 256),
+    # the largest expert count: 1024 experts, 300 of them with one row, the rest empty
+    "max_experts_sparse": lambda: _explicit(
+        np.isin(np.arange(1024), np.random.default_rng(4).choice(1024, 300, replace=False))
+        .astype(np.int32), 256, 128),
 }
 
 
