@@ -63,7 +63,8 @@ constexpr int kCodeK = 256;                   // K per code stage (4 decode stag
 constexpr int kCodeStageBytes = kBN * kCodeK / 2;         // 16 KB
 constexpr int kCodeStagesMax = 12;
 constexpr int kScaleTileBytes = 128 * 16;     // scale bytes of two code stages (512 k) x 128 rows
-constexpr int kRingBytes = 216 * 1024;        // code ring + activation tiles
+constexpr int kRingBytes = 214 * 1024;        // code ring + activation tiles
+constexpr int kItemCache = 128;               // work items of a CTA kept decoded in shared memory
 constexpr int kTmemCols = 512;
 constexpr int kAccCols = 128;                 // per accumulator buffer
 constexpr int kACol0 = 2 * kAccCols;          // A slots after the two accumulator buffers
@@ -77,9 +78,11 @@ constexpr int kOffItemOff = kOffRowOff + (kMaxE + 1) * 4;
 constexpr int kOffBars = (kOffItemOff + (kMaxE + 1) * 4 + 7) & ~7;
 constexpr int kNumBars = 2 * kCodeStagesMax + 3 * kSlotsMax + 2 * 2 + kIssuerWarps;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
-constexpr int kSmemBytes = kOffMisc + 64 + 1024;          // + alignment slack
+constexpr int kOffItems = (kOffMisc + 64 + 15) & ~15;     // int4 per cached work item (16-aligned)
+constexpr int kSmemBytes = kOffItems + kItemCache * 16 + 1024;   // + alignment slack
 
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kOffItems % 16 == 0, "the item table holds int4 entries");
 static_assert(kCodeStageBytes % 1024 == 0, "ring slots keep the 1024-byte swizzle alignment");
 static_assert(kOffBars % 8 == 0, "barrier alignment");
 static_assert(kACol0 + kSlots * kAColsPerSlot <= kTmemCols, "TMEM budget");
@@ -206,6 +209,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 8);
     int *bad_flag = reinterpret_cast<int *>(smem + kOffMisc + 16);
     int *nt_max_slot = reinterpret_cast<int *>(smem + kOffMisc + 24);
+    int4 *item_cache = reinterpret_cast<int4 *>(smem + kOffItems);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -265,6 +269,23 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
     const int total_items = ioff[E];
     if (static_cast<int>(blockIdx.x) >= total_items) return;
     const int my_items = (total_items - static_cast<int>(blockIdx.x) + gridDim.x - 1) / gridDim.x;
+    // The CTA's first kItemCache work items, decoded once (visible after the
+    // barrier set-up's __syncthreads below); later ones are decoded on demand.
+    for (int t = tid; t < my_items && t < kItemCache; t += kThreads) {
+        const Item it = decode_item(blockIdx.x + t * gridDim.x, roff, ioff, E, p.n_tiles);
+        item_cache[t] = make_int4(it.e, it.row0, it.n0, it.nvalid | (it.nt << 16));
+    }
+    auto get_item = [&](int i) -> Item {
+        if (i >= kItemCache) return decode_item(blockIdx.x + i * gridDim.x, roff, ioff, E, p.n_tiles);
+        const int4 v = item_cache[i];
+        Item it;
+        it.e = v.x;
+        it.row0 = v.y;
+        it.n0 = v.z;
+        it.nvalid = v.w & 0xFFFF;
+        it.nt = v.w >> 16;
+        return it;
+    };
     const int KT = p.k_stages;                  // multiple of 4
     // Split mode: every band <= 32 rows.  Four issuers, one per converter
     // warpgroup, each accumulating its warpgroup's stages into its own
@@ -334,7 +355,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
         // commits, always the same lane, so each commit covers its MMAs.
         const int w = warp;
         if (split || w < kSingleIssuers) {
-            Item it = decode_item(blockIdx.x, roff, ioff, E, p.n_tiles);
+            Item it = get_item(0);
             // This issuer's token columns [c0, c0 + cn) of the item (single mode).
             auto my_cols = [&](int nt, uint32_t &c0, uint32_t &cn) {
                 if (split) {
@@ -407,7 +428,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
                     __syncwarp();
                 }
                 if (ok && i + 1 < my_items) {
-                    it = decode_item(blockIdx.x + (i + 1) * gridDim.x, roff, ioff, E, p.n_tiles);
+                    it = get_item(i + 1);
                     my_cols(it.nt, c0, cn);
                     idesc = idesc_bf16_f32(128, cn ? cn : 16);
                 }
@@ -460,7 +481,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
                     sr.next(per_wg);
                 }
                 if (ok && i + 1 < my_items) {
-                    it = decode_item(blockIdx.x + (i + 1) * gridDim.x, roff, ioff, E, p.n_tiles);
+                    it = get_item(i + 1);
                     my_cols(it.nt, c0, cn);
                     idesc = idesc_bf16_f32(128, cn ? cn : 16);
                 }
@@ -487,7 +508,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
         uint32_t issued = 0;
         bool ok = true;
         for (int i = 0; i < my_items && ok; ++i) {
-            const Item it = decode_item(blockIdx.x + i * gridDim.x, roff, ioff, E, p.n_tiles);
+            const Item it = get_item(i);
             const int y = it.e * p.N + it.n0;
             for (int kc = 0; kc < KT / 4; ++kc, r.next(CS), ++issued) {
                 if (!warp_wait_bounded(&code_empty[r.slot], r.phase ^ 1u, abort_flag, p.status,
@@ -536,7 +557,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
             uint32_t issued = 0;
             bool ok = true;
             for (int i = 0; i < my_items && ok; ++i) {
-                const Item it = decode_item(blockIdx.x + i * gridDim.x, roff, ioff, E, p.n_tiles);
+                const Item it = get_item(i);
                 for (int ks = 0; ks < KT; ++ks, r.next(kSlots), ++issued) {
                     if (!wait_bounded(&slot_empty[r.slot], r.phase ^ 1u, abort_flag, p.status, lim)) {
                         ok = false;
@@ -588,7 +609,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
         // 8m + 4h + 3 of the row.  A tile row beyond N reads row N - 1 (its codes
         // are zero-filled, so the value never matters).
         auto scale_base = [&](int j) -> const uint8_t * {
-            const Item it = decode_item(blockIdx.x + j * gridDim.x, roff, ioff, E, p.n_tiles);
+            const Item it = get_item(j);
             const int n = min(it.n0 + row, p.N - 1);
             return p.scales + (static_cast<size_t>(it.e) * p.N + n) * p.scale_row + 4 * half;
         };
@@ -608,7 +629,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
             if (!warp_wait_bounded(&acc_full[buf], (i >> 1) & 1, abort_flag, p.status, lim))
                 return false;
             tc_fence_after();
-            const Item it = decode_item(blockIdx.x + i * gridDim.x, roff, ioff, E, p.n_tiles);
+            const Item it = get_item(i);
             store_item(p, it, tmem_base + lane_off + buf * acc_cols, wg, row, split, part_cols);
             tc_fence_before();
             __syncwarp();
@@ -625,7 +646,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
         bool row_ok = false;
         const uint8_t *sb = nullptr;
         auto enter_item = [&](int it_idx) {
-            const Item it = decode_item(blockIdx.x + it_idx * gridDim.x, roff, ioff, E, p.n_tiles);
+            const Item it = get_item(it_idx);
             cur_nt = it.nt;
             // Scale bytes of a tile row beyond N (read with the tile) never count
             // as errors: those rows are not part of the output.
