@@ -304,6 +304,24 @@ def test_gemm_ignores_scales_of_rows_beyond_n(B, K):
     _tol_check(out.cpu().numpy(), ref, mag, what="rows beyond N")
 
 
+@pytest.mark.parametrize("offset", [1, 4], ids=["byte_aligned", "word_aligned"])
+@pytest.mark.parametrize("bands", [[5, 0, 9], [40, 3, 70]], ids=["split_mode", "single_mode"])
+def test_gemm_scales_at_unaligned_address(B, offset, bands):
+    # K = 512 would take the TMA scale path; a scale tensor that does not start
+    # on a 16-byte boundary must fall back to per-thread loads and still match.
+    act, codes, scales, gs = _explicit(bands, 512, 128)
+    backing = torch.zeros(scales.size + 64, dtype=torch.uint8, device=DEV)
+    d_scales = backing[offset:offset + scales.size].view(scales.shape)
+    d_scales.copy_(torch.from_numpy(scales).to(DEV))
+    assert d_scales.data_ptr() % 16 == offset
+    ws = B.make_workspace(0, 1, 1, DEV)
+    out = B.grouped_gemm(B.bf16_from_bits(act, DEV), B.to_device(codes, DEV), d_scales,
+                         B.to_device(gs, DEV), workspace=ws)
+    assert B.read_status(ws) == B.MOE_OK
+    ref, mag = oracle.grouped_gemm(act, codes, scales, gs)
+    _tol_check(out.cpu().numpy(), ref, mag, what=f"scales at +{offset}")
+
+
 def _sample_pairs(gs, N, n=3000, seed=0):
     """(row, col) samples: random ones plus the first and last row of every band
     and the first and last column."""
