@@ -309,12 +309,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
     const uint32_t CS = min(static_cast<uint32_t>(kCodeStagesMax),
                             (kRingBytes - (split ? 0u : kSlots * act_stage_bytes)) / ring_stage_bytes);
     const uint32_t act_off = CS * ring_stage_bytes;     // single mode: activation slots
-    // TMEM columns: two accumulator buffers, then the A slots.  With every band
-    // <= 16 rows the K-partials need 16 columns each, which leaves room for
-    // three A slots per warpgroup (more decode ahead of the MMAs); otherwise two.
+    // TMEM columns: two accumulator buffers, then the eight A slots (two sets of
+    // four, one set per code-stage parity).  With every band <= 16 rows the
+    // K-partials need only 16 columns each.
     const bool narrow = split && nt_max <= 16;
     const uint32_t per_wg = 2u;                            // A-slot sets in flight
-    const uint32_t nslots = narrow ? kSlotsMax : kSlots;
     const uint32_t part_cols = narrow ? kPartCols / 2 : kPartCols;
     const uint32_t acc_cols = split ? kIssuerWarps * part_cols : kAccCols;
     const uint32_t acol0 = 2 * acc_cols;
