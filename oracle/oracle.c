@@ -327,3 +327,59 @@ void oracle_combine(const double *y, long N, const int32_t *slot_to_row, const f
             if (abs_out) abs_out[t * N + n] = mag;
         }
 }
+
+/* ------------------------------------------------- MXFP4 -> NVFP4 weight cast */
+
+/* E4M3 (sign bit, 4 exponent bits with bias 7, 3 mantissa bits; no infinities,
+ * exponent 15 with mantissa 7 is NaN) value of a byte, from the format's
+ * definition. */
+double oracle_e4m3_value(int byte) {
+    const int s = (byte >> 7) & 1, e = (byte >> 3) & 15, m = byte & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m, -9);              /* subnormal: m/8 * 2^-6 */
+    else v = ldexp(1.0 + m / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+/* E4M3 byte of 2^p if it is exactly representable (p in -9..8), else -1. */
+static int e4m3_of_power_of_two(int p) {
+    if (p > 8 || p < -9) return -1;
+    if (p >= -6) return (p + 7) << 3;                   /* normal, mantissa 0 */
+    return 1 << (p + 9);                                /* subnormal: 2^p = m * 2^-9 */
+}
+
+/* The lossless cast of [NVFP4] "The lossless weight cast": for each expert e
+ * (its whole [N, K/32] scale tensor, so the fused w1/w3 rows share it),
+ * k_max = max over blocks of (scale byte - 127); the per-tensor scale is
+ * 2^(k_max - 8) and block j's per-16 scale (written for both halves of the
+ * 32-element block) is 2^(k_j - k_max + 8), so that per-16 scale times the
+ * per-tensor scale is the block's own 2^(k_j).  The 4-bit codes are unchanged.
+ * A block whose per-16 scale falls below E4M3's smallest power of two (2^-9)
+ * cannot be cast exactly: it is counted in out_of_range[e] and written as 0.
+ * Scale byte 255 (E8M0 NaN) is rejected (returns 1). */
+int oracle_mxfp4_to_nvfp4(const uint8_t *scales, long E, long N, long K, uint8_t *e4m3,
+                          double *weight_scale_2, int64_t *out_of_range) {
+    const long nb = K / 32;
+    for (long e = 0; e < E; ++e) {
+        const uint8_t *s = scales + e * N * nb;
+        int kmax = -1000;
+        for (long i = 0; i < N * nb; ++i) {
+            if (s[i] == 255) return 1;
+            if ((int)s[i] - 127 > kmax) kmax = (int)s[i] - 127;
+        }
+        weight_scale_2[e] = ldexp(1.0, kmax - 8);
+        int64_t bad = 0;
+        for (long i = 0; i < N * nb; ++i) {
+            int b = e4m3_of_power_of_two((int)s[i] - 127 - kmax + 8);
+            if (b < 0) {
+                ++bad;
+                b = 0;
+            }
+            e4m3[(e * N * nb + i) * 2] = (uint8_t)b;
+            e4m3[(e * N * nb + i) * 2 + 1] = (uint8_t)b;
+        }
+        out_of_range[e] = bad;
+    }
+    return 0;
+}

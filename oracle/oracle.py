@@ -59,6 +59,10 @@ def _load():
             lib.oracle_swiglu.restype = None
             lib.oracle_combine.argtypes = [P, L, P, P, L, L, P, P]
             lib.oracle_combine.restype = None
+            lib.oracle_e4m3_value.argtypes = [I]
+            lib.oracle_e4m3_value.restype = C.c_double
+            lib.oracle_mxfp4_to_nvfp4.argtypes = [P, L, L, L, P, P, P]
+            lib.oracle_mxfp4_to_nvfp4.restype = I
             lib.oracle_threads_used.argtypes = []
             lib.oracle_threads_used.restype = I
             _lib = lib
@@ -173,3 +177,20 @@ def combine(y, slot_to_row, topk_w):
     mag = np.empty((T, N), np.float64)
     _load().oracle_combine(_p(y), N, _p(s2r), _p(w), T, k, _p(out), _p(mag))
     return out, mag
+
+
+def e4m3_value(byte: int) -> float:
+    return _load().oracle_e4m3_value(int(byte))
+
+
+def mxfp4_to_nvfp4(scales: np.ndarray):
+    """scales uint8 [E, N, K/32] (E8M0) -> (e4m3 uint8 [E, N, K/16],
+    weight_scale_2 float64 [E], out_of_range int64 [E])."""
+    scales = _c(scales, np.uint8)
+    E, N, nb = scales.shape
+    e4m3 = np.empty((E, N, 2 * nb), np.uint8)
+    ws2 = np.empty(E, np.float64)
+    oob = np.empty(E, np.int64)
+    if _load().oracle_mxfp4_to_nvfp4(_p(scales), E, N, 32 * nb, _p(e4m3), _p(ws2), _p(oob)):
+        raise ValueError("scale byte 255 (E8M0 NaN)")
+    return e4m3, ws2, oob

@@ -365,3 +365,90 @@ def test_single_expert_layer_is_dense_swiglu_mlp():
     hd = inputs.bf16_bits_to_f32(h).astype(np.float64)
     ref = (hd @ W2.T) * c["topk_w"].astype(np.float64)
     np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-300)
+
+
+# ------------------------------------------- MXFP4 -> NVFP4 lossless weight cast
+# "DeepSeek-V4-Flash-0731-NVFP4", "The lossless weight cast": the per-tensor
+# scale is 2^(k_max - 8) and every per-16 E4M3 scale 2^(k_j - k_max + 8), with
+# the 4-bit codes unchanged, so the dequantized weights are identical.
+
+def test_e4m3_value_matches_torch_float8_for_every_byte():
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("torch without float8_e4m3fn")
+    ref = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    got = np.array([oracle.e4m3_value(b) for b in range(256)])
+    both_nan = np.isnan(ref) & np.isnan(got)
+    assert np.array_equal(got[~both_nan], ref[~both_nan])
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+
+
+def test_e4m3_anchor_values():
+    # the format's definition: 0x38 = 1, 0x78 = 2^8, 0x7E = 448 (largest),
+    # 0x08 = 2^-6 (smallest normal), 0x01 = 2^-9 (smallest subnormal), 0xB8 = -1
+    assert oracle.e4m3_value(0x38) == 1.0
+    assert oracle.e4m3_value(0x78) == 256.0
+    assert oracle.e4m3_value(0x7E) == 448.0
+    assert oracle.e4m3_value(0x08) == 2.0 ** -6
+    assert oracle.e4m3_value(0x01) == 2.0 ** -9
+    assert oracle.e4m3_value(0xB8) == -1.0
+    assert math.isnan(oracle.e4m3_value(0x7F))
+
+
+def _dequant_mxfp4(codes, scales):
+    E, N, Kh = codes.shape
+    lo, hi = codes & 15, codes >> 4
+    q = np.empty((E, N, 2 * Kh), np.int64)
+    q[..., 0::2], q[..., 1::2] = lo, hi
+    vals = np.array([oracle.e2m1_value(c) for c in range(16)])[q]
+    return vals * np.repeat(np.ldexp(1.0, scales.astype(np.int64) - 127), 32, axis=2)
+
+
+def _dequant_nvfp4(codes, e4m3, ws2):
+    E, N, Kh = codes.shape
+    lo, hi = codes & 15, codes >> 4
+    q = np.empty((E, N, 2 * Kh), np.int64)
+    q[..., 0::2], q[..., 1::2] = lo, hi
+    vals = np.array([oracle.e2m1_value(c) for c in range(16)])[q]
+    s16 = np.array([oracle.e4m3_value(b) for b in range(256)])[e4m3]
+    return vals * np.repeat(s16, 16, axis=2) * ws2[:, None, None]
+
+
+def test_cast_dequantizes_to_identical_values_when_in_range():
+    rng = np.random.default_rng(21)
+    E, N, K = 3, 8, 256
+    codes = rng.integers(0, 256, (E, N, K // 2), dtype=np.uint8)
+    top = np.array([127 + 40, 127 - 60, 200])[:, None, None]
+    scales = (top - rng.integers(0, 18, (E, N, K // 32))).astype(np.uint8)   # spread <= 17
+    e4m3, ws2, oob = oracle.mxfp4_to_nvfp4(scales)
+    assert (oob == 0).all()
+    assert np.array_equal(_dequant_nvfp4(codes, e4m3, ws2), _dequant_mxfp4(codes, scales))
+
+
+def test_cast_closed_forms_at_the_edges_of_the_range():
+    s = np.array([[[130, 130 - 17, 130 - 18, 130 - 5]]], np.uint8)   # k_max = 3
+    e4m3, ws2, oob = oracle.mxfp4_to_nvfp4(s)
+    assert ws2[0] == 2.0 ** (3 - 8)
+    assert list(e4m3[0, 0]) == [0x78, 0x78, 0x01, 0x01, 0, 0, 0x50, 0x50]   # 2^8, 2^-9, -, 2^3
+    assert oob[0] == 1
+
+
+def test_cast_out_of_range_count_is_brute_force():
+    rng = np.random.default_rng(22)
+    s = rng.integers(0, 255, (4, 16, 8), dtype=np.uint8)
+    _, ws2, oob = oracle.mxfp4_to_nvfp4(s)
+    for e in range(4):
+        k = s[e].astype(np.int64) - 127
+        assert oob[e] == int((k < k.max() - 17).sum())
+        assert ws2[e] == 2.0 ** (k.max() - 8)
+
+
+def test_cast_shares_k_max_across_the_fused_rows_and_rejects_nan_scale():
+    # rows [0, I) (w1) small, rows [I, 2I) (w3) large: one k_max for the tensor
+    s = np.full((1, 4, 2), 120, np.uint8)
+    s[0, 2:] = 125
+    _, ws2, _ = oracle.mxfp4_to_nvfp4(s)
+    assert ws2[0] == 2.0 ** (125 - 127 - 8)
+    s[0, 0, 0] = 255
+    with pytest.raises(ValueError):
+        oracle.mxfp4_to_nvfp4(s)
