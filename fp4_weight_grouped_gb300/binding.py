@@ -23,7 +23,7 @@ SYMBOLS = (
     "moe_status_string", "moe_workspace_bytes", "moe_clear_status", "moe_read_status",
     "moe_route_sort", "moe_mxfp4_grouped_gemm", "moe_swiglu", "moe_combine", "moe_layer_forward",
     "moe_mxfp4_decode_expert", "moe_debug_bounded_wait", "moe_last_launch_count",
-    "moe_route_sort_noalloc",
+    "moe_route_sort_noalloc", "moe_nvfp4_cast_workspace_bytes", "moe_mxfp4_to_nvfp4",
 )
 
 _lock = threading.Lock()
@@ -67,6 +67,8 @@ def load(path: str | None = None):
                 "moe_mxfp4_decode_expert": ([P, P, I32, I32, I32, I32, P, P, SZ, P], C.c_int),
                 "moe_debug_bounded_wait": ([U64, P, SZ, P], C.c_int),
                 "moe_last_launch_count": ([], I32),
+                "moe_nvfp4_cast_workspace_bytes": ([I32], SZ),
+                "moe_mxfp4_to_nvfp4": ([P, I32, I32, I32, P, P, P, P, SZ, P], C.c_int),
             }
             for name, (args, res) in sig.items():
                 f = getattr(lib, name)
@@ -262,6 +264,29 @@ def decode_expert(codes: torch.Tensor, scales: torch.Tensor, e: int,
     rc = load().moe_mxfp4_decode_expert(_ptr(codes), _ptr(scales), E, N, K, e, _ptr(out),
                                         _ptr(workspace), workspace.numel(), _stream(stream))
     _check(rc, "moe_mxfp4_decode_expert")
+    return out
+
+
+def mxfp4_to_nvfp4(scales: torch.Tensor, out=None, workspace: torch.Tensor | None = None,
+                   stream=None):
+    """Lossless MXFP4 -> NVFP4 scale cast.  scales uint8 [E, N, K/32] ->
+    (e4m3 uint8 [E, N, K/16], weight_scale_2 f32 [E], out_of_range int64 [E]);
+    `out` may hold those three tensors already (out_of_range holds the uint64
+    counts of the C call, which never exceed 2^63)."""
+    E, N, Kb = scales.shape
+    dev = scales.device
+    if out is None:
+        out = (torch.empty((E, N, 2 * Kb), dtype=torch.uint8, device=dev),
+               torch.empty(E, dtype=torch.float32, device=dev),
+               torch.empty(E, dtype=torch.int64, device=dev))
+    e4m3, ws2, oob = out
+    if workspace is None:
+        workspace = torch.empty(int(load().moe_nvfp4_cast_workspace_bytes(E)), dtype=torch.uint8,
+                                device=dev)
+        clear_status(workspace, stream)
+    rc = load().moe_mxfp4_to_nvfp4(_ptr(scales), E, N, 32 * Kb, _ptr(e4m3), _ptr(ws2), _ptr(oob),
+                                   _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "moe_mxfp4_to_nvfp4")
     return out
 
 

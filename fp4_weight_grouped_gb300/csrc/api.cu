@@ -296,6 +296,31 @@ moe_status moe_mxfp4_decode_expert(const uint8_t *codes, const uint8_t *scales, 
     return st;
 }
 
+size_t moe_nvfp4_cast_workspace_bytes(int32_t E) {
+    return E <= 0 ? kStatusBytes : kStatusBytes + ((static_cast<size_t>(E) * sizeof(int) + 255) & ~size_t(255));
+}
+
+moe_status moe_mxfp4_to_nvfp4(const uint8_t *scales, int32_t E, int32_t N, int32_t K,
+                              uint8_t *e4m3_scales, float *weight_scale_2, uint64_t *out_of_range,
+                              void *workspace, size_t workspace_bytes, void *stream) {
+    if (!scales || !e4m3_scales || !weight_scale_2 || !out_of_range || !workspace || E <= 0 ||
+        E > 65535 || N <= 0 || K <= 0 || K % 32 || !aligned(workspace, 16) ||
+        !aligned(weight_scale_2, 4) || !aligned(out_of_range, 8) ||
+        workspace_bytes < moe_nvfp4_cast_workspace_bytes(E))
+        return MOE_ERR_INVALID_ARG;
+    int sms = 0;
+    moe_status st = current_device(&sms);
+    if (st != MOE_OK) return st;
+    int launches = 0;
+    st = moe::launch_mxfp4_to_nvfp4(
+        scales, E, N, K, e4m3_scales, weight_scale_2,
+        reinterpret_cast<unsigned long long *>(out_of_range),
+        reinterpret_cast<int *>(static_cast<uint8_t *>(workspace) + kStatusBytes),
+        status_word(workspace), static_cast<cudaStream_t>(stream), sms, &launches);
+    g_last_launches = launches;
+    return st;
+}
+
 moe_status moe_debug_bounded_wait(uint64_t limit_ns, void *workspace, size_t workspace_bytes,
                                   void *stream) {
     if (!workspace || workspace_bytes < kStatusBytes || limit_ns < 1000 ||

@@ -20,7 +20,7 @@ import numpy as np
 
 # Stream tags keep each tensor's random stream independent of the others, so a
 # caller can regenerate one tensor without drawing the rest.
-_TAG_ROUTE, _TAG_ACT, _TAG_W13, _TAG_W2, _TAG_X, _TAG_GATE = 1, 2, 3, 4, 5, 6
+_TAG_ROUTE, _TAG_ACT, _TAG_W13, _TAG_W2, _TAG_X, _TAG_GATE, _TAG_SCALES = 1, 2, 3, 4, 5, 6, 7
 
 CONFIGS = {
     # Tiny MXFP4 grouped GEMM: E=8, top-2, T=16 (32 rows), K=256, N=512,
@@ -107,6 +107,12 @@ def mxfp4_weights(seed: int, tag: int, E: int, N: int, K: int, exp=(-10, -2)):
     codes = np.frombuffer(rng.bytes(E * N * (K // 2)), dtype=np.uint8).reshape(E, N, K // 2).copy()
     scales = (127 + rng.integers(exp[0], exp[1] + 1, size=(E, N, K // 32))).astype(np.uint8)
     return codes, scales
+
+
+def e8m0_scales(seed: int, shape, lo: int, hi: int, tag: int = _TAG_SCALES) -> np.ndarray:
+    """E8M0 scale bytes drawn uniformly from lo..hi (inclusive), uint8 of `shape`."""
+    assert 0 <= lo <= hi <= 255
+    return _rng(seed, tag, lo, hi).integers(lo, hi + 1, size=shape, dtype=np.int64).astype(np.uint8)
 
 
 def normal_bf16(seed: int, tag: int, shape) -> np.ndarray:

@@ -273,6 +273,49 @@ MOE_API moe_status moe_mxfp4_decode_expert(const uint8_t *codes, const uint8_t *
                                    int32_t N, int32_t K, int32_t e, uint16_t *out,
                                    void *workspace, size_t workspace_bytes, void *stream);
 
+/* Bytes of device workspace needed by moe_mxfp4_to_nvfp4 for E experts: the
+ * status word plus one 32-bit scratch word per expert. */
+MOE_API size_t moe_nvfp4_cast_workspace_bytes(int32_t E);
+
+/*
+ * moe_mxfp4_to_nvfp4 — lossless cast of MXFP4 weight scales to NVFP4's two
+ * scale levels ([NVFP4] "The lossless weight cast").  The e2m1 codes are
+ * shared by both formats and are not touched; only the scales change.
+ *
+ * For each expert e, over its whole scale tensor (so the w1 and w3 rows of a
+ * fused w13 tensor share one per-tensor scale), with k_max = max(s) - 127:
+ *   weight_scale_2[e]          = 2^(k_max - 8)                 (f32, exact)
+ *   e4m3_scales[e, n, 2b], [2b+1] = 2^(s[e, n, b] - 127 - k_max + 8) (E4M3)
+ * so that E4M3 scale x weight_scale_2 = 2^(s - 127) for every 16-element half
+ * of every 32-block: each weight dequantizes to exactly its MXFP4 value.  E4M3
+ * holds the powers of two 2^-9..2^8, so a block whose scale lies more than 17
+ * binades below the expert's largest has no exact E4M3 scale: its two bytes
+ * are written as 0 and it is counted in out_of_range[e] (the exactness audit;
+ * 0 means the cast is lossless for that expert).
+ *
+ *  scales          device uint8 [E, N, K/32]: E8M0 bytes (127 = 1.0).  Byte
+ *                  255 (NaN) sets MOE_ERR_DATA; the outputs are then
+ *                  unspecified.
+ *  E, N, K         experts (1..65535), rows per expert (>= 1), reduction
+ *                  length (multiple of 32).
+ *  e4m3_scales     device uint8 [E, N, K/16] out: E4M3 bytes (sign 0, 4
+ *                  exponent bits with bias 7, 3 mantissa bits).
+ *  weight_scale_2  device f32 [E] out.
+ *  out_of_range    device uint64 [E] out: blocks written as 0 (cleared by the
+ *                  call before counting).
+ *  workspace       device, >= moe_nvfp4_cast_workspace_bytes(E) bytes,
+ *                  16-byte aligned; its status word as for every call.
+ * Launches one kernel when each expert's scale tensor (N * K/32 bytes) is a
+ * multiple of 16 bytes and at most 512 KiB and both byte buffers are 16-byte
+ * aligned: a cluster of up to 8 CTAs per expert reads the scales once.
+ * Otherwise two kernels (per-expert maximum into the workspace, then the
+ * conversion).  Results are exact integers, identical from run to run.
+ */
+MOE_API moe_status moe_mxfp4_to_nvfp4(const uint8_t *scales, int32_t E, int32_t N, int32_t K,
+                                      uint8_t *e4m3_scales, float *weight_scale_2,
+                                      uint64_t *out_of_range, void *workspace,
+                                      size_t workspace_bytes, void *stream);
+
 /*
  * moe_debug_bounded_wait — failure-detection self-test.  Launches one block
  * that waits on a shared-memory barrier nothing will ever complete, using the

@@ -53,6 +53,35 @@ def test_workspace_bytes(lib):
     assert lib.moe_workspace_bytes(8192, 6, 256) == 256 + 48 * 256 * 4 + 49152 * 4
 
 
+def test_nvfp4_cast_workspace_and_host_checks(lib):
+    lib.moe_nvfp4_cast_workspace_bytes.restype = C.c_size_t
+    lib.moe_nvfp4_cast_workspace_bytes.argtypes = [C.c_int32]
+    assert lib.moe_nvfp4_cast_workspace_bytes(1) == 512
+    assert lib.moe_nvfp4_cast_workspace_bytes(256) == 256 + 1024
+    f = lib.moe_mxfp4_to_nvfp4
+    P = C.c_void_p
+    f.argtypes = [P, C.c_int32, C.c_int32, C.c_int32, P, P, P, P, C.c_size_t, P]
+    f.restype = C.c_int
+    fake = P(4096)
+
+    def call(s=fake, E=4, N=8, K=64, o=fake, w2=fake, oob=fake, ws=fake, wsb=1 << 12):
+        return f(s, E, N, K, o, w2, oob, ws, wsb, None)
+
+    INVALID = 1
+    assert call(K=48) == INVALID            # K % 32
+    assert call(K=0) == INVALID
+    assert call(E=0) == INVALID
+    assert call(E=65536) == INVALID         # one grid row per expert
+    assert call(N=0) == INVALID
+    assert call(s=None) == INVALID
+    assert call(o=None) == INVALID
+    assert call(w2=None) == INVALID
+    assert call(oob=None) == INVALID
+    assert call(oob=P(4100)) == INVALID     # uint64 counts need 8-byte alignment
+    assert call(ws=P(4104)) == INVALID
+    assert call(wsb=256 + 15) == INVALID    # E = 4 needs 256 + 256 bytes
+
+
 def test_gemm_rejects_bad_arguments_on_host(lib):
     f = lib.moe_mxfp4_grouped_gemm
     P = C.c_void_p
