@@ -43,8 +43,13 @@ WORKLOADS = {
                      "experts unused; full path",
     "layer_T8192": "Full MoE layer: T=8192 tokens (49152 rows), top-6 of N(0,1) logits, softmax "
                    "router weights; full path",
+    "cast_w13": "Lossless MXFP4 -> NVFP4 scale cast of the w13 scales: E8M0 [256, 4096, 128] "
+                "(128 MiB) -> E4M3 [256, 4096, 256] + per-expert f32 scale + out-of-range count",
 }
-DEFAULT_STEPS = {"decode_T64": 2000, "decode_T256": 1000, "prefill_T4096": 60, "layer_T8192": 30}
+DEFAULT_STEPS = {"decode_T64": 2000, "decode_T256": 1000, "prefill_T4096": 60, "layer_T8192": 30,
+                 "cast_w13": 200}
+CAST_METRIC = "lossless MXFP4 -> NVFP4 scale cast GB/s (algorithmic bytes), % of measured HBM, 1 GPU"
+CAST_SHAPE, CAST_BYTES = (256, 4096, 128), (117, 125)   # w13 scale tensor, exponents [-10, -2]
 
 # Fallback peaks (only if the measured-peaks file is absent).
 FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
@@ -338,6 +343,143 @@ def run_ours(args, rank, world, local):
     return result, dict(workload=args.workload, rank=rank)
 
 
+# ------------------------------------------------------------ scale cast workload
+
+def cast_alg_bytes(shape) -> int:
+    """Algorithmic bytes of one cast: read every scale byte once, write two E4M3
+    bytes per scale byte, a 4-byte scale and an 8-byte count per expert."""
+    E, N, nb = shape
+    return 3 * E * N * nb + 12 * E
+
+
+def run_cast(args, rank, world, local):
+    import torch
+
+    import __graft_entry__ as ge
+    ge.build()
+    from fp4_weight_grouped_gb300 import binding as B
+    from fp4_weight_grouped_gb300 import inputs
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    scales_np = inputs.e8m0_scales(args.seed + rank, CAST_SHAPE, *CAST_BYTES)
+    E, N, nb = CAST_SHAPE
+    scales = torch.from_numpy(scales_np).to(dev)
+    out = (torch.empty((E, N, 2 * nb), dtype=torch.uint8, device=dev),
+           torch.empty(E, dtype=torch.float32, device=dev),
+           torch.empty(E, dtype=torch.int64, device=dev))
+    ws = torch.empty(int(B.load().moe_nvfp4_cast_workspace_bytes(E)), dtype=torch.uint8, device=dev)
+    B.clear_status(ws)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)     # > 129 MB L2
+
+    for i in range(args.warmup):
+        flush.fill_(i & 0xFF)
+        B.mxfp4_to_nvfp4(scales, out=out, workspace=ws)
+    launches_per_cast = B.last_launch_count()
+    torch.cuda.synchronize(dev)
+    if B.read_status(ws) != B.MOE_OK or int(out[2].sum()) != 0:
+        raise RuntimeError("scale cast reported an error or an inexact block")
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        wall0 = time.time()
+        for i in range(K):
+            flush.fill_(i & 0xFF)                # L2 flush between timed casts, outside the events
+            ev[i][0].record(stream)
+            B.mxfp4_to_nvfp4(scales, out=out, workspace=ws)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        wall1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = clk.summary(wall0, wall1)
+    launch_ms = statistics.fmean(a.elapsed_time(b) for a, b in ev)
+
+    # ---- end to end: pinned host scales in, E4M3 bytes + scales + counts out
+    hs = torch.from_numpy(scales_np).pin_memory()
+    hout = (torch.empty(out[0].shape, dtype=torch.uint8).pin_memory(),
+            torch.empty(E, dtype=torch.float32).pin_memory(),
+            torch.empty(E, dtype=torch.int64).pin_memory())
+    ds = torch.empty_like(scales)
+
+    def e2e_step():
+        ds.copy_(hs, non_blocking=True)
+        B.mxfp4_to_nvfp4(ds, out=out, workspace=ws)
+        for h, d in zip(hout, out):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e2e_steps = max(3, min(K, 50))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if B.read_status(ws) != B.MOE_OK:
+        raise RuntimeError("scale cast reported an error")
+
+    launch_ms, e2e_ms = reduce_max_over_ranks([launch_ms, e2e_ms], device=dev)
+    alg = cast_alg_bytes(CAST_SHAPE)
+    hbm, _, _, peak_src = load_peaks()
+    achieved = alg / (launch_ms * 1e-3) / 1e9
+    h2d = scales.numel()
+    d2h = sum(t.numel() * t.element_size() for t in hout)
+    return {
+        "metric": CAST_METRIC,
+        "value": round(whole_job_rate(alg, launch_ms, world) / 1e9, 1),
+        "unit": "GB/s",
+        "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": round(launch_ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+        "data": "synthetic: seeded numpy PCG64 E8M0 bytes 127 + U{-10..-2}",
+        "config": {"workload": "cast_w13", "description": WORKLOADS["cast_w13"],
+                   "shape": list(CAST_SHAPE),
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "256 MiB L2 flush before every timed cast, outside its events"},
+        "roofline": {"kernel": "stream_kernel (one cast call)" if launches_per_cast == 1
+                     else "kmax_kernel + convert_kernel (one cast call, timed together)",
+                     "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "traffic": None, "peak_source": peak_src,
+                     "algorithmic_bytes_per_launch": alg, "avg_launch_ms": round(launch_ms, 5)},
+        "e2e": {"value": round(whole_job_rate(alg, e2e_ms, world) / 1e9, 1), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "api": "moe_mxfp4_to_nvfp4 with pinned host copies"},
+        "gpu_launches": launches_per_cast * K,
+        "clocks": clocks,
+    }
+
+
+def run_cast_oracle(steps: int, budget_s: float, seed: int):
+    """Times the oracle's cast on the first n experts of the w13 scales, n chosen
+    from a one-expert calibration so that `steps` passes take about budget_s."""
+    import numpy as np
+
+    import oracle
+    from fp4_weight_grouped_gb300 import inputs
+    scales = inputs.e8m0_scales(seed, CAST_SHAPE, *CAST_BYTES)
+    t = time.perf_counter()
+    oracle.mxfp4_to_nvfp4(scales[:1])
+    t1 = max(time.perf_counter() - t, 1e-6)
+    n = int(max(1, min(CAST_SHAPE[0], budget_s / steps // t1)))
+    sample = np.ascontiguousarray(scales[:n])
+    times = []
+    for _ in range(steps):
+        t = time.perf_counter()
+        oracle.mxfp4_to_nvfp4(sample)
+        times.append(time.perf_counter() - t)
+    alg = cast_alg_bytes(sample.shape)
+    ms = 1e3 * statistics.fmean(times)
+    return alg / (ms * 1e-3) / 1e9, ms, f"oracle cast of the first {n} of {CAST_SHAPE[0]} experts' w13 scales"
+
+
 # --------------------------------------------------------------- CPU oracle arm
 
 def oracle_sample(c, max_experts: int):
@@ -397,6 +539,25 @@ def run_reference(args, rank, world):
     a one-band calibration so the run fits REFERENCE_BUDGET_S.  Rank 0 only."""
     if rank != 0:
         return None
+    if args.workload == "cast_w13":
+        run_cast_oracle(args.warmup, REFERENCE_BUDGET_S * args.warmup / (args.steps + args.warmup),
+                        args.seed)
+        val, ms, sample = run_cast_oracle(args.steps,
+                                          REFERENCE_BUDGET_S * args.steps / (args.steps + args.warmup),
+                                          args.seed)
+        val = round(val, 3)
+        return {
+            "impl": "reference", "metric": CAST_METRIC, "value": val, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+            "data": "synthetic (same generator and seed as the GPU arm)",
+            "config": {"workload": args.workload, "description": WORKLOADS[args.workload],
+                       "sample": sample},
+            "cpu_baseline": {"value": val, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0,
+        }
     from fp4_weight_grouped_gb300 import inputs
     c = inputs.layer_workload(args.workload, args.seed)
     gs1, xs1 = oracle_sample(c, 1)
@@ -450,9 +611,17 @@ def main():
         import torch
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    res, _ = run_ours(args, rank, world, local)
+    if args.workload == "cast_w13":
+        res = run_cast(args, rank, world, local)
+    else:
+        res, _ = run_ours(args, rank, world, local)
     if rank == 0:
-        if world == 1 and not args.no_cpu_baseline:
+        if world == 1 and not args.no_cpu_baseline and args.workload == "cast_w13":
+            val, ms, sample = run_cast_oracle(3, 20.0, args.seed)
+            res["cpu_baseline"] = {"value": round(val, 3), "unit": "GB/s", "cores": 1,
+                                   "kind": "oracle", "sample": f"{sample}, mean of 3 passes "
+                                                               f"({ms:.0f} ms each)"}
+        elif world == 1 and not args.no_cpu_baseline:
             res["cpu_baseline"] = cpu_baseline(args.workload, args.seed)
         print(json.dumps(res), flush=True)
     if world > 1:
