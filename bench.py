@@ -444,7 +444,7 @@ def run_cast(args, rank, world, local):
                    "shape": list(CAST_SHAPE),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "256 MiB L2 flush before every timed cast, outside its events"},
-        "roofline": {"kernel": "stream_kernel (one cast call)" if launches_per_cast == 1
+        "roofline": {"kernel": "onepass_kernel (one cast call)" if launches_per_cast == 1
                      else "kmax_kernel + convert_kernel (one cast call, timed together)",
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 4), "traffic": None, "peak_source": peak_src,
