@@ -15,7 +15,8 @@
  *        ragged groups including empty ones.
  *  [NVFP4] "DeepSeek-V4-Flash-0731-NVFP4", "The lossless weight cast": E8M0
  *        power-of-two scales per 32 elements; w1/w3 fused into one GEMM; E2M1 -0
- *        is canonicalised to +0.
+ *        is canonicalised to +0; NVFP4's two scale levels (per-16 E4M3 block
+ *        scales under a per-tensor weight_scale_2) and the cast into them.
  *  [Pocket] "DeepSeek-V4-Flash" (PocketLLM), "Correctness and precision":
  *        deterministic expert reduction without atomics.
  *
@@ -382,4 +383,84 @@ int oracle_mxfp4_to_nvfp4(const uint8_t *scales, long E, long N, long K, uint8_t
         out_of_range[e] = bad;
     }
     return 0;
+}
+
+/* ------------------------------------------------------ NVFP4 grouped GEMM */
+
+/* Exact value of NVFP4 weight (e, n, k): e2m1(code) * e4m3(s16[e, n, k/16]) *
+ * weight_scale_2[e].  [TPU] section 1 describes an NVFP4 kernel that decodes
+ * the e2m1 weights and their per-16 E4M3 scales; [NVFP4] "The lossless weight
+ * cast" gives the two scale levels (per-16 E4M3 under a per-tensor f32
+ * weight_scale_2) whose product reconstructs each weight.  Every factor is
+ * exact in double and so is their product (at most 2 + 4 + 24 significant
+ * bits).  Returns -1 for a NaN scale byte (0x7F or 0xFF). */
+static int nvfp4_weight_value(const uint8_t *codes, const uint8_t *s16, const float *ws2, long N,
+                              long K, long e, long n, long k, double *w) {
+    uint8_t byte = codes[(e * N + n) * (K / 2) + k / 2];
+    int code = (k & 1) ? (byte >> 4) : (byte & 15);
+    double s = oracle_e4m3_value(s16[(e * N + n) * (K / 16) + k / 16]);
+    if (isnan(s)) return -1;
+    *w = E2M1_VALUE[code] * s * (double)ws2[e];
+    return 0;
+}
+
+typedef struct {
+    const uint16_t *act;
+    const uint8_t *codes, *s16;
+    const float *ws2;
+    const int32_t *offsets;
+    long K, N, n_blocks_per_e;
+    double *out, *abs_out;
+    int bad_scale;
+} nvfp4_ctx;
+
+static void nvfp4_gemm_item(void *vctx, long item) {
+    nvfp4_ctx *c = (nvfp4_ctx *)vctx;
+    long e = item / c->n_blocks_per_e;
+    long n0 = (item % c->n_blocks_per_e) * N_BLOCK;
+    long r0 = c->offsets[e], r1 = c->offsets[e + 1];
+    if (r1 <= r0) return;                       /* empty group: no rows, no work */
+    long K = c->K, N = c->N;
+    double *w = (double *)malloc(sizeof(double) * (size_t)K);
+    for (long n = n0; n < n0 + N_BLOCK && n < N; ++n) {
+        for (long k = 0; k < K; ++k)
+            if (nvfp4_weight_value(c->codes, c->s16, c->ws2, N, K, e, n, k, &w[k])) c->bad_scale = 1;
+        for (long r = r0; r < r1; ++r) {
+            const uint16_t *a = c->act + r * K;
+            double acc = 0.0, mag = 0.0;
+            for (long k = 0; k < K; ++k) {      /* ascending k */
+                double p = bf16_bits_to_double(a[k]) * w[k];
+                acc += p;
+                mag += fabs(p);
+            }
+            c->out[r * N + n] = acc;
+            if (c->abs_out) c->abs_out[r * N + n] = mag;
+        }
+    }
+    free(w);
+}
+
+/* out[r, n] = sum_k act[r, k] * w_e[n, k] with the NVFP4 weights above, for
+ * every row r of band e (bands = group_sizes in expert order), summed in
+ * ascending k.  codes [E, N, K/2] as for MXFP4; scales16 [E, N, K/16] E4M3
+ * bytes; weight_scale_2 [E] f32.  abs_out (optional) receives sum_k |a * w|.
+ * Returns -1 if K % 16 != 0, a group size is negative, sum(group_sizes) !=
+ * rows, or a scale byte read is NaN. */
+int oracle_nvfp4_grouped_gemm(const uint16_t *act, long rows, long K, const uint8_t *codes,
+                              const uint8_t *scales16, const float *weight_scale_2,
+                              const int32_t *group_sizes, long E, long N, double *out,
+                              double *abs_out, int n_threads) {
+    if (K % 16 || K <= 0) return -1;
+    int32_t *off = (int32_t *)malloc(sizeof(int32_t) * (size_t)(E + 1));
+    off[0] = 0;
+    for (long e = 0; e < E; ++e) {
+        if (group_sizes[e] < 0) { free(off); return -1; }
+        off[e + 1] = off[e] + group_sizes[e];
+    }
+    if (off[E] != rows) { free(off); return -1; }
+    nvfp4_ctx c = {act, codes, scales16, weight_scale_2, off, K, N, (N + N_BLOCK - 1) / N_BLOCK,
+                   out, abs_out, 0};
+    run_parallel(nvfp4_gemm_item, &c, E * c.n_blocks_per_e, n_threads);
+    free(off);
+    return c.bad_scale ? -1 : 0;
 }

@@ -63,6 +63,8 @@ def _load():
             lib.oracle_e4m3_value.restype = C.c_double
             lib.oracle_mxfp4_to_nvfp4.argtypes = [P, L, L, L, P, P, P]
             lib.oracle_mxfp4_to_nvfp4.restype = I
+            lib.oracle_nvfp4_grouped_gemm.argtypes = [P, L, L, P, P, P, P, L, L, P, P, I]
+            lib.oracle_nvfp4_grouped_gemm.restype = I
             lib.oracle_threads_used.argtypes = []
             lib.oracle_threads_used.restype = I
             _lib = lib
@@ -194,3 +196,22 @@ def mxfp4_to_nvfp4(scales: np.ndarray):
     if _load().oracle_mxfp4_to_nvfp4(_p(scales), E, N, 32 * nb, _p(e4m3), _p(ws2), _p(oob)):
         raise ValueError("scale byte 255 (E8M0 NaN)")
     return e4m3, ws2, oob
+
+
+def nvfp4_grouped_gemm(act, codes, scales16, weight_scale_2, group_sizes, n_threads: int = 0,
+                       with_abs: bool = True):
+    """NVFP4 W4A16 grouped GEMM in float64: codes uint8 [E, N, K/2], scales16
+    uint8 [E, N, K/16] (E4M3), weight_scale_2 float32 [E].  Returns
+    (out[rows, N], abs[rows, N] or None)."""
+    act = _c(act, np.uint16)
+    codes, s16 = _c(codes, np.uint8), _c(scales16, np.uint8)
+    ws2, gs = _c(weight_scale_2, np.float32), _c(group_sizes, np.int32)
+    rows, K = act.shape
+    E, N, _ = codes.shape
+    out = np.zeros((rows, N), np.float64)
+    mag = np.zeros((rows, N), np.float64) if with_abs else None
+    rc = _load().oracle_nvfp4_grouped_gemm(_p(act), rows, K, _p(codes), _p(s16), _p(ws2), _p(gs), E,
+                                           N, _p(out), _p(mag) if with_abs else None, n_threads)
+    if rc:
+        raise ValueError("K % 16, sum(group_sizes) != rows, a negative size, or a NaN E4M3 scale")
+    return out, mag

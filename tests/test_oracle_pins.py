@@ -452,3 +452,118 @@ def test_cast_shares_k_max_across_the_fused_rows_and_rejects_nan_scale():
     s[0, 0, 0] = 255
     with pytest.raises(ValueError):
         oracle.mxfp4_to_nvfp4(s)
+
+
+# ------------------------------------------------------------ NVFP4 grouped GEMM
+# "Running DeepSeek V4 Flash on TPU v6", section 1: an NVFP4 kernel decodes the
+# e2m1 weights and their per-16 E4M3 scales; "DeepSeek-V4-Flash-0731-NVFP4",
+# "The lossless weight cast": the per-16 E4M3 scale and the per-tensor
+# weight_scale_2 together reconstruct each weight.  The pins decode E4M3 with
+# torch's float8_e4m3fn and e2m1 from the page's magnitudes, not the oracle.
+
+def _torch_e4m3(bytes_):
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("torch without float8_e4m3fn")
+    t = torch.from_numpy(np.ascontiguousarray(bytes_, np.uint8).reshape(-1)).view(torch.float8_e4m3fn)
+    return t.double().numpy().reshape(np.shape(bytes_))
+
+
+def _e2m1_from_page(codes, mags):
+    E, N, Kh = codes.shape
+    q = np.empty((E, N, 2 * Kh), np.int64)
+    q[..., 0::2], q[..., 1::2] = codes & 15, codes >> 4
+    mag = np.asarray(mags, np.float64)[q & 7]
+    return np.where(q & 8, -mag, mag)
+
+
+def _random_e4m3_scales(rng, shape, lo=0x20, hi=0x58):
+    """Finite E4M3 bytes with random mantissas and both signs (0x7F/0xFF excluded)."""
+    b = rng.integers(lo, hi, size=shape).astype(np.uint8)
+    return b | (rng.integers(0, 2, size=shape).astype(np.uint8) << 7)
+
+
+def test_nvfp4_gemm_tiny_exact_rational(golden_dir):
+    rng = np.random.default_rng(31)
+    mags = _golden_magnitudes(golden_dir)
+    E, N, K = 3, 5, 64
+    gs = np.array([2, 0, 3], np.int32)
+    rows = int(gs.sum())
+    codes = rng.integers(0, 256, size=(E, N, K // 2), dtype=np.uint8)
+    s16 = _random_e4m3_scales(rng, (E, N, K // 16))
+    ws2 = (np.float32(2.0) ** rng.integers(-12, 4, E) * (1 + rng.integers(0, 8, E) / 8)).astype(np.float32)
+    act = inputs.f32_to_bf16_bits(rng.standard_normal((rows, K)).astype(np.float32))
+    out, mag = oracle.nvfp4_grouped_gemm(act, codes, s16, ws2, gs, n_threads=2)
+    a = inputs.bf16_bits_to_f32(act)
+    w2 = _e2m1_from_page(codes, mags)
+    sv = _torch_e4m3(s16)
+    band = np.repeat(np.arange(E), gs)
+    for r in range(rows):
+        e = band[r]
+        for n in range(N):
+            exact = Fraction(0)
+            for k in range(K):
+                w = Fraction(float(w2[e, n, k])) * Fraction(float(sv[e, n, k // 16])) * Fraction(float(ws2[e]))
+                exact += Fraction(float(a[r, k])) * w
+            assert abs(Fraction(out[r, n]) - exact) <= Fraction(mag[r, n]) * Fraction(K, 2 ** 52)
+
+
+def test_nvfp4_gemm_single_expert_is_dense_matmul(golden_dir):
+    rng = np.random.default_rng(32)
+    N, K, rows = 48, 160, 7                      # N != K: a transposed operand fails
+    codes = rng.integers(0, 256, size=(1, N, K // 2), dtype=np.uint8)
+    s16 = _random_e4m3_scales(rng, (1, N, K // 16))
+    ws2 = np.array([0.0625 * 1.375], np.float32)
+    act = inputs.f32_to_bf16_bits(rng.standard_normal((rows, K)).astype(np.float32))
+    out, _ = oracle.nvfp4_grouped_gemm(act, codes, s16, ws2, np.array([rows], np.int32))
+    W = _e2m1_from_page(codes, _golden_magnitudes(golden_dir)) * np.repeat(_torch_e4m3(s16), 16, axis=2)
+    ref = inputs.bf16_bits_to_f32(act).astype(np.float64) @ (W[0] * float(ws2[0])).T
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-300)
+
+
+def test_nvfp4_scale_blocks_are_16_wide_and_tensor_scale_per_expert():
+    # act one-hot at k picks column k: k = 15 and k = 16 fall in different
+    # per-16 blocks; expert 1 has its own per-tensor scale.
+    K, N = 32, 1
+    codes = np.full((2, N, K // 2), 0x22, np.uint8)        # every weight code 1.0
+    s16 = np.zeros((2, N, 2), np.uint8)
+    s16[:, 0, 0] = 0x38                                    # block 0: 1.0
+    s16[:, 0, 1] = 0x44                                    # block 1: 1.5 * 2 = 3.0
+    ws2 = np.array([0.5, 4.0], np.float32)
+    one = inputs.f32_to_bf16_bits(np.array([1.0], np.float32))[0]
+    act = np.zeros((4, K), np.uint16)
+    act[0, 15] = act[1, 16] = act[2, 15] = act[3, 16] = one
+    out, _ = oracle.nvfp4_grouped_gemm(act, codes, s16, ws2, np.array([2, 2], np.int32))
+    np.testing.assert_array_equal(out[:, 0], [0.5, 1.5, 4.0, 12.0])
+
+
+def test_nvfp4_gemm_of_the_lossless_cast_equals_the_mxfp4_gemm():
+    # MXFP4 weights cast losslessly to NVFP4 reconstruct the same values, so
+    # both GEMMs sum identical exact products in the same order.
+    case = inputs.gemm_case(dict(E=6, k=2, T=40, K=128, N=96, exp=(-9, -3)), seed=3)
+    gs, *_ = oracle.route_sort(case["ids"], case["E"])
+    mx, mx_mag = oracle.grouped_gemm(case["act"], case["codes"], case["scales"], gs)
+    e4m3, ws2, oob = oracle.mxfp4_to_nvfp4(case["scales"])
+    assert (oob == 0).all()
+    nv, nv_mag = oracle.nvfp4_grouped_gemm(case["act"], case["codes"], e4m3, ws2.astype(np.float32), gs)
+    np.testing.assert_array_equal(nv, mx)
+    np.testing.assert_array_equal(nv_mag, mx_mag)
+
+
+def test_nvfp4_gemm_rejects_nan_scales_and_bad_sizes_but_never_reads_empty_experts():
+    act = np.zeros((4, 32), np.uint16)
+    codes = np.zeros((2, 8, 16), np.uint8)
+    s16 = np.full((2, 8, 2), 0x38, np.uint8)
+    ws2 = np.ones(2, np.float32)
+    s16[1, 3, 1] = 0x7F                                    # E4M3 NaN in expert 1
+    oracle.nvfp4_grouped_gemm(act, codes, s16, ws2, np.array([4, 0], np.int32))   # expert 1 empty
+    with pytest.raises(ValueError):
+        oracle.nvfp4_grouped_gemm(act, codes, s16, ws2, np.array([1, 3], np.int32))
+    s16[1, 3, 1] = 0xFF
+    with pytest.raises(ValueError):
+        oracle.nvfp4_grouped_gemm(act, codes, s16, ws2, np.array([2, 2], np.int32))
+    with pytest.raises(ValueError):                        # rows != sum(group_sizes)
+        oracle.nvfp4_grouped_gemm(act, codes, s16, ws2, np.array([1, 0], np.int32))
+    with pytest.raises(ValueError):                        # K % 16
+        oracle.nvfp4_grouped_gemm(np.zeros((1, 24), np.uint16), np.zeros((1, 8, 12), np.uint8),
+                                  np.full((1, 8, 1), 0x38, np.uint8), ws2[:1], np.array([1], np.int32))
