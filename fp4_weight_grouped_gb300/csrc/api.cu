@@ -3,6 +3,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/moe_mxfp4.h"
 #include "launch.h"
 
@@ -14,30 +16,27 @@ constexpr size_t kStatusBytes = 256;
 
 thread_local int32_t g_last_launches = 0;
 
-struct DeviceInfo {
-    bool known = false;
-    bool supported = false;
-    int num_sms = 0;
-};
-DeviceInfo g_dev[64];
+// Per device: 0 not yet looked up, -1 not compute capability 10.3, else its
+// SM count.  Host threads may race on the first lookup; each stores the same
+// value, published with release and read with acquire.
+std::atomic<int> g_dev_sms[64];
 
 // Current device must be compute capability 10.3 (GB300).
 moe_status current_device(int *num_sms) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
-    DeviceInfo &d = g_dev[dev];
-    if (!d.known) {
-        int major = 0, minor = 0, sms = 0;
+    int sms = g_dev_sms[dev].load(std::memory_order_acquire);
+    if (sms == 0) {
+        int major = 0, minor = 0, count = 0;
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            cudaDeviceGetAttribute(&count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return MOE_ERR_CUDA;
-        d.supported = (major == 10 && minor == 3);
-        d.num_sms = sms;
-        d.known = true;
+        sms = (major == 10 && minor == 3 && count > 0) ? count : -1;
+        g_dev_sms[dev].store(sms, std::memory_order_release);
     }
-    if (!d.supported) return MOE_ERR_UNSUPPORTED;
-    *num_sms = d.num_sms;
+    if (sms < 0) return MOE_ERR_UNSUPPORTED;
+    *num_sms = sms;
     return MOE_OK;
 }
 

@@ -34,6 +34,8 @@
 //  * Every wait is bounded (no unbounded barrier inside the pipeline); on
 //    timeout the kernel records MOE_ERR_TIMEOUT, drains its own copies and
 //    MMAs, frees tensor memory and returns.
+#include <atomic>
+
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -824,17 +826,18 @@ __global__ void bounded_wait_kernel(uint64_t limit_ns, int *status) {
 
 // ----------------------------------------------------------------- host side
 
+// The driver's tensor-map encoder, looked up once per process (a function-local
+// static is initialised once even when host threads race on the first call).
 static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
         void *ptr = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
                                              cudaEnableDefault, &q) != cudaSuccess ||
             q != cudaDriverEntryPointSuccess)
-            return nullptr;
-        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    }
+            return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }();
     return fn;
 }
 
@@ -915,14 +918,16 @@ moe_status launch_grouped_gemm(const uint16_t *act, int rows, int K, const uint8
     } else {
         tm_scales = tm_codes;
     }
-    static uint64_t attr_dev_mask = 0;
+    // Devices (0..63) whose shared-memory attribute is set; others set it on every call.
+    static std::atomic<uint64_t> attr_dev_mask{0};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
-    if (!(attr_dev_mask & (1ull << (dev & 63)))) {
+    const uint64_t dev_bit = dev >= 0 && dev < 64 ? 1ull << dev : 0;
+    if (!(attr_dev_mask.load(std::memory_order_acquire) & dev_bit) || !dev_bit) {
         if (cudaFuncSetAttribute(grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kSmemBytes) != cudaSuccess)
             return MOE_ERR_CUDA;
-        attr_dev_mask |= 1ull << (dev & 63);
+        attr_dev_mask.fetch_or(dev_bit, std::memory_order_release);
     }
     Params p;
     p.scales = scales;

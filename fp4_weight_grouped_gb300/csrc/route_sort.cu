@@ -18,6 +18,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "device_common.cuh"
@@ -172,14 +173,16 @@ moe_status launch_route_sort(const int32_t *ids, int T, int k, int E, int32_t *g
     *launches = 0;
     if (chunks > 0) {
         const size_t shmem = static_cast<size_t>(32) * E * sizeof(uint16_t);
-        static int attr_dev_mask = 0;
+        // Devices (0..63) whose shared-memory attribute is set; others set it on every call.
+        static std::atomic<uint64_t> attr_dev_mask{0};
         int dev = 0;
-        cudaGetDevice(&dev);
-        if (!(attr_dev_mask & (1 << (dev & 31)))) {
+        if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+        const uint64_t dev_bit = dev >= 0 && dev < 64 ? 1ull << dev : 0;
+        if (!(attr_dev_mask.load(std::memory_order_acquire) & dev_bit) || !dev_bit) {
             if (cudaFuncSetAttribute(rs::count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      32 * 1024 * 2) != cudaSuccess)
                 return MOE_ERR_CUDA;
-            attr_dev_mask |= 1 << (dev & 31);
+            attr_dev_mask.fetch_or(dev_bit, std::memory_order_release);
         }
         rs::count_kernel<<<chunks, rs::kChunk, shmem, stream>>>(ids, rows, E, chunk_tot, rank,
                                                                status);
