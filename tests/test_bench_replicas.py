@@ -60,3 +60,20 @@ def test_whole_job_rate_counts_every_replica():
 def test_reference_arm_runs_on_rank_zero_only():
     args = argparse.Namespace(workload="decode_T64", seed=0, steps=2, warmup=3)
     assert bench.run_reference(args, rank=1, world=2) is None
+
+
+def test_cast_algorithmic_bytes():
+    # one read and two written bytes per scale byte, 4 + 8 bytes per expert
+    assert bench.cast_alg_bytes((256, 4096, 128)) == 3 * 256 * 4096 * 128 + 12 * 256
+    assert bench.cast_alg_bytes((1, 1, 1)) == 15
+
+
+def test_cast_reference_arm_runs_on_rank_zero_only():
+    args = argparse.Namespace(workload="cast_w13", seed=0, steps=2, warmup=3)
+    assert bench.run_reference(args, rank=1, world=2) is None
+
+
+def test_cast_oracle_sample_is_bounded():
+    # a tiny budget still times at least one expert and reports GB/s > 0
+    gbs, ms, sample = bench.run_cast_oracle(1, 1e-6, 0)
+    assert gbs > 0 and ms > 0 and "first 1 of 256" in sample
