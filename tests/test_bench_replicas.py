@@ -77,3 +77,38 @@ def test_cast_oracle_sample_is_bounded():
     # a tiny budget still times at least one expert and reports GB/s > 0
     gbs, ms, sample = bench.run_cast_oracle(1, 1e-6, 0)
     assert gbs > 0 and ms > 0 and "first 1 of 256" in sample
+
+
+def _failing_worker(rank, world, port, q):
+    import datetime
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world,
+                            timeout=datetime.timedelta(seconds=10))
+    if rank == 1:
+        # this replica fails between steps and leaves without reducing
+        os._exit(3)
+    try:
+        bench.reduce_max_over_ranks([1.0, 2.0])
+        q.put((rank, "returned"))
+    except Exception as exc:                     # the peer's exit surfaces as an error
+        q.put((rank, type(exc).__name__))
+
+
+def test_a_replica_that_dies_is_detected_by_the_others():
+    """Failure detection on the host: when one replica exits between steps, the
+    surviving rank's max-over-ranks reduction ends with an error within the
+    process group's timeout instead of hanging."""
+    world = 2
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_failing_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+    assert procs[1].exitcode == 3
+    assert procs[0].exitcode == 0
+    rank, outcome = q.get(timeout=10)
+    assert rank == 0 and outcome != "returned"
