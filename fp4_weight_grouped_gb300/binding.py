@@ -24,6 +24,7 @@ SYMBOLS = (
     "moe_route_sort", "moe_mxfp4_grouped_gemm", "moe_swiglu", "moe_combine", "moe_layer_forward",
     "moe_mxfp4_decode_expert", "moe_debug_bounded_wait", "moe_last_launch_count",
     "moe_route_sort_noalloc", "moe_nvfp4_cast_workspace_bytes", "moe_mxfp4_to_nvfp4",
+    "moe_nvfp4_grouped_gemm",
 )
 
 _lock = threading.Lock()
@@ -69,6 +70,8 @@ def load(path: str | None = None):
                 "moe_last_launch_count": ([], I32),
                 "moe_nvfp4_cast_workspace_bytes": ([I32], SZ),
                 "moe_mxfp4_to_nvfp4": ([P, I32, I32, I32, P, P, P, P, SZ, P], C.c_int),
+                "moe_nvfp4_grouped_gemm": ([P, C.c_int, I64, I32, P, P, P, P, I32, I32, P, C.c_int,
+                                            P, SZ, P], C.c_int),
             }
             for name, (args, res) in sig.items():
                 f = getattr(lib, name)
@@ -193,6 +196,27 @@ def grouped_gemm(act: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor,
                                        _ptr(group_sizes), E, N, _ptr(out), _dtype_code(out.dtype),
                                        _ptr(workspace), workspace.numel(), _stream(stream))
     _check(rc, "moe_mxfp4_grouped_gemm")
+    return out
+
+
+def nvfp4_grouped_gemm(act: torch.Tensor, codes: torch.Tensor, scales16: torch.Tensor,
+                       weight_scale_2: torch.Tensor, group_sizes: torch.Tensor,
+                       out: torch.Tensor | None = None, out_dtype=torch.float32,
+                       workspace: torch.Tensor | None = None, stream=None,
+                       act_layout: int = MOE_ACT_ROW_MAJOR):
+    """act bf16 [rows, K]; codes uint8 [E, N, K/2]; scales16 uint8 [E, N, K/16]
+    (E4M3); weight_scale_2 f32 [E]; group_sizes int32 [E] -> out [rows, N]."""
+    rows, K = act.shape
+    E, N, _ = codes.shape
+    if out is None:
+        out = torch.empty((rows, N), dtype=out_dtype, device=act.device)
+    if workspace is None:
+        workspace = make_workspace(0, 1, 1, act.device, stream)
+    rc = load().moe_nvfp4_grouped_gemm(_ptr(act), act_layout, rows, K, _ptr(codes), _ptr(scales16),
+                                       _ptr(weight_scale_2), _ptr(group_sizes), E, N, _ptr(out),
+                                       _dtype_code(out.dtype), _ptr(workspace), workspace.numel(),
+                                       _stream(stream))
+    _check(rc, "moe_nvfp4_grouped_gemm")
     return out
 
 

@@ -190,6 +190,27 @@ moe_status moe_mxfp4_grouped_gemm(const uint16_t *act, moe_act_layout act_layout
     return st;
 }
 
+moe_status moe_nvfp4_grouped_gemm(const uint16_t *act, moe_act_layout act_layout, int64_t rows,
+                                  int32_t K, const uint8_t *codes, const uint8_t *scales16,
+                                  const float *weight_scale_2, const int32_t *group_sizes,
+                                  int32_t E, int32_t N, void *out, moe_dtype out_dtype,
+                                  void *workspace, size_t workspace_bytes, void *stream) {
+    moe_status st = check_gemm_args(act, act_layout, rows, K, codes, scales16, group_sizes, E, N,
+                                    out, out_dtype, workspace, workspace_bytes);
+    if (st != MOE_OK) return st;
+    if (!weight_scale_2 || !aligned(weight_scale_2, 4)) return MOE_ERR_INVALID_ARG;
+    int sms = 0;
+    if ((st = current_device(&sms)) != MOE_OK) return st;
+    st = moe::launch_grouped_gemm_nvfp4(act, static_cast<int>(rows), K, codes, scales16,
+                                        weight_scale_2, group_sizes, E, N, out,
+                                        out_dtype == MOE_BF16,
+                                        act_layout == MOE_ACT_K8_INTERLEAVED,
+                                        status_word(workspace), kWaitLimitNs,
+                                        static_cast<cudaStream_t>(stream), sms);
+    g_last_launches = rows > 0 ? 1 : 0;
+    return st;
+}
+
 moe_status moe_swiglu(const void *gu, moe_dtype in_dtype, int64_t rows, int32_t I, uint16_t *h,
                       moe_act_layout h_layout, void *stream) {
     if (rows < 0 || I <= 0 || (in_dtype != MOE_F32 && in_dtype != MOE_BF16))

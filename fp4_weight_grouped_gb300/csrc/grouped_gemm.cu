@@ -1,4 +1,11 @@
-// MXFP4 (W4A16) grouped GEMM over expert-sorted row bands, sm_103a.
+// MXFP4 and NVFP4 (W4A16) grouped GEMM over expert-sorted row bands, sm_103a.
+//
+// NVFP4 ("DeepSeek-V4-Flash-0731-NVFP4", "The lossless weight cast": per-16
+// E4M3 block scales under a per-tensor weight_scale_2) runs the same kernel
+// body (grouped_gemm_nvfp4_kernel): every 16 codes take the constant
+// bf16(E4M3 * 2^117) from a 256-entry shared-memory table, so each decoded
+// weight e2m1 * E4M3 * 2^-9 is still one exact bf16 FMA, and the epilogue
+// multiplies the f32 sums by 2^9 * weight_scale_2.
 //
 // What it computes ("Running DeepSeek V4 Flash on TPU v6", section 1, the
 // grouped-matmul loop nest with the decode step): for every expert e with a
@@ -83,7 +90,12 @@ constexpr int kOffMisc = kOffBars + kNumBars * 8;
 constexpr int kOffItems = (kOffMisc + 64 + 15) & ~15;     // int4 per cached work item (16-aligned)
 constexpr int kSmemBytes = kOffItems + kItemCache * 16 + 1024;   // + alignment slack
 
+// NVFP4: a 256-entry table of per-16 scale constants after the item table.
+constexpr int kOffNvTab = kOffItems + kItemCache * 16;
+constexpr int kSmemBytesNv = kOffNvTab + 256 * 4 + 1024;
+
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kSmemBytesNv <= 232448, "shared memory budget (NVFP4)");
 static_assert(kOffItems % 16 == 0, "the item table holds int4 entries");
 static_assert(kCodeStageBytes % 1024 == 0, "ring slots keep the 1024-byte swizzle alignment");
 static_assert(kOffBars % 8 == 0, "barrier alignment");
@@ -152,8 +164,10 @@ struct Ring {
 // Epilogue of one work item for converter warpgroup `wg`: the warpgroup writes
 // its quarter of the item's token columns.  In split mode the four K-partials
 // are added in warpgroup order (deterministic); f32 or bf16 output.
+template <bool kNv>
 __device__ __forceinline__ void store_item(const Params &p, const Item &it, uint32_t acc_base,
-                                           int wg, int row, bool split, uint32_t part_cols) {
+                                           int wg, int row, bool split, uint32_t part_cols,
+                                           float tensor_scale) {
     const int n = it.n0 + row;
     const int qc = it.nt >> 2;                 // columns per warpgroup (multiple of 4)
     for (int c = wg * qc; c < (wg + 1) * qc; c += 4) {
@@ -176,23 +190,57 @@ __device__ __forceinline__ void store_item(const Params &p, const Item &it, uint
                 const int tok = c + t;
                 if (tok < it.nvalid) {
                     const size_t off = static_cast<size_t>(it.row0 + tok) * p.N + n;
+                    float val = __uint_as_float(v[t]);
+                    // NVFP4: the decoded weights carry 2^-9 / weight_scale_2 (exact
+                    // power-of-two scaling); one rounding restores the scale.
+                    if constexpr (kNv) val = (val * 512.0f) * tensor_scale;
                     if (p.out_bf16)
-                        reinterpret_cast<__nv_bfloat16 *>(p.out)[off] =
-                            __float2bfloat16_rn(__uint_as_float(v[t]));
+                        reinterpret_cast<__nv_bfloat16 *>(p.out)[off] = __float2bfloat16_rn(val);
                     else
-                        reinterpret_cast<float *>(p.out)[off] = __uint_as_float(v[t]);
+                        reinterpret_cast<float *>(p.out)[off] = val;
                 }
             }
         }
     }
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
-grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
-                    const __grid_constant__ CUtensorMap tm_act,
-                    const __grid_constant__ CUtensorMap tm_act3,
-                    const __grid_constant__ CUtensorMap tm_scales,
-                    const __grid_constant__ CUtensorMap tm_act64, const Params p) {
+// bf16 bits of E4M3 byte b times 2^117, in both halves of a bf16x2.  Exact:
+// E4M3 has at most four significant bits, and the factor 2^117 keeps every
+// finite value normal in bf16 (2^99 .. 448 * 2^117).  Normal bytes move their
+// exponent by 110 + 127; subnormals m * 2^-9 become m * 2^108; 0x7F / 0xFF
+// (E4M3 NaN) become a bf16 NaN.
+__device__ __forceinline__ uint32_t e4m3_scaled_pair(uint32_t b) {
+    const uint32_t mag = b & 0x7Fu;
+    uint32_t v;
+    if (mag == 0x7Fu) v = 0x7FC0u;
+    else if (mag >= 8u) v = (mag << 4) + (237u << 7);
+    else if (mag == 0u) v = 0u;
+    else v = (__float_as_uint(static_cast<float>(mag)) + (108u << 23)) >> 16;
+    v |= (b & 0x80u) << 8;
+    return v | (v << 16);
+}
+
+// 16 codes (two code words) of one NVFP4 block with its scale constant S:
+// o[4w + j] = (element 8w + j, element 8w + j + 4) times S, for w = 0, 1.
+__device__ __forceinline__ void decode16_scaled(uint32_t c0, uint32_t c1, uint32_t S, uint32_t *o) {
+    uint32_t x[4];
+    e2m1_pairs_scaled_down(c0, x);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) o[j] = bf16x2_fma(x[j], S, 0u);
+    e2m1_pairs_scaled_down(c1, x);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) o[4 + j] = bf16x2_fma(x[j], S, 0u);
+}
+
+// The kernel body for both weight formats.  kNv = false: MXFP4 (per-32 E8M0
+// scales).  kNv = true: NVFP4 (per-16 E4M3 scales `p.scales`, per-expert f32
+// weight_scale_2 `ws2`): each decoded weight is e2m1 * E4M3 * 2^-9, exact in
+// bf16, and the epilogue multiplies by 2^9 * weight_scale_2.
+template <bool kNv>
+__device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUtensorMap &tm_act,
+                                          const CUtensorMap &tm_act3, const CUtensorMap &tm_scales,
+                                          const CUtensorMap &tm_act64, const Params &p,
+                                          const float *ws2) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -276,6 +324,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
     for (int t = tid; t < my_items && t < kItemCache; t += kThreads) {
         const Item it = decode_item(blockIdx.x + t * gridDim.x, roff, ioff, E, p.n_tiles);
         item_cache[t] = make_int4(it.e, it.row0, it.n0, it.nvalid | (it.nt << 16));
+    }
+    uint32_t *nv_tab = reinterpret_cast<uint32_t *>(smem + kOffNvTab);
+    if constexpr (kNv) {
+        for (int t = tid; t < 256; t += kThreads) nv_tab[t] = e4m3_scaled_pair(static_cast<uint32_t>(t));
     }
     auto get_item = [&](int i) -> Item {
         if (i >= kItemCache) return decode_item(blockIdx.x + i * gridDim.x, roff, ioff, E, p.n_tiles);
@@ -524,8 +576,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
                                           kCodeStageBytes + (split ? it.nt * 512u : 0u) +
                                               (scales_here ? kScaleTileBytes : 0u));
                     tma_load_2d(dst, &tm_codes, kc * 128, y, &code_full[r.slot]);
-                    if (scales_here)   // 16 bytes a row: this code stage and its even/odd twin
-                        tma_load_2d(dst + scale_off, &tm_scales, (kc & ~1) * 8, y,
+                    // 16 bytes a row: MXFP4 this code stage and its even/odd twin;
+                    // NVFP4 this code stage's sixteen per-16 scales.
+                    if (scales_here)
+                        tma_load_2d(dst + scale_off, &tm_scales, kNv ? kc * 16 : (kc & ~1) * 8, y,
                                     &code_full[r.slot]);
                     if (split) {
                         for (int grp = 0; grp < it.nt / 16; ++grp) {
@@ -612,7 +666,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
         auto scale_base = [&](int j) -> const uint8_t * {
             const Item it = get_item(j);
             const int n = min(it.n0 + row, p.N - 1);
-            return p.scales + (static_cast<size_t>(it.e) * p.N + n) * p.scale_row + 4 * half;
+            return p.scales + (static_cast<size_t>(it.e) * p.N + n) * p.scale_row +
+                   (kNv ? 8 : 4) * half;
         };
         auto load_scales = [&](const uint8_t *sb, int m) -> uint32_t {
             uint32_t v = 0;
@@ -625,13 +680,27 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
             }
             return v;
         };
+        // NVFP4: the eight per-16 scale bytes of code stage m for this row and
+        // half (blocks 16m + 8h .. 16m + 8h + 7); blocks past K read 1.0 (0x38).
+        auto load_scales_nv = [&](const uint8_t *sbase, int m) -> uint2 {
+            uint32_t v[2] = {0u, 0u};
+#pragma unroll
+            for (int b = 0; b < 8; ++b) {
+                const int blk = 16 * m + 8 * half + b;
+                const uint32_t sbyte =
+                    blk < p.scale_row ? static_cast<uint32_t>(__ldg(sbase + 16 * m + b)) : 0x38u;
+                v[b >> 2] |= sbyte << (8 * (b & 3));
+            }
+            return make_uint2(v[0], v[1]);
+        };
         auto epilogue = [&](int i) -> bool {
             const uint32_t buf = i & 1;
             if (!warp_wait_bounded(&acc_full[buf], (i >> 1) & 1, abort_flag, p.status, lim))
                 return false;
             tc_fence_after();
             const Item it = get_item(i);
-            store_item(p, it, tmem_base + lane_off + buf * acc_cols, wg, row, split, part_cols);
+            store_item<kNv>(p, it, tmem_base + lane_off + buf * acc_cols, wg, row, split, part_cols,
+                            kNv ? __ldg(ws2 + it.e) : 0.0f);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[buf]);
@@ -669,9 +738,21 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
             }
             uint8_t *slot_base = smem + kOffCode + code.slot * ring_stage_bytes;
             const uint32_t sw =
-                p.scale_tma ? *reinterpret_cast<const uint32_t *>(slot_base + scale_off + row * 16 +
-                                                                  (m & 1) * 8 + 4 * half)
-                            : load_scales(sb, m);
+                kNv ? 0u
+                    : (p.scale_tma ? *reinterpret_cast<const uint32_t *>(slot_base + scale_off +
+                                                                         row * 16 + (m & 1) * 8 +
+                                                                         4 * half)
+                                   : load_scales(sb, m));
+            uint2 swn = make_uint2(0u, 0u);        // NVFP4: sub-stage h's four per-16 scales
+            if constexpr (kNv) {
+                swn = p.scale_tma ? *reinterpret_cast<const uint2 *>(slot_base + scale_off +
+                                                                     row * 16 + 8 * half)
+                                  : load_scales_nv(sb, m);
+                // E4M3 NaN bytes (low seven bits all set) are errors.
+                const uint32_t nan = (((swn.x & 0x7F7F7F7Fu) + 0x01010101u) |
+                                      ((swn.y & 0x7F7F7F7Fu) + 0x01010101u)) & 0x80808080u;
+                if (nan && row_ok) bad_scale = 1;
+            }
             uint32_t cw[4][4];
 #pragma unroll
             for (int ch = 0; ch < 4; ++ch) {
@@ -716,7 +797,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
             // errors; the warp agrees on the path.  A byte is above 128 exactly
             // when its top bit and one of its low seven bits are set.
             const uint32_t big = sw & ((sw & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) & 0x80808080u;
-            const bool slow = __any_sync(0xffffffffu, big != 0);
+            const bool slow = !kNv && __any_sync(0xffffffffu, big != 0);
             if (!__all_sync(0xffffffffu, slots_ready) &&
                 (!warp_wait_bounded(&slot_empty[slot0], sphase ^ 1u, abort_flag, p.status, lim) ||
                  !warp_wait_bounded(&slot_empty[slot0 + 1], sphase ^ 1u, abort_flag, p.status,
@@ -728,6 +809,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
 #pragma unroll
             for (int h = 0; h < 2; ++h) {          // sub-stage 2·half + h -> A slot slot0 + h
                 uint32_t o[32];
+                if constexpr (kNv) {
+                    // Per-16 blocks: words 0-1 and 2-3 of each 32-code chunk.
+                    const uint32_t sv = h ? swn.y : swn.x;
+                    decode16_scaled(cw[2 * h][0], cw[2 * h][1], nv_tab[sv & 0xFFu], &o[0]);
+                    decode16_scaled(cw[2 * h][2], cw[2 * h][3], nv_tab[(sv >> 8) & 0xFFu], &o[8]);
+                    decode16_scaled(cw[2 * h + 1][0], cw[2 * h + 1][1], nv_tab[(sv >> 16) & 0xFFu],
+                                    &o[16]);
+                    decode16_scaled(cw[2 * h + 1][2], cw[2 * h + 1][3], nv_tab[sv >> 24], &o[24]);
+                } else {
                 if (__builtin_expect(!slow, 1)) {
                     // Scale byte b of sw in both 16-bit halves, then 2^(s-1) as bf16x2.
                     const uint32_t sp0 = prmt(sw, 0u, h ? 0x4242u : 0x4040u);
@@ -739,6 +829,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
                         bad_scale = 1;
                     if (!decode32_any(cw[2 * h + 1], (sw >> (16 * h + 8)) & 0xFFu, &o[16]) && row_ok)
                         bad_scale = 1;
+                }
                 }
                 __syncwarp();
                 tmem_st32(a_base + h * kAColsPerSlot, o);
@@ -781,6 +872,25 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
         __syncwarp();
         tmem_dealloc(tmem_base, kTmemCols);
     }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
+                    const __grid_constant__ CUtensorMap tm_act,
+                    const __grid_constant__ CUtensorMap tm_act3,
+                    const __grid_constant__ CUtensorMap tm_scales,
+                    const __grid_constant__ CUtensorMap tm_act64, const Params p) {
+    gemm_body<false>(tm_codes, tm_act, tm_act3, tm_scales, tm_act64, p, nullptr);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+grouped_gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tm_codes,
+                          const __grid_constant__ CUtensorMap tm_act,
+                          const __grid_constant__ CUtensorMap tm_act3,
+                          const __grid_constant__ CUtensorMap tm_scales,
+                          const __grid_constant__ CUtensorMap tm_act64, const Params p,
+                          const float *__restrict__ ws2) {
+    gemm_body<true>(tm_codes, tm_act, tm_act3, tm_scales, tm_act64, p, ws2);
 }
 
 // Debug view of the decode: one thread per (weight row n, 32-element block); the
@@ -841,10 +951,14 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
     return fn;
 }
 
-moe_status launch_grouped_gemm(const uint16_t *act, int rows, int K, const uint8_t *codes,
-                               const uint8_t *scales, const int32_t *group_sizes, int E, int N,
-                               void *out, int out_bf16, int act_k8, int *status,
-                               uint64_t wait_limit_ns, cudaStream_t stream, int num_sms) {
+// Both weight formats.  kNv = false: `scales` are per-32 E8M0 bytes [E, N, K/32].
+// kNv = true: `scales` are per-16 E4M3 bytes [E, N, K/16] and ws2 the per-expert
+// f32 weight_scale_2.
+template <bool kNv>
+static moe_status launch_gemm(const uint16_t *act, int rows, int K, const uint8_t *codes,
+                              const uint8_t *scales, const float *ws2, const int32_t *group_sizes,
+                              int E, int N, void *out, int out_bf16, int act_k8, int *status,
+                              uint64_t wait_limit_ns, cudaStream_t stream, int num_sms) {
     using namespace gemm;
     if (rows == 0) return MOE_OK;
     PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode_fn();
@@ -901,13 +1015,16 @@ moe_status launch_grouped_gemm(const uint16_t *act, int rows, int K, const uint8
     } else {
         tm_act3 = tm_act;
     }
-    // Scale tiles: [E*N rows][K/32 bytes], boxes of 16 bytes (two code stages) x
-    // 128 rows, when the row pitch and the base allow 16-byte TMA rows.
-    const int scale_tma = (K % 512) == 0 && (reinterpret_cast<uintptr_t>(scales) & 15) == 0;
+    // Scale tiles: [E*N rows][scale bytes a row], boxes of 16 bytes x 128 rows,
+    // when the row pitch and the base allow 16-byte TMA rows.  MXFP4: K/32
+    // bytes a row, a box covers two code stages.  NVFP4: K/16 bytes a row, a box
+    // covers one code stage.
+    const int scale_row = kNv ? K / 16 : K / 32;
+    const int scale_tma = (K % (kNv ? 256 : 512)) == 0 && (reinterpret_cast<uintptr_t>(scales) & 15) == 0;
     if (scale_tma) {
-        cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 32),
+        cuuint64_t dims[2] = {static_cast<cuuint64_t>(scale_row),
                               static_cast<cuuint64_t>(E) * static_cast<cuuint64_t>(N)};
-        cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 32)};
+        cuuint64_t strides[1] = {static_cast<cuuint64_t>(scale_row)};
         cuuint32_t box[2] = {16, 128};
         cuuint32_t estr[2] = {1, 1};
         if (encode(&tm_scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(scales), dims,
@@ -918,15 +1035,20 @@ moe_status launch_grouped_gemm(const uint16_t *act, int rows, int K, const uint8
     } else {
         tm_scales = tm_codes;
     }
-    // Devices (0..63) whose shared-memory attribute is set; others set it on every call.
+    // Devices (0..63) whose shared-memory attribute is set (one mask per format);
+    // others set it on every call.
     static std::atomic<uint64_t> attr_dev_mask{0};
+    const int smem_bytes = kNv ? kSmemBytesNv : kSmemBytes;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
     const uint64_t dev_bit = dev >= 0 && dev < 64 ? 1ull << dev : 0;
     if (!(attr_dev_mask.load(std::memory_order_acquire) & dev_bit) || !dev_bit) {
-        if (cudaFuncSetAttribute(grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemBytes) != cudaSuccess)
-            return MOE_ERR_CUDA;
+        const cudaError_t rc =
+            kNv ? cudaFuncSetAttribute(grouped_gemm_nvfp4_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes)
+                : cudaFuncSetAttribute(grouped_gemm_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+        if (rc != cudaSuccess) return MOE_ERR_CUDA;
         attr_dev_mask.fetch_or(dev_bit, std::memory_order_release);
     }
     Params p;
@@ -941,16 +1063,37 @@ moe_status launch_grouped_gemm(const uint16_t *act, int rows, int K, const uint8
     p.out_bf16 = out_bf16;
     p.n_tiles = (N + kBN - 1) / kBN;
     p.k_stages = 4 * ((K + kCodeK - 1) / kCodeK);
-    p.scale_row = K / 32;
+    p.scale_row = scale_row;
     p.scale_vec2 = ((K / 32) % 2 == 0) && ((reinterpret_cast<uintptr_t>(scales) & 1) == 0);
     p.scale_full = p.scale_vec2 && (K % kCodeK) == 0;
     p.wait_limit_ns = wait_limit_ns;
     p.act_k8 = act_k8;
     p.act3d = act3d;
     p.scale_tma = scale_tma;
-    grouped_gemm_kernel<<<num_sms, kThreads, kSmemBytes, stream>>>(tm_codes, tm_act, tm_act3,
-                                                                   tm_scales, tm_act64, p);
+    if constexpr (kNv)
+        grouped_gemm_nvfp4_kernel<<<num_sms, kThreads, smem_bytes, stream>>>(
+            tm_codes, tm_act, tm_act3, tm_scales, tm_act64, p, ws2);
+    else
+        grouped_gemm_kernel<<<num_sms, kThreads, smem_bytes, stream>>>(tm_codes, tm_act, tm_act3,
+                                                                       tm_scales, tm_act64, p);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status launch_grouped_gemm(const uint16_t *act, int rows, int K, const uint8_t *codes,
+                               const uint8_t *scales, const int32_t *group_sizes, int E, int N,
+                               void *out, int out_bf16, int act_k8, int *status,
+                               uint64_t wait_limit_ns, cudaStream_t stream, int num_sms) {
+    return launch_gemm<false>(act, rows, K, codes, scales, nullptr, group_sizes, E, N, out,
+                              out_bf16, act_k8, status, wait_limit_ns, stream, num_sms);
+}
+
+moe_status launch_grouped_gemm_nvfp4(const uint16_t *act, int rows, int K, const uint8_t *codes,
+                                     const uint8_t *scales16, const float *weight_scale_2,
+                                     const int32_t *group_sizes, int E, int N, void *out,
+                                     int out_bf16, int act_k8, int *status,
+                                     uint64_t wait_limit_ns, cudaStream_t stream, int num_sms) {
+    return launch_gemm<true>(act, rows, K, codes, scales16, weight_scale_2, group_sizes, E, N, out,
+                             out_bf16, act_k8, status, wait_limit_ns, stream, num_sms);
 }
 
 moe_status launch_decode_expert(const uint8_t *codes, const uint8_t *scales, int N, int K, int e,

@@ -20,7 +20,7 @@ import numpy as np
 
 # Stream tags keep each tensor's random stream independent of the others, so a
 # caller can regenerate one tensor without drawing the rest.
-_TAG_ROUTE, _TAG_ACT, _TAG_W13, _TAG_W2, _TAG_X, _TAG_GATE, _TAG_SCALES = 1, 2, 3, 4, 5, 6, 7
+_TAG_ROUTE, _TAG_ACT, _TAG_W13, _TAG_W2, _TAG_X, _TAG_GATE, _TAG_SCALES, _TAG_NV = 1, 2, 3, 4, 5, 6, 7, 8
 
 CONFIGS = {
     # Tiny MXFP4 grouped GEMM: E=8, top-2, T=16 (32 rows), K=256, N=512,
@@ -113,6 +113,23 @@ def e8m0_scales(seed: int, shape, lo: int, hi: int, tag: int = _TAG_SCALES) -> n
     """E8M0 scale bytes drawn uniformly from lo..hi (inclusive), uint8 of `shape`."""
     assert 0 <= lo <= hi <= 255
     return _rng(seed, tag, lo, hi).integers(lo, hi + 1, size=shape, dtype=np.int64).astype(np.uint8)
+
+
+def e4m3_scales(seed: int, shape, lo: int = 0x28, hi: int = 0x48, signs: bool = False) -> np.ndarray:
+    """E4M3 scale bytes: the low seven bits uniform in lo..hi (inclusive, at
+    most 0x7E so no NaN is drawn), the sign bit random when `signs`."""
+    assert 0 <= lo <= hi <= 0x7E
+    rng = _rng(seed, _TAG_NV, lo, hi)
+    b = rng.integers(lo, hi + 1, size=shape, dtype=np.int64)
+    if signs:
+        b |= rng.integers(0, 2, size=shape, dtype=np.int64) << 7
+    return b.astype(np.uint8)
+
+
+def tensor_scales(seed: int, E: int) -> np.ndarray:
+    """Per-expert float32 scales 2^U{-12..4} * (1 + U{0..7}/8)."""
+    rng = _rng(seed, _TAG_NV, E)
+    return (np.ldexp(1.0, rng.integers(-12, 5, E)) * (1 + rng.integers(0, 8, E) / 8)).astype(np.float32)
 
 
 def normal_bf16(seed: int, tag: int, shape) -> np.ndarray:

@@ -205,6 +205,34 @@ MOE_API moe_status moe_mxfp4_grouped_gemm(const uint16_t *act, moe_act_layout ac
                                   void *stream);
 
 /*
+ * moe_nvfp4_grouped_gemm — the same grouped matmul with NVFP4 weights ([TPU]
+ * section 1: the NVFP4 kernel that decodes e2m1 weights and per-16 E4M3 scales;
+ * [NVFP4] "The lossless weight cast": per-16 E4M3 block scales under a
+ * per-tensor f32 weight_scale_2).
+ *
+ *   out[r, n] = sum_k act[r, k] * e2m1(code[e, n, k]) * e4m3(scales16[e, n, k/16])
+ *                              * weight_scale_2[e]
+ *
+ * for every row r of band e.  Arguments as for moe_mxfp4_grouped_gemm, except:
+ *  scales16        device uint8 [E, N, K/16]: E4M3 bytes (sign, 4 exponent bits
+ *                  with bias 7, 3 mantissa bits).  0x7F and 0xFF (NaN) set
+ *                  MOE_ERR_DATA and produce NaN.
+ *  weight_scale_2  device f32 [E], 4-byte aligned.
+ *  K               multiple of 32.
+ * Each weight e2m1 * E4M3 * 2^-9 is exact in bf16, its products with bf16
+ * activations are exact in f32, and the f32 sums are multiplied by 2^9 *
+ * weight_scale_2 once per output.  Weights cast losslessly from MXFP4
+ * (moe_mxfp4_to_nvfp4) therefore give exactly the outputs of
+ * moe_mxfp4_grouped_gemm on the original weights.
+ */
+MOE_API moe_status moe_nvfp4_grouped_gemm(const uint16_t *act, moe_act_layout act_layout,
+                                          int64_t rows, int32_t K, const uint8_t *codes,
+                                          const uint8_t *scales16, const float *weight_scale_2,
+                                          const int32_t *group_sizes, int32_t E, int32_t N,
+                                          void *out, moe_dtype out_dtype, void *workspace,
+                                          size_t workspace_bytes, void *stream);
+
+/*
  * moe_swiglu — gate/up activation on the fused w13 output ([TPU] section 1,
  * where the activation is timed apart from the grouped matmuls; [NVFP4]: w1
  * and w3 fused into the first GEMM).

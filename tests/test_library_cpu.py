@@ -82,6 +82,25 @@ def test_nvfp4_cast_workspace_and_host_checks(lib):
     assert call(wsb=256 + 15) == INVALID    # E = 4 needs 256 + 256 bytes
 
 
+def test_nvfp4_gemm_rejects_bad_arguments_on_host(lib):
+    f = lib.moe_nvfp4_grouped_gemm
+    P = C.c_void_p
+    f.argtypes = [P, C.c_int, C.c_int64, C.c_int32, P, P, P, P, C.c_int32, C.c_int32, P, C.c_int, P,
+                  C.c_size_t, P]
+    f.restype = C.c_int
+    fake = P(4096)
+
+    def call(K=256, ws2=fake, s16=fake):
+        return f(fake, 0, 8, K, fake, s16, ws2, fake, 4, 128, fake, 0, fake, 1 << 12, None)
+
+    INVALID = 1
+    assert call(ws2=None) == INVALID
+    assert call(ws2=P(4098)) == INVALID     # f32 scales need 4-byte alignment
+    assert call(s16=None) == INVALID
+    assert call(K=48) == INVALID            # K % 32
+    assert call(K=0) == INVALID
+
+
 def test_gemm_rejects_bad_arguments_on_host(lib):
     f = lib.moe_mxfp4_grouped_gemm
     P = C.c_void_p
