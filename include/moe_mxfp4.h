@@ -31,9 +31,10 @@
  *  - Return value: argument errors found on the host (null pointer, bad size,
  *    misalignment, unsupported device) and launch failures are returned
  *    synchronously.  Errors that depend on device data (an expert id out of
- *    range, group sizes that do not add up, a scale byte above 252, a pipeline
- *    wait that gave up) are recorded in the status word of the caller's
- *    workspace and read with moe_read_status().  The first error recorded wins.
+ *    range, group sizes that do not add up, a scale byte the format does not
+ *    allow, a pipeline wait that gave up) are recorded in the status word of
+ *    the caller's workspace and read with moe_read_status().  The first error
+ *    recorded wins.
  *  - Only compute capability 10.3 (GB300, sm_103a) is supported.
  */
 #ifndef MOE_MXFP4_H
@@ -58,7 +59,9 @@ typedef enum {
     MOE_ERR_UNSUPPORTED = 2, /* device is not compute capability 10.3 */
     MOE_ERR_CUDA = 3,        /* a CUDA runtime/driver call or launch failed */
     MOE_ERR_DATA = 4,        /* device-side: id out of range, sum(group_sizes) != rows,
-                                negative group size, or scale byte > 252 */
+                                negative group size, an E8M0 scale byte > 252 in the
+                                MXFP4 GEMM or 255 in the cast, or an E4M3 NaN scale
+                                in the NVFP4 GEMM */
     MOE_ERR_TIMEOUT = 5,     /* device-side: a pipeline wait exceeded its bound */
     MOE_ERR_CAPACITY = 6     /* host check: the problem needs more scratch than a
                                 fixed-capacity entry point holds */
