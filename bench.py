@@ -5,18 +5,21 @@ One step = one pass of the whole routed-expert path over one batch:
 route sort (+ activation gather) -> w13 grouped GEMM -> SwiGLU -> w2 grouped GEMM
 -> combine, all launched through the C ABI on one CUDA stream.
 
-Default workload (N=1): the decode shape of 64 tokens, 256 experts, top-6 (384
-sorted rows), w13 K = N = 4096, w2 K = 2048, N = 4096.  Other workloads
-(--workload) are the prefill and full-layer shapes.
+Default workload (N=1): the full MoE layer, T = 8192 tokens, 256 experts, top-6
+(49152 sorted rows), w13 K = N = 4096, w2 K = 2048, N = 4096: the largest
+single-GPU configuration.  The same run also times the decode (T = 64, 256) and
+prefill (T = 4096) shapes and reports them under "workloads".
 
 Prints one JSON line (rank 0).  value = grouped-GEMM TFLOP/s of the whole step
 (2 * rows * K * N for both GEMMs / step time); also reported: weight GB/s
 (touched experts x N x K x 17/32 bytes per GEMM), the roofline of the dominant
-kernel, an end-to-end number through host buffers, the CPU oracle baseline and
-the SM clocks seen during the timed region.
+kernel (the w13 launch), an end-to-end number through host buffers, the CPU
+oracle baseline and the SM clocks seen during the timed region.
 
---impl reference times the CPU oracle on the host cores instead (a bounded
-sample of the same workload per step).
+--gpus N without a torchrun environment starts N replica processes through
+torch.distributed.run (one per GPU, weak scaling).  --impl reference times the
+CPU oracle on the host cores instead (a bounded sample of the same workload per
+step).
 """
 from __future__ import annotations
 
@@ -46,7 +49,7 @@ WORKLOADS = {
     "cast_w13": "Lossless MXFP4 -> NVFP4 scale cast of the w13 scales: E8M0 [256, 4096, 128] "
                 "(128 MiB) -> E4M3 [256, 4096, 256] + per-expert f32 scale + out-of-range count",
 }
-DEFAULT_STEPS = {"decode_T64": 2000, "decode_T256": 1000, "prefill_T4096": 60, "layer_T8192": 30,
+DEFAULT_STEPS = {"decode_T64": 2000, "decode_T256": 1000, "prefill_T4096": 300, "layer_T8192": 300,
                  "cast_w13": 200}
 CAST_METRIC = "lossless MXFP4 -> NVFP4 scale cast GB/s (algorithmic bytes), % of measured HBM, 1 GPU"
 CAST_SHAPE, CAST_BYTES = (256, 4096, 128), (117, 125)   # w13 scale tensor, exponents [-10, -2]
@@ -57,7 +60,7 @@ FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
 # DRAM bytes (read + write) per launch of the w13 GEMM kernel measured by ncu for
 # each workload, with the hash of the kernel source they were taken on.  A
 # changed kernel reports traffic = null until re-measured.
-NCU_TRAFFIC = {"decode_T64": 1785893000 + 9752064}   # ncu capture summarised under profiles/
+NCU_TRAFFIC = {"decode_T64": 1785893000 + 9752064}
 NCU_KERNEL_HASH = "9e4fd4cd9e3ab695"
 
 WEIGHT_BYTES_PER_ELEM = 17.0 / 32.0       # 4-bit code + one E8M0 byte per 32
@@ -179,6 +182,112 @@ class ClockSampler:
 
 # ---------------------------------------------------------------------- our arm
 
+def kernel_roofline(flops, wbytes, extra_bytes, ms, hbm, bf16):
+    """Roofline of one grouped-GEMM launch: the bound is the slower of its FLOPs
+    at the bf16 tensor peak and its touched-expert weight bytes at HBM peak."""
+    t_flop = flops / (bf16 * 1e12)
+    t_byte = wbytes / (hbm * 1e9)
+    sec = ms * 1e-3
+    out = {"ms": round(ms, 5), "tflops": round(flops / sec / 1e12, 2),
+           "weight_GBps": round(wbytes / sec / 1e9, 1),
+           "bound": "hbm" if t_byte > t_flop else "tensor",
+           "frac_of_bound": round(max(t_flop, t_byte) / sec, 4),
+           "frac_hbm": round((wbytes + extra_bytes) / sec / 1e9 / hbm, 4),
+           "frac_tensor": round(flops / sec / 1e12 / bf16, 4)}
+    return out
+
+
+class Workload:
+    """One full-path workload on the device: routing, token activations and the
+    caller-owned intermediates; the weights are shared between workloads."""
+
+    def __init__(self, name, seed, dev, wts, B, inputs):
+        self.name, self.B, self.dev, self.wts = name, B, dev, wts
+        c = inputs.workload_tokens(name, seed)
+        self.T, self.k, self.E, self.H = c["T"], c["k"], c["E"], c["hidden"]
+        self.I = wts["w13_codes"].shape[1] // 2
+        self.x = B.bf16_from_bits(c["x"], dev)
+        self.ids = B.to_device(c["ids"], dev)
+        self.w = B.to_device(c["topk_w"], dev)
+        self.bufs = B.LayerBuffers(self.T, self.k, self.E, self.H, self.I, dev)
+
+    def step(self, ev=None):
+        """route sort (+ gather) -> w13 -> SwiGLU -> w2 -> combine.  ev: four
+        events recorded around the two grouped-GEMM launches."""
+        B, b, w = self.B, self.bufs, self.wts
+        K8 = B.MOE_ACT_K8_INTERLEAVED     # the layer path keeps activations in the GEMM's k order
+        stream = self.stream
+        gsz, _, _, s2r, xs = B.route_sort(self.ids, self.E, self.x, b.workspace,
+                                          out=(b.group_sizes, b.group_offsets, b.sorted_slot,
+                                               b.slot_to_row, b.x_sorted), x_layout=K8)
+        if ev is not None:
+            ev[0].record(stream)
+        B.grouped_gemm(xs, w["w13_codes"], w["w13_scales"], gsz, out=b.y13, workspace=b.workspace,
+                       act_layout=K8)
+        if ev is not None:
+            ev[1].record(stream)
+        B.swiglu(b.y13, out=b.h, layout=K8)
+        if ev is not None:
+            ev[2].record(stream)
+        B.grouped_gemm(b.h, w["w2_codes"], w["w2_scales"], gsz, out=b.y2, workspace=b.workspace,
+                       act_layout=K8)
+        if ev is not None:
+            ev[3].record(stream)
+        B.combine(b.y2, s2r, self.w, out=b.out)
+
+    LAUNCHES_PER_STEP = 7     # count, scan, scatter, w13, SwiGLU, w2, combine
+
+    def warm(self, n):
+        import torch
+        self.stream = torch.cuda.current_stream(self.dev)
+        for _ in range(n):
+            self.step()
+        torch.cuda.synchronize(self.dev)
+        st = self.B.read_status(self.bufs.workspace)
+        if st != self.B.MOE_OK:
+            raise RuntimeError(f"{self.name}: device status after warm-up: {self.B.status_string(st)}")
+        gs = self.bufs.group_sizes.cpu().numpy()
+        self.f13, self.b13, self.touched, self.rows = gemm_work(gs, self.H, 2 * self.I)
+        self.f2, self.b2, _, _ = gemm_work(gs, self.I, self.H)
+        # activation and output bytes of each launch (read act, write f32 out)
+        self.x13 = self.rows * self.H * 2 + self.rows * 2 * self.I * 4
+        self.x2 = self.rows * self.I * 2 + self.rows * self.H * 4
+
+    def timed(self, steps):
+        """Exactly `steps` steps between two events; per-step GEMM launch events."""
+        import torch
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(self.dev)
+        t0.record(self.stream)
+        for i in range(steps):
+            self.step(ev[i])
+        t1.record(self.stream)
+        torch.cuda.synchronize(self.dev)
+        st = self.B.read_status(self.bufs.workspace)
+        if st != self.B.MOE_OK:
+            raise RuntimeError(f"{self.name}: device status after timing: {self.B.status_string(st)}")
+        ms = t0.elapsed_time(t1) / steps
+        w13 = statistics.fmean(e[0].elapsed_time(e[1]) for e in ev)
+        w2 = statistics.fmean(e[2].elapsed_time(e[3]) for e in ev)
+        return ms, w13, w2
+
+    def summary(self, ms, w13, w2, hbm, bf16):
+        return {"T": self.T, "rows": self.rows, "touched_experts": self.touched,
+                "ms_per_step": round(ms, 5),
+                "gemm_tflops": round((self.f13 + self.f2) / (ms * 1e-3) / 1e12, 2),
+                "w13": kernel_roofline(self.f13, self.b13, self.x13, w13, hbm, bf16),
+                "w2": kernel_roofline(self.f2, self.b2, self.x2, w2, hbm, bf16)}
+
+    def free(self):
+        del self.bufs, self.x, self.ids, self.w
+
+
+SUB_WORKLOADS = ("decode_T64", "decode_T256", "prefill_T4096")
+SUB_STEPS = {"decode_T64": 300, "decode_T256": 300, "prefill_T4096": 100, "layer_T8192": 60}
+SUSTAIN_S = 1.0          # the clock record covers at least this much back-to-back work
+
+
 def run_ours(args, rank, world, local):
     import numpy as np
     import torch
@@ -190,82 +299,59 @@ def run_ours(args, rank, world, local):
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    c = inputs.layer_workload(args.workload, seed=args.seed + rank)
-    T, k, E, H, I = c["T"], c["k"], c["E"], c["hidden"], c["inter"]
-    x = B.bf16_from_bits(c["x"], dev)
-    ids = B.to_device(c["ids"], dev)
-    w = B.to_device(c["topk_w"], dev)
-    w13c, w13s = B.to_device(c["w13_codes"], dev), B.to_device(c["w13_scales"], dev)
-    w2c, w2s = B.to_device(c["w2_codes"], dev), B.to_device(c["w2_scales"], dev)
-    del c
-    bufs = B.LayerBuffers(T, k, E, H, I, dev)
-    stream = torch.cuda.current_stream(dev)
-    ws = bufs.workspace
-    K8 = B.MOE_ACT_K8_INTERLEAVED     # the layer path keeps activations in the GEMM's k order
+    hbm, bf16_burst, bf16_sus, peak_src = load_peaks()
+    wts = {k: B.to_device(v, dev) for k, v in inputs.layer_weights(args.seed + rank).items()}
 
-    def step(ev13=None):
-        gsz, _, _, s2r, xs = B.route_sort(ids, E, x, ws, out=(bufs.group_sizes, bufs.group_offsets,
-                                                                bufs.sorted_slot, bufs.slot_to_row,
-                                                                bufs.x_sorted), x_layout=K8)
-        if ev13 is not None:
-            ev13[0].record(stream)
-        B.grouped_gemm(xs, w13c, w13s, gsz, out=bufs.y13, workspace=ws, act_layout=K8)
-        if ev13 is not None:
-            ev13[1].record(stream)
-        B.swiglu(bufs.y13, out=bufs.h, layout=K8)
-        B.grouped_gemm(bufs.h, w2c, w2s, gsz, out=bufs.y2, workspace=ws, act_layout=K8)
-        B.combine(bufs.y2, s2r, w, out=bufs.out)
+    # ---- the other workloads first (each its own warm-up and timed steps)
+    subs = {}
+    if not args.no_sub_workloads:
+        for name in SUB_WORKLOADS:
+            if name == args.workload:
+                continue
+            wl = Workload(name, args.seed + rank, dev, wts, B, inputs)
+            wl.warm(max(3, args.warmup))
+            ms, w13, w2 = wl.timed(SUB_STEPS[name])
+            subs[name] = dict(wl.summary(ms, w13, w2, hbm, bf16_burst), steps=SUB_STEPS[name])
+            wl.free()
+            del wl
+            torch.cuda.empty_cache()
 
-    launches_per_step = 7
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize(dev)
-    st = B.read_status(ws)
-    if st != B.MOE_OK:
-        raise RuntimeError(f"device status after warm-up: {B.status_string(st)}")
-    # Work accounting from the library's own routing output.
-    gs_np = bufs.group_sizes.cpu().numpy()
-    f13, b13, touched, rows = gemm_work(gs_np, H, 2 * I)
-    f2, b2, _, _ = gemm_work(gs_np, I, H)
-    act_bytes13 = rows * H * 2 + rows * 2 * I * 4          # x_sorted read + y13 (f32) write
-
+    # ---- the headline workload: exactly K timed steps
+    wl = Workload(args.workload, args.seed + rank, dev, wts, B, inputs)
+    wl.warm(args.warmup)
     K = args.steps
-    ev_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
         wall0 = time.time()
-        t0.record(stream)
-        for i in range(K):
-            step(ev_pairs[i])
-        t1.record(stream)
-        torch.cuda.synchronize(dev)
+        ms_step, w13_ms, w2_ms = wl.timed(K)
+        # The same steps back to back for at least SUSTAIN_S more, inside the
+        # clock record, so that the clocks are those of sustained load.
+        n_sus = int(min(5000, max(1, SUSTAIN_S / (ms_step * 1e-3))))
+        ms_sus, w13_sus, _ = wl.timed(n_sus)
         wall1 = time.time()
     if world > 1:
         torch.distributed.barrier()
     clocks = clk.summary(wall0, wall1)
-    ms_total = t0.elapsed_time(t1)
-    w13_ms = [a.elapsed_time(b) for a, b in ev_pairs]
-    st = B.read_status(ws)
-    if st != B.MOE_OK:
-        raise RuntimeError(f"device status after timing: {B.status_string(st)}")
 
     # ---- end to end through host buffers (pinned), same path via moe_layer_forward
+    bufs, x, ids, w = wl.bufs, wl.x, wl.ids, wl.w
+    T, H = wl.T, wl.H
     hx = torch.from_numpy(B.bits_from_bf16(x).view(np.int16)).pin_memory()
     hids = ids.cpu().pin_memory()
     hw = w.cpu().pin_memory()
     hout = torch.empty((T, H), dtype=torch.float32).pin_memory()
     dx, dids, dw = torch.empty_like(x), torch.empty_like(ids), torch.empty_like(w)
+    stream = wl.stream
     e2e_steps = max(3, min(K, 200))
 
     def e2e_step():
         dx.view(torch.int16).copy_(hx, non_blocking=True)
         dids.copy_(hids, non_blocking=True)
         dw.copy_(hw, non_blocking=True)
-        B.layer_forward(dx, dids, dw, w13c, w13s, w2c, w2s, bufs)
+        B.layer_forward(dx, dids, dw, wts["w13_codes"], wts["w13_scales"], wts["w2_codes"],
+                        wts["w2_scales"], bufs)
         hout.copy_(bufs.out, non_blocking=True)
 
     for _ in range(3):
@@ -278,17 +364,20 @@ def run_ours(args, rank, world, local):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
+    if B.read_status(bufs.workspace) != B.MOE_OK:
+        raise RuntimeError("device status after the end-to-end steps")
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     h2d = hx.numel() * 2 + hids.numel() * 4 + hw.numel() * 4
     d2h = hout.numel() * 4
 
     # ---- aggregate over ranks (max time)
-    ms_step, e2e_ms = reduce_max_over_ranks([ms_total / K, e2e_ms], device=dev)
-    flops = f13 + f2
-    hbm, bf16_burst, bf16_sus, peak_src = load_peaks()
-    w13_avg_ms = statistics.fmean(w13_ms)
-    w13_alg_bytes = b13 + act_bytes13
-    achieved = w13_alg_bytes / (w13_avg_ms * 1e-3) / 1e9
+    ms_step, e2e_ms = reduce_max_over_ranks([ms_step, e2e_ms], device=dev)
+    flops = wl.f13 + wl.f2
+    head = wl.summary(ms_step, w13_ms, w2_ms, hbm, bf16_burst)
+    r13 = head["w13"]
+    bound = r13["bound"]
+    achieved_tf = wl.f13 / (w13_ms * 1e-3) / 1e12
+    achieved_gb = (wl.b13 + wl.x13) / (w13_ms * 1e-3) / 1e9
     traffic = None
     if NCU_KERNEL_HASH is not None and NCU_KERNEL_HASH == kernel_source_hash():
         traffic = NCU_TRAFFIC.get(args.workload)
@@ -306,40 +395,41 @@ def run_ours(args, rank, world, local):
         "dtype": "bf16",
         "data": "synthetic: seeded numpy PCG64; bf16 N(0,1) tokens; uniform e2m1 nibbles with E8M0 "
                 "exponents in [-10,-2]; routing per workload",
-        "config": {"workload": args.workload, "description": WORKLOADS[args.workload], "T": T, "E": E,
-                   "top_k": k, "hidden": H, "inter": I, "rows": rows, "touched_experts": touched,
+        "config": {"workload": args.workload, "description": WORKLOADS[args.workload], "T": wl.T,
+                   "E": wl.E, "top_k": wl.k, "hidden": wl.H, "inter": wl.I, "rows": wl.rows,
+                   "touched_experts": wl.touched,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2: %.2f GB of touched MXFP4 weights per step vs 129 MB L2; "
-                         "no flush" % ((b13 + b2) / 1e9)},
-        "weight_GBps": round(whole_job_rate(b13 + b2, ms_step, world) / 1e9, 1),
+                         "no flush" % ((wl.b13 + wl.b2) / 1e9)},
+        "weight_GBps": round(whole_job_rate(wl.b13 + wl.b2, ms_step, world) / 1e9, 1),
         "gemm_flops_per_step": flops,
-        "weight_bytes_per_step": b13 + b2,
+        "weight_bytes_per_step": wl.b13 + wl.b2,
         "roofline": {
-            "kernel": "grouped_gemm_kernel (w13)",
-            "bound": "hbm" if b13 / (hbm * 1e9) > f13 / (bf16_sus * 1e12) else "tensor",
-            "achieved": round(achieved, 1) if b13 / (hbm * 1e9) > f13 / (bf16_sus * 1e12)
-            else round(f13 / (w13_avg_ms * 1e-3) / 1e12, 1),
-            "peak": hbm if b13 / (hbm * 1e9) > f13 / (bf16_sus * 1e12) else bf16_burst,
-            "unit": "GB/s" if b13 / (hbm * 1e9) > f13 / (bf16_sus * 1e12) else "TFLOP/s",
+            "kernel": "grouped_gemm_kernel (w13 launch)",
+            "bound": bound,
+            "achieved": round(achieved_gb, 1) if bound == "hbm" else round(achieved_tf, 1),
+            "peak": hbm if bound == "hbm" else bf16_burst,
+            "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
             "frac": None,
             "traffic": traffic,
-            "peak_source": peak_src,
-            "algorithmic_bytes_per_launch": w13_alg_bytes,
-            "flops_per_launch": f13,
-            "avg_launch_ms": round(w13_avg_ms, 5),
-            "roofline_frac_of_max": None,
+            "peak_source": f"{peak_src} ({'HBM copy' if bound == 'hbm' else 'bf16 cuBLAS burst'})",
+            "algorithmic_bytes_per_launch": wl.b13 + wl.x13,
+            "flops_per_launch": wl.f13,
+            "avg_launch_ms": round(w13_ms, 5),
+            "roofline_frac_of_max": r13["frac_of_bound"],
         },
+        "kernels": {"w13": r13, "w2": head["w2"]},
+        "sustained": {"steps": n_sus, "ms_per_step": round(ms_sus, 5),
+                      "w13_ms": round(w13_sus, 5), "seconds": round(n_sus * ms_sus * 1e-3, 3)},
+        "workloads": subs,
         "e2e": {"value": round(whole_job_rate(flops, e2e_ms, world) / 1e12, 3), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "api": "moe_layer_forward with pinned host copies"},
-        "gpu_launches": launches_per_step * K,
+        "gpu_launches": Workload.LAUNCHES_PER_STEP * K,
         "clocks": clocks,
     }
     r = result["roofline"]
     r["frac"] = round(r["achieved"] / r["peak"], 4)
-    # Roofline fraction in the max(flop time, byte time) sense for the w13 launch.
-    t_roof = max(f13 / (bf16_burst * 1e12), b13 / (hbm * 1e9))
-    r["roofline_frac_of_max"] = round(t_roof / (w13_avg_ms * 1e-3), 4)
     return result, dict(workload=args.workload, rank=rank)
 
 
@@ -517,10 +607,18 @@ def run_oracle_steps(c, gs_s, xs, steps):
     return (f13 + f2), times, oracle.threads_used()
 
 
+CPU_BASELINE_BUDGET_S = 15.0
+
+
 def cpu_baseline(workload: str, seed: int):
+    """The oracle on the first n non-empty expert bands of the workload, n
+    chosen from a one-band calibration so the timed pass takes about
+    CPU_BASELINE_BUDGET_S."""
     from fp4_weight_grouped_gb300 import inputs
-    n_exp = 64
     c = inputs.layer_workload(workload, seed)
+    gs1, xs1 = oracle_sample(c, 1)
+    _, t1, _ = run_oracle_steps(c, gs1, xs1, 1)
+    n_exp = int(max(1, min(64, CPU_BASELINE_BUDGET_S // max(t1[0], 1e-6))))
     gs_s, xs = oracle_sample(c, n_exp)
     flops, times, threads = run_oracle_steps(c, gs_s, xs, 1)
     return {"value": round(flops / times[0] / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
@@ -585,21 +683,42 @@ def run_reference(args, rank, world):
     }
 
 
+def spawn_replicas(n: int) -> int:
+    """Re-run this command as n replica processes under torch.distributed.run
+    (one per GPU, rendezvous on 127.0.0.1) and return its exit status."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr=127.0.0.1", f"--master-port={port}", os.path.abspath(__file__),
+           *sys.argv[1:]]
+    return subprocess.call(cmd)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decode_T64")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="layer_T8192")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle leg")
+    ap.add_argument("--no-sub-workloads", action="store_true",
+                    help="time only --workload (skip the other shapes)")
     args = ap.parse_args()
     if args.steps is None:
         args.steps = DEFAULT_STEPS[args.workload]
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.gpus < 1:
+        ap.error("--gpus must be >= 1")
     rank, world, local = dist_env()
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(spawn_replicas(args.gpus))
+    if "WORLD_SIZE" in os.environ and world != args.gpus:
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE={world}")
 
     if args.impl == "reference":
         res = run_reference(args, rank, world)

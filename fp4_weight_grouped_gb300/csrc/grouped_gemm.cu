@@ -274,8 +274,11 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
     __syncthreads();
     // Row offsets and work-item offsets: exclusive prefix sums over experts,
     // done by warp 0 in chunks of 32 (E <= 1024); also the widest work item.
+    // The running sums are 64-bit and every prefix is checked against rows, so
+    // group sizes whose 32-bit sum would wrap around to rows are still caught.
     if (warp == 0) {
-        int run_rows = 0, run_items = 0, nt_max = 0;
+        long long run_rows = 0, run_items = 0;
+        int nt_max = 0;
         for (int base = 0; base < E; base += 32) {
             const int e = base + lane;
             int gs = 0;
@@ -284,31 +287,33 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
                 if (gs < 0) *bad_flag = 1;
             }
             const int g = gs > 0 ? gs : 0;
-            const int items = ((g + kMaxNT - 1) / kMaxNT) * p.n_tiles;
-            nt_max = max(nt_max, min(kMaxNT, (g + 15) & ~15));
-            int incl_r = g, incl_i = items;
+            const long long items = ((static_cast<long long>(g) + kMaxNT - 1) / kMaxNT) * p.n_tiles;
+            nt_max = max(nt_max, g >= kMaxNT ? kMaxNT : (g + 15) & ~15);
+            long long incl_r = g, incl_i = items;
 #pragma unroll
             for (int d = 1; d < 32; d <<= 1) {
-                const int a = __shfl_up_sync(0xffffffffu, incl_r, d);
-                const int b = __shfl_up_sync(0xffffffffu, incl_i, d);
+                const long long a = __shfl_up_sync(0xffffffffu, incl_r, d);
+                const long long b = __shfl_up_sync(0xffffffffu, incl_i, d);
                 if (lane >= d) {
                     incl_r += a;
                     incl_i += b;
                 }
             }
+            const long long end_r = run_rows + incl_r, end_i = run_items + incl_i;
             if (e < E) {
-                roff[e] = run_rows + incl_r - g;
-                ioff[e] = run_items + incl_i - items;
+                if (end_r > p.rows || end_i > INT32_MAX) *bad_flag = 1;
+                roff[e] = static_cast<int>(end_r - g);
+                ioff[e] = static_cast<int>(end_i - items);
             }
             run_rows += __shfl_sync(0xffffffffu, incl_r, 31);
             run_items += __shfl_sync(0xffffffffu, incl_i, 31);
         }
         nt_max = __reduce_max_sync(0xffffffffu, nt_max);
         if (lane == 0) {
-            roff[E] = run_rows;
-            ioff[E] = run_items;
+            if (run_rows != p.rows || run_items > INT32_MAX) *bad_flag = 1;
+            roff[E] = static_cast<int>(run_rows);
+            ioff[E] = static_cast<int>(run_items);
             *nt_max_slot = nt_max;
-            if (run_rows != p.rows) *bad_flag = 1;
         }
     }
     __syncthreads();

@@ -15,6 +15,7 @@
 //  3. scatter — one warp per slot: row = offset[e] + chunk base + rank; writes
 //               both maps and copies the token row (16-byte vectors).
 // Scratch (caller workspace): chunk totals [chunks, E] and ranks [rows].
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -115,7 +116,10 @@ scatter_kernel(const int32_t *ids, int rows, int k, int E, const int32_t *chunk_
     const int s = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (s >= rows) return;
     const int e = ids[s];
-    if (e < 0 || e >= E) return;           // recorded by the count kernel
+    if (e < 0 || e >= E) {                 // recorded by the count kernel
+        if (lane == 0) slot_to_row[s] = -1;   // no row: the combine skips this slot
+        return;
+    }
     const int row =
         offsets[e] + chunk_base[static_cast<size_t>(s / kChunk) * E + e] + rank[s];
     if (lane == 0) {
@@ -215,7 +219,27 @@ static __device__ __align__(256) uint8_t
 namespace {
 constexpr int kMaxDevices = 64;
 std::mutex noalloc_mutex;
-void *noalloc_base[kMaxDevices];   // device address of noalloc_area, per device
+// Device address of noalloc_area per device, with the context it was looked up
+// in: after a device reset the primary context (and the module holding the
+// array) is created anew, so the address is looked up again.
+void *noalloc_base[kMaxDevices];
+CUcontext noalloc_ctx[kMaxDevices];
+
+CUcontext current_context() {
+    using Fn = CUresult (*)(CUcontext *);
+    static const Fn fn = [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return static_cast<Fn>(nullptr);
+        return reinterpret_cast<Fn>(ptr);
+    }();
+    CUcontext ctx = nullptr;
+    if (!fn || fn(&ctx) != CUDA_SUCCESS) return nullptr;
+    return ctx;
+}
 }  // namespace
 
 moe_status launch_route_sort_noalloc(const int32_t *ids, int T, int k, int E,
@@ -229,12 +253,16 @@ moe_status launch_route_sort_noalloc(const int32_t *ids, int T, int k, int E,
     void *base = nullptr;
     {
         std::lock_guard<std::mutex> lock(noalloc_mutex);
-        if (!noalloc_base[dev]) {
-            // The device is current; the address is valid for this device only.
+        // A thread whose context is not yet current (null) or differs from the
+        // one of the lookup looks the address up again; the lookup itself makes
+        // the device's primary context current.
+        if (!noalloc_base[dev] || current_context() != noalloc_ctx[dev]) {
+            noalloc_base[dev] = nullptr;
             if (cudaGetSymbolAddress(&noalloc_base[dev], noalloc_area) != cudaSuccess) {
                 noalloc_base[dev] = nullptr;
                 return MOE_ERR_CUDA;
             }
+            noalloc_ctx[dev] = current_context();
         }
         base = noalloc_base[dev];
     }

@@ -99,11 +99,14 @@ template <bool OUT_BF16>
 __global__ void combine_vec4(const float *y, const int32_t *s2r, const float *w, int T, int k,
                              int N, void *out) {
     const int n4 = N / 4;
+    const int rows = T * k;
     for (int t = blockIdx.x; t < T; t += gridDim.x) {
         for (int c = threadIdx.x; c < n4; c += blockDim.x) {
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int j = 0; j < k; ++j) {
                 const int row = __ldg(s2r + static_cast<size_t>(t) * k + j);
+                // A slot whose id was out of range has no row (-1): it adds nothing.
+                if (static_cast<unsigned>(row) >= static_cast<unsigned>(rows)) continue;
                 const float wj = __ldg(w + static_cast<size_t>(t) * k + j);
                 const float4 v = __ldg(reinterpret_cast<const float4 *>(y + static_cast<size_t>(row) * N) + c);
                 acc.x = fmaf(wj, v.x, acc.x);
@@ -126,11 +129,13 @@ __global__ void combine_vec4(const float *y, const int32_t *s2r, const float *w,
 template <bool OUT_BF16>
 __global__ void combine_scalar(const float *y, const int32_t *s2r, const float *w, int T, int k,
                                int N, void *out) {
+    const int rows = T * k;
     for (int t = blockIdx.x; t < T; t += gridDim.x) {
         for (int n = threadIdx.x; n < N; n += blockDim.x) {
             float acc = 0.f;
             for (int j = 0; j < k; ++j) {
                 const int row = s2r[static_cast<size_t>(t) * k + j];
+                if (static_cast<unsigned>(row) >= static_cast<unsigned>(rows)) continue;
                 acc = fmaf(w[static_cast<size_t>(t) * k + j], y[static_cast<size_t>(row) * N + n], acc);
             }
             if (OUT_BF16) {

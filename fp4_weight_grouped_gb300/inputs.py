@@ -202,6 +202,33 @@ def router_weights_uniform(seed: int, T: int, k: int) -> np.ndarray:
     return (w / w.sum(axis=1, keepdims=True)).astype(np.float32)
 
 
+WORKLOAD_TOKENS = {"decode_T64": (64, "uniform"), "decode_T256": (256, "uniform"),
+                   "prefill_T4096": (4096, "zipf"), "layer_T8192": (8192, "logits")}
+
+
+def layer_weights(seed: int = 0, E: int = 256, hidden: int = 4096, inter: int = 2048):
+    """w13 (gate|up fused, N = 2*inter, K = hidden) and w2 (N = hidden, K =
+    inter) codes and scales; the same draws as layer_case/layer_workload with
+    the same seed."""
+    c13, s13 = mxfp4_weights(seed, _TAG_W13, E, 2 * inter, hidden)
+    c2, s2 = mxfp4_weights(seed, _TAG_W2, E, hidden, inter)
+    return dict(w13_codes=c13, w13_scales=s13, w2_codes=c2, w2_scales=s2)
+
+
+def workload_tokens(name: str, seed: int = 0, E: int = 256, k: int = 6, hidden: int = 4096) -> dict:
+    """Routing ids, router weights and token activations of a named full-path
+    workload (no weights): the draws layer_workload makes for the same name
+    and seed."""
+    T, routing = WORKLOAD_TOKENS[name]
+    if routing == "logits":
+        ids, w = route_logits(seed, T, E, k)
+    else:
+        ids = route_uniform(seed, T, E, k) if routing == "uniform" else route_zipf(seed, T, E, k)
+        w = router_weights_uniform(seed, T, k)
+    x = normal_bf16(seed, _TAG_X, (T, hidden))
+    return dict(ids=ids, topk_w=w, x=x, T=T, E=E, k=k, hidden=hidden)
+
+
 def layer_workload(name: str, seed: int = 0) -> dict:
     """Full-path inputs (route sort -> w13 -> SwiGLU -> w2 -> combine) for the
     named workload; the token count and routing follow the named config."""

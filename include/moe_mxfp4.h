@@ -113,7 +113,9 @@ MOE_API moe_status moe_read_status(const void *workspace, void *stream);
  *               x[sorted_slot[row] / k] (the activation permutation), x row-major.
  *  x_sorted_layout  order of the reduction dimension written to x_sorted.
  *  workspace    device, >= moe_workspace_bytes(T, k, E) bytes, 16-byte aligned.
- * Ids outside [0, E) set MOE_ERR_DATA; the outputs are then unspecified.
+ * Ids outside [0, E) set MOE_ERR_DATA.  Such a slot is left out of every
+ * band: slot_to_row holds -1 for it, group_offsets[E] < T*k, and the rows
+ * past group_offsets[E] of sorted_slot and x_sorted are not written.
  * Launches three kernels (count, scan, scatter+gather); no atomics on data.
  */
 MOE_API moe_status moe_route_sort(const int32_t *topk_ids, int32_t T, int32_t k, int32_t E,
@@ -152,7 +154,10 @@ MOE_API moe_status moe_route_sort(const int32_t *topk_ids, int32_t T, int32_t k,
  * First call: on each device, the first call looks up the device address of
  * the array (cudaGetSymbolAddress, with that device current) and sets a kernel
  * attribute; the lookup may make the driver load the library's device code.
- * Make one call on every device before any stream capture begins.
+ * Make one call on every device before any stream capture begins.  The address
+ * is kept with the CUDA context it was looked up in; when the calling thread's
+ * current context differs (another thread before its first CUDA call, or a new
+ * primary context after cudaDeviceReset), the call looks the address up again.
  *
  * Overlap: every call on a device shares the one array.  Two calls whose kernels
  * can run at the same time (streams with no ordering between them, or host
@@ -196,8 +201,12 @@ MOE_API moe_status moe_route_sort_noalloc(const int32_t *topk_ids, int32_t T, in
  *  E            1..1024 experts.  N >= 1 output columns.
  *  out          device [rows, N], f32 (4-byte aligned) or bf16 (RNE).
  *  workspace    device, >= 256 bytes (status word).
- * Products of bf16 activations and the exactly decoded bf16 weights are exact
- * in f32; results differ from an exact sum only by f32 accumulation order.
+ * Every weight is decoded exactly to bf16.  With scale bytes >= 2 every
+ * nonzero weight is a normal bf16 number, its products with bf16 activations
+ * are exact in f32, and results differ from an exact sum only by f32
+ * accumulation order.  Scale bytes 0 and 1 make the smallest weights bf16
+ * subnormals (below 2^-126), which the tensor core may read as zero; for
+ * those blocks only the accumulation bound, not exactness, is claimed.
  * Empty experts launch no work and their weights are never read.
  */
 MOE_API moe_status moe_mxfp4_grouped_gemm(const uint16_t *act, moe_act_layout act_layout,
@@ -261,7 +270,9 @@ MOE_API moe_status moe_swiglu(const void *gu, moe_dtype in_dtype, int64_t rows, 
  * bitwise reproducible run to run.
  *
  *  y            device f32 [T*k, N], 16-byte aligned.
- *  slot_to_row  device int32 [T*k] (from moe_route_sort).
+ *  slot_to_row  device int32 [T*k] (from moe_route_sort).  An entry outside
+ *               [0, T*k) (moe_route_sort writes -1 for an id out of range)
+ *               adds nothing: y is never read outside its T*k rows.
  *  topk_w       device f32 [T, k].
  *  out          device [T, N], f32 or bf16.
  */

@@ -403,6 +403,33 @@ def test_combine_matches_oracle_and_repeats(B, T, k, N):
                                       .cpu().numpy(), y[s2r])
 
 
+def test_bad_id_leaves_slot_out_and_combine_skips_it(B):
+    # An id out of range: MOE_ERR_DATA, slot_to_row = -1 for that slot, and the
+    # combine adds nothing for it (it never reads y outside its T*k rows).
+    T, k, E, N = 40, 3, 8, 64
+    ids = inputs.route_uniform(21, T, E, k)
+    bad = 7 * k + 1
+    ids.reshape(-1)[bad] = E + 5
+    ws = B.make_workspace(T, k, E, DEV)
+    gs, off, ss, s2r, _ = B.route_sort(B.to_device(ids, DEV), E, workspace=ws)
+    assert B.read_status(ws) == B.MOE_ERR_DATA
+    s2r_h = s2r.cpu().numpy()
+    assert s2r_h[bad] == -1
+    assert int(off[E]) == T * k - 1
+    good = np.delete(np.arange(T * k), bad)
+    assert sorted(s2r_h[good].tolist()) == list(range(T * k - 1))
+    rng = np.random.default_rng(3)
+    y = rng.standard_normal((T * k, N)).astype(np.float32)
+    w = rng.random((T, k)).astype(np.float32)
+    out = B.combine(B.to_device(y, DEV), s2r, B.to_device(w, DEV)).cpu().numpy()
+    # Reference: the same sum with the bad slot's weight set to zero.
+    s2r_ref, w_ref = s2r_h.copy(), w.copy()
+    s2r_ref[bad] = 0
+    w_ref.reshape(-1)[bad] = 0.0
+    ref, mag = oracle.combine(y.astype(np.float64), s2r_ref, w_ref)
+    _tol_check(out, ref, mag, rel=1e-6, what="combine with a skipped slot")
+
+
 # --------------------------------------------------------------------- layer
 
 def test_layer_forward_stagewise(B):

@@ -132,8 +132,8 @@ def test_gemm_rejects_bad_arguments_on_host(lib):
     assert call(codes=P(4104)) == INVALID
     assert call(dt=7) == INVALID
     assert call(lay=2) == INVALID
-    # Valid arguments get past the host checks; without a GPU the device query fails.
-    assert call() in (2, 3)
+    # No call here gets past the host checks: the pointers are not device memory,
+    # so a call with valid arguments would reach a kernel launch on a GPU machine.
 
 
 def test_route_sort_rejects_bad_arguments_on_host(lib):

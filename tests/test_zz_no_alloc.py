@@ -32,9 +32,10 @@ def test_capacity_is_checked_on_the_host():
     f.argtypes = [P, I32, I32, I32, P, P, P, P, P, I32, P, C.c_int, P]
     f.restype = C.c_int
     fake = P(4096)
-    # 17408 * 6 = 104448 slots at E = 256: 522240 bytes of scratch, fits.
+    # 17408 * 6 = 104448 slots at E = 256: 522240 bytes of scratch, fits (the
+    # GPU test below runs it; here only calls rejected on the host are made,
+    # because the pointers are not device memory).
     assert _scratch_bytes(17408, 6, 256) <= SCRATCH_MAX
-    assert f(fake, 17408, 6, 256, fake, fake, fake, fake, None, 0, None, 0, None) in (2, 3)
     # One more 1024-slot chunk does not.
     assert _scratch_bytes(17408 + 171, 6, 256) > SCRATCH_MAX
     assert f(fake, 17408 + 171, 6, 256, fake, fake, fake, fake, None, 0, None, 0, None) == 6
