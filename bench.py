@@ -2,8 +2,8 @@
 """Benchmark of the MXFP4 grouped MoE hot path on GB300.
 
 One step = one pass of the whole routed-expert path over one batch:
-route sort (+ activation gather) -> w13 grouped GEMM -> SwiGLU -> w2 grouped GEMM
--> combine, all launched through the C ABI on one CUDA stream.
+route sort (+ activation gather) -> w13 grouped GEMM with SwiGLU in its epilogue
+-> w2 grouped GEMM -> combine, all launched through the C ABI on one CUDA stream.
 
 Default workload (N=1): the full MoE layer, T = 8192 tokens, 256 experts, top-6
 (49152 sorted rows), w13 K = N = 4096, w2 K = 2048, N = 4096: the largest
@@ -46,11 +46,13 @@ WORKLOADS = {
                      "experts unused; full path",
     "layer_T8192": "Full MoE layer: T=8192 tokens (49152 rows), top-6 of N(0,1) logits, softmax "
                    "router weights; full path",
+    "layer_E64_T2048": "Profiling shape: the full layer path with the layer's band size (about 192 "
+                       "rows per expert) on 64 experts, T=2048 tokens (12288 rows); fits an ncu capture",
     "cast_w13": "Lossless MXFP4 -> NVFP4 scale cast of the w13 scales: E8M0 [256, 4096, 128] "
                 "(128 MiB) -> E4M3 [256, 4096, 256] + per-expert f32 scale + out-of-range count",
 }
 DEFAULT_STEPS = {"decode_T64": 2000, "decode_T256": 1000, "prefill_T4096": 300, "layer_T8192": 300,
-                 "cast_w13": 200}
+                 "layer_E64_T2048": 300, "cast_w13": 200}
 CAST_METRIC = "lossless MXFP4 -> NVFP4 scale cast GB/s (algorithmic bytes), % of measured HBM, 1 GPU"
 CAST_SHAPE, CAST_BYTES = (256, 4096, 128), (117, 125)   # w13 scale tensor, exponents [-10, -2]
 
@@ -212,8 +214,9 @@ class Workload:
         self.bufs = B.LayerBuffers(self.T, self.k, self.E, self.H, self.I, dev)
 
     def step(self, ev=None):
-        """route sort (+ gather) -> w13 -> SwiGLU -> w2 -> combine.  ev: four
-        events recorded around the two grouped-GEMM launches."""
+        """route sort (+ gather) -> w13 with SwiGLU in its epilogue -> w2 ->
+        combine.  ev: three events recorded around the two grouped-GEMM
+        launches."""
         B, b, w = self.B, self.bufs, self.wts
         K8 = B.MOE_ACT_K8_INTERLEAVED     # the layer path keeps activations in the GEMM's k order
         stream = self.stream
@@ -222,20 +225,17 @@ class Workload:
                                                b.slot_to_row, b.x_sorted), x_layout=K8)
         if ev is not None:
             ev[0].record(stream)
-        B.grouped_gemm(xs, w["w13_codes"], w["w13_scales"], gsz, out=b.y13, workspace=b.workspace,
-                       act_layout=K8)
+        B.grouped_gemm_swiglu(xs, w["w13_codes"], w["w13_scales"], gsz, out=b.h,
+                              workspace=b.workspace, act_layout=K8, h_layout=K8)
         if ev is not None:
             ev[1].record(stream)
-        B.swiglu(b.y13, out=b.h, layout=K8)
-        if ev is not None:
-            ev[2].record(stream)
         B.grouped_gemm(b.h, w["w2_codes"], w["w2_scales"], gsz, out=b.y2, workspace=b.workspace,
                        act_layout=K8)
         if ev is not None:
-            ev[3].record(stream)
+            ev[2].record(stream)
         B.combine(b.y2, s2r, self.w, out=b.out)
 
-    LAUNCHES_PER_STEP = 7     # count, scan, scatter, w13, SwiGLU, w2, combine
+    LAUNCHES_PER_STEP = 6     # count, scan, scatter, w13 + SwiGLU, w2, combine
 
     def warm(self, n):
         import torch
@@ -249,14 +249,15 @@ class Workload:
         gs = self.bufs.group_sizes.cpu().numpy()
         self.f13, self.b13, self.touched, self.rows = gemm_work(gs, self.H, 2 * self.I)
         self.f2, self.b2, _, _ = gemm_work(gs, self.I, self.H)
-        # activation and output bytes of each launch (read act, write f32 out)
-        self.x13 = self.rows * self.H * 2 + self.rows * 2 * self.I * 4
+        # activation and output bytes of each launch: w13 reads x_sorted and
+        # writes bf16 h; w2 reads h and writes f32 y2
+        self.x13 = self.rows * self.H * 2 + self.rows * self.I * 2
         self.x2 = self.rows * self.I * 2 + self.rows * self.H * 4
 
     def timed(self, steps):
         """Exactly `steps` steps between two events; per-step GEMM launch events."""
         import torch
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize(self.dev)
         t0.record(self.stream)
@@ -269,7 +270,7 @@ class Workload:
             raise RuntimeError(f"{self.name}: device status after timing: {self.B.status_string(st)}")
         ms = t0.elapsed_time(t1) / steps
         w13 = statistics.fmean(e[0].elapsed_time(e[1]) for e in ev)
-        w2 = statistics.fmean(e[2].elapsed_time(e[3]) for e in ev)
+        w2 = statistics.fmean(e[1].elapsed_time(e[2]) for e in ev)
         return ms, w13, w2
 
     def summary(self, ms, w13, w2, hbm, bf16):
@@ -300,11 +301,13 @@ def run_ours(args, rank, world, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     hbm, bf16_burst, bf16_sus, peak_src = load_peaks()
-    wts = {k: B.to_device(v, dev) for k, v in inputs.layer_weights(args.seed + rank).items()}
+    E_head = inputs.WORKLOAD_TOKENS[args.workload][2]
+    wts = {k: B.to_device(v, dev) for k, v in inputs.layer_weights(args.seed + rank, E=E_head).items()}
 
-    # ---- the other workloads first (each its own warm-up and timed steps)
+    # ---- the other workloads first (each its own warm-up and timed steps; they
+    # share the 256-expert weights)
     subs = {}
-    if not args.no_sub_workloads:
+    if not args.no_sub_workloads and E_head == 256:
         for name in SUB_WORKLOADS:
             if name == args.workload:
                 continue
@@ -405,7 +408,7 @@ def run_ours(args, rank, world, local):
         "gemm_flops_per_step": flops,
         "weight_bytes_per_step": wl.b13 + wl.b2,
         "roofline": {
-            "kernel": "grouped_gemm_kernel (w13 launch)",
+            "kernel": "grouped_gemm_kernel (w13 launch with SwiGLU epilogue)",
             "bound": bound,
             "achieved": round(achieved_gb, 1) if bound == "hbm" else round(achieved_tf, 1),
             "peak": hbm if bound == "hbm" else bf16_burst,

@@ -24,7 +24,7 @@ SYMBOLS = (
     "moe_route_sort", "moe_mxfp4_grouped_gemm", "moe_swiglu", "moe_combine", "moe_layer_forward",
     "moe_mxfp4_decode_expert", "moe_debug_bounded_wait", "moe_last_launch_count",
     "moe_route_sort_noalloc", "moe_nvfp4_cast_workspace_bytes", "moe_mxfp4_to_nvfp4",
-    "moe_nvfp4_grouped_gemm",
+    "moe_nvfp4_grouped_gemm", "moe_mxfp4_grouped_gemm_swiglu",
 )
 
 _lock = threading.Lock()
@@ -61,10 +61,12 @@ def load(path: str | None = None):
                                            C.c_int),
                 "moe_mxfp4_grouped_gemm": ([P, C.c_int, I64, I32, P, P, P, I32, I32, P, C.c_int, P, SZ,
                                             P], C.c_int),
+                "moe_mxfp4_grouped_gemm_swiglu": ([P, C.c_int, I64, I32, P, P, P, I32, I32, P,
+                                                   C.c_int, P, SZ, P], C.c_int),
                 "moe_swiglu": ([P, C.c_int, I64, I32, P, C.c_int, P], C.c_int),
                 "moe_combine": ([P, P, P, I32, I32, I32, P, C.c_int, P], C.c_int),
                 "moe_layer_forward": ([P, P, P, I32, I32, I32, I32, I32, P, P, P, P, P,
-                                       P, P, P, P, P, P, P, P, P, SZ, P], C.c_int),
+                                       P, P, P, P, P, P, P, P, SZ, P], C.c_int),
                 "moe_mxfp4_decode_expert": ([P, P, I32, I32, I32, I32, P, P, SZ, P], C.c_int),
                 "moe_debug_bounded_wait": ([U64, P, SZ, P], C.c_int),
                 "moe_last_launch_count": ([], I32),
@@ -199,6 +201,28 @@ def grouped_gemm(act: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor,
     return out
 
 
+def grouped_gemm_swiglu(act: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor,
+                        group_sizes: torch.Tensor, out: torch.Tensor | None = None,
+                        workspace: torch.Tensor | None = None, stream=None,
+                        act_layout: int = MOE_ACT_ROW_MAJOR, h_layout: int = MOE_ACT_ROW_MAJOR):
+    """w13 grouped GEMM with SwiGLU in its epilogue.  act bf16 [rows, K]; codes
+    uint8 [E, 2I, K/2] and scales uint8 [E, 2I, K/32] with gate rows [0, I) and
+    up rows [I, 2I); group_sizes int32 [E] -> h bf16 [rows, I] in `h_layout`."""
+    rows, K = act.shape
+    E, two_i, _ = codes.shape
+    I = two_i // 2
+    if out is None:
+        out = torch.empty((rows, I), dtype=torch.bfloat16, device=act.device)
+    if workspace is None:
+        workspace = make_workspace(0, 1, 1, act.device, stream)
+    rc = load().moe_mxfp4_grouped_gemm_swiglu(_ptr(act), act_layout, rows, K, _ptr(codes),
+                                              _ptr(scales), _ptr(group_sizes), E, I, _ptr(out),
+                                              h_layout, _ptr(workspace), workspace.numel(),
+                                              _stream(stream))
+    _check(rc, "moe_mxfp4_grouped_gemm_swiglu")
+    return out
+
+
 def nvfp4_grouped_gemm(act: torch.Tensor, codes: torch.Tensor, scales16: torch.Tensor,
                        weight_scale_2: torch.Tensor, group_sizes: torch.Tensor,
                        out: torch.Tensor | None = None, out_dtype=torch.float32,
@@ -255,7 +279,6 @@ class LayerBuffers:
         self.sorted_slot = torch.empty(rows, **i32)
         self.slot_to_row = torch.empty(rows, **i32)
         self.x_sorted = torch.empty((rows, hidden), dtype=torch.bfloat16, device=device)
-        self.y13 = torch.empty((rows, 2 * inter), dtype=torch.float32, device=device)
         self.h = torch.empty((rows, inter), dtype=torch.bfloat16, device=device)
         self.y2 = torch.empty((rows, hidden), dtype=torch.float32, device=device)
         self.out = torch.empty((T, hidden), dtype=torch.float32, device=device)
@@ -272,7 +295,7 @@ def layer_forward(x, topk_ids, topk_w, w13_codes, w13_scales, w2_codes, w2_scale
         _ptr(x), _ptr(topk_ids), _ptr(topk_w), T, k, E, hidden, inter,
         _ptr(w13_codes), _ptr(w13_scales), _ptr(w2_codes), _ptr(w2_scales), _ptr(b.out),
         _ptr(b.group_sizes), _ptr(b.group_offsets), _ptr(b.sorted_slot), _ptr(b.slot_to_row),
-        _ptr(b.x_sorted), _ptr(b.y13), _ptr(b.h), _ptr(b.y2), _ptr(b.workspace),
+        _ptr(b.x_sorted), _ptr(b.h), _ptr(b.y2), _ptr(b.workspace),
         b.workspace.numel(), _stream(stream))
     _check(rc, "moe_layer_forward")
     return b.out

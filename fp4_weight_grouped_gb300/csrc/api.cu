@@ -190,6 +190,29 @@ moe_status moe_mxfp4_grouped_gemm(const uint16_t *act, moe_act_layout act_layout
     return st;
 }
 
+moe_status moe_mxfp4_grouped_gemm_swiglu(const uint16_t *act, moe_act_layout act_layout,
+                                         int64_t rows, int32_t K, const uint8_t *codes,
+                                         const uint8_t *scales, const int32_t *group_sizes,
+                                         int32_t E, int32_t I, uint16_t *h,
+                                         moe_act_layout h_layout, void *workspace,
+                                         size_t workspace_bytes, void *stream) {
+    if (I <= 0 || I % 16 != 0 || static_cast<int64_t>(I) * 2 > INT32_MAX) return MOE_ERR_INVALID_ARG;
+    moe_status st = check_gemm_args(act, act_layout, rows, K, codes, scales, group_sizes, E, 2 * I,
+                                    h, MOE_BF16, workspace, workspace_bytes);
+    if (st != MOE_OK) return st;
+    if (h_layout != MOE_ACT_ROW_MAJOR && (h_layout != MOE_ACT_K8_INTERLEAVED || I % 8 != 0))
+        return MOE_ERR_INVALID_ARG;
+    int sms = 0;
+    if ((st = current_device(&sms)) != MOE_OK) return st;
+    st = moe::launch_grouped_gemm_swiglu(act, static_cast<int>(rows), K, codes, scales, group_sizes,
+                                         E, 2 * I, h, act_layout == MOE_ACT_K8_INTERLEAVED,
+                                         h_layout == MOE_ACT_K8_INTERLEAVED,
+                                         status_word(workspace), kWaitLimitNs,
+                                         static_cast<cudaStream_t>(stream), sms);
+    g_last_launches = rows > 0 ? 1 : 0;
+    return st;
+}
+
 moe_status moe_nvfp4_grouped_gemm(const uint16_t *act, moe_act_layout act_layout, int64_t rows,
                                   int32_t K, const uint8_t *codes, const uint8_t *scales16,
                                   const float *weight_scale_2, const int32_t *group_sizes,
@@ -249,24 +272,24 @@ moe_status moe_layer_forward(const uint16_t *x, const int32_t *topk_ids, const f
                              const uint8_t *w13_codes, const uint8_t *w13_scales,
                              const uint8_t *w2_codes, const uint8_t *w2_scales, float *out,
                              int32_t *group_sizes, int32_t *group_offsets, int32_t *sorted_slot,
-                             int32_t *slot_to_row, uint16_t *x_sorted, float *y13, uint16_t *h,
-                             float *y2, void *workspace, size_t workspace_bytes, void *stream) {
+                             int32_t *slot_to_row, uint16_t *x_sorted, uint16_t *h, float *y2,
+                             void *workspace, size_t workspace_bytes, void *stream) {
     if (hidden <= 0 || inter <= 0 || hidden % 32 || inter % 32) return MOE_ERR_INVALID_ARG;
-    if (T > 0 && (!x || !out || !x_sorted || !y13 || !h || !y2 || !topk_w))
-        return MOE_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(inter) * 2 > INT32_MAX) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!x || !out || !x_sorted || !h || !y2 || !topk_w)) return MOE_ERR_INVALID_ARG;
     const int64_t rows = static_cast<int64_t>(T) * k;
     moe_status st = check_route_args(topk_ids, T, k, E, group_sizes, group_offsets, sorted_slot,
                                      slot_to_row, x, hidden, x_sorted, MOE_ACT_K8_INTERLEAVED,
                                      workspace, workspace_bytes);
     if (st != MOE_OK) return st;
     if ((st = check_gemm_args(x_sorted, MOE_ACT_K8_INTERLEAVED, rows, hidden, w13_codes,
-                              w13_scales, group_sizes, E, 2 * inter, y13, MOE_F32, workspace,
+                              w13_scales, group_sizes, E, 2 * inter, h, MOE_BF16, workspace,
                               workspace_bytes)) != MOE_OK ||
         (st = check_gemm_args(h, MOE_ACT_K8_INTERLEAVED, rows, inter, w2_codes, w2_scales,
                               group_sizes, E, hidden, y2, MOE_F32, workspace, workspace_bytes)) !=
             MOE_OK)
         return st;
-    if (T > 0 && (!aligned(y13, 16) || !aligned(h, 16) || !aligned(y2, 16) || !aligned(out, 16)))
+    if (T > 0 && (!aligned(h, 16) || !aligned(y2, 16) || !aligned(out, 16)))
         return MOE_ERR_INVALID_ARG;
     int sms = 0;
     if ((st = current_device(&sms)) != MOE_OK) return st;
@@ -277,14 +300,10 @@ moe_status moe_layer_forward(const uint16_t *x, const int32_t *topk_ids, const f
                                 slot_to_row, x, hidden, x_sorted, 1,
                                 static_cast<uint8_t *>(workspace) + kStatusBytes, status, s, &n);
     launches += n;
-    if (st == MOE_OK && rows > 0) {
-        st = moe::launch_grouped_gemm(x_sorted, static_cast<int>(rows), hidden, w13_codes,
-                                      w13_scales, group_sizes, E, 2 * inter, y13, 0, 1, status,
-                                      kWaitLimitNs, s, sms);
-        ++launches;
-    }
-    if (st == MOE_OK && rows > 0) {
-        st = moe::launch_swiglu(y13, 0, rows, inter, h, 1, s, sms);
+    if (st == MOE_OK && rows > 0) {   // w13 with SwiGLU in its epilogue: h, never y13
+        st = moe::launch_grouped_gemm_swiglu(x_sorted, static_cast<int>(rows), hidden, w13_codes,
+                                             w13_scales, group_sizes, E, 2 * inter, h, 1, 1,
+                                             status, kWaitLimitNs, s, sms);
         ++launches;
     }
     if (st == MOE_OK && rows > 0) {

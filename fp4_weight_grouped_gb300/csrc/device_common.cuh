@@ -168,6 +168,18 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// 5-D tiled load of one box into shared memory (x innermost, then d1 .. d4).
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map, int32_t x,
+                                            int32_t d1, int32_t d2, int32_t d3, int32_t d4,
+                                            uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(d1), "r"(d2), "r"(d3), "r"(d4),
+        "r"(smem_u32(bar))
+        : "memory");
+}
+
 // -------------------------------------------------------------------- tcgen05
 
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {

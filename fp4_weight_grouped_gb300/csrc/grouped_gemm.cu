@@ -58,6 +58,10 @@ namespace gemm {
 
 constexpr int kIssuerWarps = 2;               // warps 0..1: MMA issuers (one elected lane each)
 constexpr int kSingleIssuers = 2;             // single mode: issuers splitting the token columns
+#ifndef MOE_WIDE_ISSUERS
+#define MOE_WIDE_ISSUERS 2
+#endif
+constexpr int kWideIssuers = MOE_WIDE_ISSUERS;   // wide mode: issuers splitting the token columns
 constexpr int kConvWG = 4;                    // converter warpgroups: warps 2..17
 constexpr int kConvWarp0 = kIssuerWarps;
 constexpr int kActWarp = kConvWarp0 + 4 * kConvWG;    // warp 18: activation producer
@@ -65,6 +69,11 @@ constexpr int kCodeWarp = kActWarp + 1;               // warp 19: code producer
 constexpr int kThreads = 32 * (kCodeWarp + 1);        // 640
 constexpr int kBN = 128;                      // output columns per tile (MMA M)
 constexpr int kMaxNT = 128;                   // tokens per work item (MMA N)
+constexpr int kWideNT = 256;                  // wide mode: tokens per work item
+#ifndef MOE_WIDE_ACT_SLOTS
+#define MOE_WIDE_ACT_SLOTS 4
+#endif
+constexpr int kWideActSlots = MOE_WIDE_ACT_SLOTS;   // wide mode: activation slots (32 KB each)
 constexpr int kStageK = 64;                   // K per decode / MMA stage
 constexpr int kSlots = 8;                     // A slots in TMEM (+ activation slots in smem)
 constexpr int kSlotsMax = 12;                 // bands <= 16 rows: three A slots per warpgroup
@@ -85,7 +94,7 @@ constexpr int kOffCode = 0;
 constexpr int kOffRowOff = kOffCode + kRingBytes;
 constexpr int kOffItemOff = kOffRowOff + (kMaxE + 1) * 4;
 constexpr int kOffBars = (kOffItemOff + (kMaxE + 1) * 4 + 7) & ~7;
-constexpr int kNumBars = 2 * kCodeStagesMax + 3 * kSlotsMax + 2 * 2 + kIssuerWarps;
+constexpr int kNumBars = 2 * kCodeStagesMax + 4 * kSlotsMax + 2 * 2 + kIssuerWarps;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
 constexpr int kOffItems = (kOffMisc + 64 + 15) & ~15;     // int4 per cached work item (16-aligned)
 constexpr int kSmemBytes = kOffItems + kItemCache * 16 + 1024;   // + alignment slack
@@ -121,6 +130,15 @@ struct Params {
     int scale_tma;     // K % 512 == 0, 16-byte aligned scales: scale tiles ride in the ring
     int act_k8;        // activations already in the K8-interleaved order
     int act3d;         // K % 256 == 0: one 3-D box fetches a band's 256-k activation tile
+    // Fused SwiGLU (w13 with N = 2 * I rows, gate rows [0, I), up rows [I, 2I)):
+    // a tile holds 64 gate rows and the 64 matching up rows, interleaved in
+    // groups of 16 (tile row 32q + i: gate row n0 + 16q + i; 32q + 16 + i: up
+    // row I + n0 + 16q + i), and the epilogue writes h = silu(g) * u as bf16
+    // [rows, I] (K8-interleaved when h_k8).  n_tiles = ceil(I / 64) then.
+    int swiglu;
+    int I;
+    int h_k8;
+    int allow_wide;    // K8 activations: bands over 128 rows take 256-token items
     uint64_t wait_limit_ns;
 };
 
@@ -128,9 +146,12 @@ struct Item {
     int e, row0, nvalid, nt, n0;
 };
 
-// Work item j -> (expert, token chunk, column tile); ioff/roff in shared memory.
+// Work item j -> (expert, token chunk, column tile); ioff/roff in shared
+// memory.  chunk: tokens per item (128, or 256 in wide mode).  n0 is the
+// first output column of the tile: weight row n0 (plain) or h column n0 (fused
+// SwiGLU, 64 columns a tile).
 __device__ __forceinline__ Item decode_item(int j, const int *roff, const int *ioff, int E,
-                                            int n_tiles) {
+                                            int n_tiles, int chunk, int tile_cols) {
     int lo = 0, hi = E - 1;   // last e with ioff[e] <= j (its band is non-empty)
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -139,14 +160,36 @@ __device__ __forceinline__ Item decode_item(int j, const int *roff, const int *i
     Item it;
     it.e = lo;
     const int r = j - ioff[lo];
-    const int chunk = r / n_tiles;
-    it.n0 = (r - chunk * n_tiles) * kBN;
-    const int t0 = chunk * kMaxNT;
+    const int ch = r / n_tiles;
+    it.n0 = (r - ch * n_tiles) * tile_cols;
+    const int t0 = ch * chunk;
     const int rem = roff[lo + 1] - roff[lo] - t0;
-    it.nvalid = rem < kMaxNT ? rem : kMaxNT;
+    it.nvalid = rem < chunk ? rem : chunk;
     it.nt = (it.nvalid + 15) & ~15;
     it.row0 = roff[lo] + t0;
     return it;
+}
+
+// Fused SwiGLU tile layout: tile row (TMEM lane) -> offset of its weight row
+// from n0 (up rows carry + I), and whether it is an up row.
+__device__ __forceinline__ int swiglu_row_offset(int row) {
+    return 16 * (row >> 5) + (row & 15);
+}
+__device__ __forceinline__ bool swiglu_row_is_up(int row) { return (row & 16) != 0; }
+
+// silu(g) = g / (1 + e^-g); for g < 0 the algebraically equal g*e^g / (1 + e^g)
+// avoids overflow of e^-g.  The same expression as the standalone SwiGLU
+// kernel, so the fused epilogue rounds to the same bf16 values.
+__device__ __forceinline__ float silu_f32(float g) {
+    if (g >= 0.f) return g / (1.f + expf(-g));
+    const float t = expf(g);
+    return g * t / (1.f + t);
+}
+
+// Column j of h in the K8-interleaved order: within each 8, element e is
+// stored at position 2e (e < 4) or 2(e - 4) + 1.
+__device__ __forceinline__ int k8_position(int j) {
+    return (j & ~7) | ((j & 3) << 1) | ((j >> 2) & 1);
 }
 
 // Position in a ring of `n` mbarrier-guarded slots: slot index and the parity
@@ -162,14 +205,18 @@ struct Ring {
 };
 
 // Epilogue of one work item for converter warpgroup `wg`: the warpgroup writes
-// its quarter of the item's token columns.  In split mode the four K-partials
-// are added in warpgroup order (deterministic); f32 or bf16 output.
+// its quarter of the item's token columns.  In split mode the two K-partials
+// are added in a fixed order (deterministic); f32 or bf16 output.  Fused
+// SwiGLU: lanes l and l ^ 16 of a warp hold the gate and up sums of the same
+// output column, so one shuffle pairs them; lanes 0-15 finish token c, lanes
+// 16-31 token c + 1, and h is written as bf16.
 template <bool kNv>
 __device__ __forceinline__ void store_item(const Params &p, const Item &it, uint32_t acc_base,
                                            int wg, int row, bool split, uint32_t part_cols,
                                            float tensor_scale) {
-    const int n = it.n0 + row;
     const int qc = it.nt >> 2;                 // columns per warpgroup (multiple of 4)
+    const bool up_lane = swiglu_row_is_up(row);
+    const int n = p.swiglu ? it.n0 + swiglu_row_offset(row) : it.n0 + row;
     for (int c = wg * qc; c < (wg + 1) * qc; c += 4) {
         uint32_t v[4];
         __syncwarp();
@@ -184,20 +231,39 @@ __device__ __forceinline__ void store_item(const Params &p, const Item &it, uint
         } else {
             tmem_ld_wait();
         }
-        if (n < p.N) {
+        float f[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            f[t] = __uint_as_float(v[t]);
+            // NVFP4: the decoded weights carry 2^-9 / weight_scale_2 (exact
+            // power-of-two scaling); one rounding restores the scale.
+            if constexpr (kNv) f[t] = (f[t] * 512.0f) * tensor_scale;
+        }
+        if (p.swiglu) {
+#pragma unroll
+            for (int pr = 0; pr < 2; ++pr) {
+                const float a0 = f[2 * pr], a1 = f[2 * pr + 1];
+                const float recv = __shfl_xor_sync(0xffffffffu, up_lane ? a0 : a1, 16);
+                const float g = up_lane ? recv : a0;
+                const float u = up_lane ? a1 : recv;
+                const int tok = c + 2 * pr + (up_lane ? 1 : 0);
+                if (n < p.I && tok < it.nvalid) {
+                    const int col = p.h_k8 ? k8_position(n) : n;
+                    const size_t off = static_cast<size_t>(it.row0 + tok) * p.I + col;
+                    reinterpret_cast<__nv_bfloat16 *>(p.out)[off] =
+                        __float2bfloat16_rn(silu_f32(g) * u);
+                }
+            }
+        } else if (n < p.N) {
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
                 const int tok = c + t;
                 if (tok < it.nvalid) {
                     const size_t off = static_cast<size_t>(it.row0 + tok) * p.N + n;
-                    float val = __uint_as_float(v[t]);
-                    // NVFP4: the decoded weights carry 2^-9 / weight_scale_2 (exact
-                    // power-of-two scaling); one rounding restores the scale.
-                    if constexpr (kNv) val = (val * 512.0f) * tensor_scale;
                     if (p.out_bf16)
-                        reinterpret_cast<__nv_bfloat16 *>(p.out)[off] = __float2bfloat16_rn(val);
+                        reinterpret_cast<__nv_bfloat16 *>(p.out)[off] = __float2bfloat16_rn(f[t]);
                     else
-                        reinterpret_cast<float *>(p.out)[off] = val;
+                        reinterpret_cast<float *>(p.out)[off] = f[t];
                 }
             }
         }
@@ -252,13 +318,15 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
     uint64_t *a_full = code_empty + kCodeStagesMax;      // converters -> issuer (4 warps)
     uint64_t *act_full = a_full + kSlotsMax;             // TMA -> issuer (single mode)
     uint64_t *slot_empty = act_full + kSlotsMax;         // MMA commit -> converters, act producer
-    uint64_t *acc_full = slot_empty + kSlotsMax;         // MMA commits -> epilogue
+    uint64_t *act_empty = slot_empty + kSlotsMax;        // wide mode: MMA commit -> act producer
+    uint64_t *acc_full = act_empty + kSlotsMax;          // MMA commits -> epilogue
     uint64_t *acc_empty = acc_full + 2;                  // epilogue (16 warps) -> issuers
     uint64_t *final_bar = acc_empty + 2;                 // one per issuer thread
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 8);
     int *bad_flag = reinterpret_cast<int *>(smem + kOffMisc + 16);
     int *nt_max_slot = reinterpret_cast<int *>(smem + kOffMisc + 24);
+    int *chunk_slot = reinterpret_cast<int *>(smem + kOffMisc + 32);
     int4 *item_cache = reinterpret_cast<int4 *>(smem + kOffItems);
 
     const int tid = threadIdx.x;
@@ -276,19 +344,26 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
     // done by warp 0 in chunks of 32 (E <= 1024); also the widest work item.
     // The running sums are 64-bit and every prefix is checked against rows, so
     // group sizes whose 32-bit sum would wrap around to rows are still caught.
+    // A first pass finds the largest band: with one over 128 rows (and K8
+    // activations) every work item takes up to 256 tokens (wide mode).
     if (warp == 0) {
+        int g_max = 0;
+        for (int base = 0; base < E; base += 32) {
+            const int e = base + lane;
+            const int gs = e < E ? p.group_sizes[e] : 0;
+            if (gs < 0) *bad_flag = 1;
+            g_max = max(g_max, gs);
+        }
+        g_max = __reduce_max_sync(0xffffffffu, g_max);
+        const int chunk = (p.allow_wide && g_max > kMaxNT) ? kWideNT : kMaxNT;
         long long run_rows = 0, run_items = 0;
         int nt_max = 0;
         for (int base = 0; base < E; base += 32) {
             const int e = base + lane;
-            int gs = 0;
-            if (e < E) {
-                gs = p.group_sizes[e];
-                if (gs < 0) *bad_flag = 1;
-            }
+            const int gs = e < E ? p.group_sizes[e] : 0;
             const int g = gs > 0 ? gs : 0;
-            const long long items = ((static_cast<long long>(g) + kMaxNT - 1) / kMaxNT) * p.n_tiles;
-            nt_max = max(nt_max, g >= kMaxNT ? kMaxNT : (g + 15) & ~15);
+            const long long items = ((static_cast<long long>(g) + chunk - 1) / chunk) * p.n_tiles;
+            nt_max = max(nt_max, g >= chunk ? chunk : (g + 15) & ~15);
             long long incl_r = g, incl_i = items;
 #pragma unroll
             for (int d = 1; d < 32; d <<= 1) {
@@ -314,6 +389,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
             roff[E] = static_cast<int>(run_rows);
             ioff[E] = static_cast<int>(run_items);
             *nt_max_slot = nt_max;
+            *chunk_slot = chunk;
         }
     }
     __syncthreads();
@@ -324,10 +400,13 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
     const int total_items = ioff[E];
     if (static_cast<int>(blockIdx.x) >= total_items) return;
     const int my_items = (total_items - static_cast<int>(blockIdx.x) + gridDim.x - 1) / gridDim.x;
+    const int chunk = *chunk_slot;
+    const int tile_cols = p.swiglu ? kBN / 2 : kBN;
     // The CTA's first kItemCache work items, decoded once (visible after the
     // barrier set-up's __syncthreads below); later ones are decoded on demand.
     for (int t = tid; t < my_items && t < kItemCache; t += kThreads) {
-        const Item it = decode_item(blockIdx.x + t * gridDim.x, roff, ioff, E, p.n_tiles);
+        const Item it = decode_item(blockIdx.x + t * gridDim.x, roff, ioff, E, p.n_tiles, chunk,
+                                    tile_cols);
         item_cache[t] = make_int4(it.e, it.row0, it.n0, it.nvalid | (it.nt << 16));
     }
     uint32_t *nv_tab = reinterpret_cast<uint32_t *>(smem + kOffNvTab);
@@ -335,7 +414,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
         for (int t = tid; t < 256; t += kThreads) nv_tab[t] = e4m3_scaled_pair(static_cast<uint32_t>(t));
     }
     auto get_item = [&](int i) -> Item {
-        if (i >= kItemCache) return decode_item(blockIdx.x + i * gridDim.x, roff, ioff, E, p.n_tiles);
+        if (i >= kItemCache)
+            return decode_item(blockIdx.x + i * gridDim.x, roff, ioff, E, p.n_tiles, chunk, tile_cols);
         const int4 v = item_cache[i];
         Item it;
         it.e = v.x;
@@ -354,28 +434,42 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
     // converter warps have read the codes and the 4 issuers' MMAs are done.
     // Single mode (wider bands): the code ring holds codes only and the
     // activations use eight 64-k slots of their own, released with the A
-    // slot of the same stage.
+    // slot of the same stage.  Wide mode (a band over 128 rows, K8
+    // activations): items of up to 256 tokens; one 256-column accumulator (the
+    // epilogue of an item runs before the next item's first MMA), and four
+    // 32 KB activation slots with their own ring, released by their own MMA
+    // commits, because eight would not fit in shared memory.
     const int nt_max = *nt_max_slot;
     const bool split = nt_max <= kPartCols;
+    const bool wide = chunk == kWideNT;
     // One 64-k activation tile: split mode nt_max rows (16-row boxes); single
-    // mode nt_max rounded up to 64 rows (64-row boxes, one or two copies a stage).
+    // and wide mode nt_max rounded up to 64 rows (64-row boxes, up to four
+    // copies a stage).
     const uint32_t act_stage_bytes =
         static_cast<uint32_t>(nt_max <= kPartCols ? nt_max : (nt_max + 63) & ~63) * 128u;
+    const uint32_t n_act = wide ? kWideActSlots : kSlots;   // activation slots (single, wide)
     // Ring slot: codes (16 KB), [split: activation tile], [scale tile, loaded
     // with every even code stage for itself and the next one].
     const uint32_t scale_off = kCodeStageBytes + (split ? 4u * act_stage_bytes : 0u);
     const uint32_t ring_stage_bytes = scale_off + (p.scale_tma ? kScaleTileBytes : 0u);
     const uint32_t CS = min(static_cast<uint32_t>(kCodeStagesMax),
-                            (kRingBytes - (split ? 0u : kSlots * act_stage_bytes)) / ring_stage_bytes);
-    const uint32_t act_off = CS * ring_stage_bytes;     // single mode: activation slots
-    // TMEM columns: two accumulator buffers, then the eight A slots (two sets of
-    // four, one set per code-stage parity).  With every band <= 16 rows the
-    // K-partials need only 16 columns each.
+                            (kRingBytes - (split ? 0u : n_act * act_stage_bytes)) / ring_stage_bytes);
+    const uint32_t act_off = CS * ring_stage_bytes;     // single/wide mode: activation slots
+    // TMEM columns: the accumulator buffers (two; one in wide mode), then the
+    // eight A slots (two sets of four, one set per code-stage parity).  With
+    // every band <= 16 rows the K-partials need only 16 columns each.
     const bool narrow = split && nt_max <= 16;
     const uint32_t per_wg = 2u;                            // A-slot sets in flight
     const uint32_t part_cols = narrow ? kPartCols / 2 : kPartCols;
-    const uint32_t acc_cols = split ? kIssuerWarps * part_cols : kAccCols;
-    const uint32_t acol0 = 2 * acc_cols;
+    const uint32_t nbuf = wide ? 1u : 2u;                  // accumulator buffers
+    const uint32_t acc_cols =
+        split ? kIssuerWarps * part_cols : (wide ? static_cast<uint32_t>(kWideNT) : kAccCols);
+    const uint32_t acol0 = nbuf * acc_cols;
+    // Activation-slot barriers the act producer waits on: the A-slot
+    // barriers in single mode (one slot ring for both), their own in wide mode.
+    uint64_t *act_free = wide ? act_empty : slot_empty;
+    // Issuers splitting the token columns of an item (single and wide mode).
+    const int n_iss = wide ? kWideIssuers : kSingleIssuers;
 
     if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
     if (tid == 0) {
@@ -386,10 +480,11 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
         for (int i = 0; i < kSlotsMax; ++i) {
             mbar_init(&a_full[i], 4);
             mbar_init(&act_full[i], 1);
-            mbar_init(&slot_empty[i], split ? 1 : kSingleIssuers);
+            mbar_init(&slot_empty[i], split ? 1 : n_iss);
+            mbar_init(&act_empty[i], n_iss);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&acc_full[i], split ? kIssuerWarps : kSingleIssuers);
+            mbar_init(&acc_full[i], split ? kIssuerWarps : n_iss);
             mbar_init(&acc_empty[i], 4 * kConvWG);
         }
         for (int i = 0; i < kIssuerWarps; ++i) mbar_init(&final_bar[i], 1);
@@ -412,11 +507,11 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
         // values stay warp-uniform); one elected lane issues the MMAs and the
         // commits, always the same lane, so each commit covers its MMAs.
         const int w = warp;
-        if (split || w < kSingleIssuers) {
+        if (split || w < n_iss) {
             Item it = get_item(0);
             // This issuer's token columns [c0, c0 + cn) of the item (single mode).
             auto my_cols = [&](int nt, uint32_t &c0, uint32_t &cn) {
-                if (split) {
+                if (split || n_iss == 1) {
                     c0 = 0;
                     cn = nt;
                     return;
@@ -435,33 +530,48 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
             // Single mode: stages come in groups of four (KT is a multiple of 4), and
             // the eight barriers of a group are probed together, so the probe
             // latency is paid once per group; the MMAs of the four stages follow,
-            // each stage's slot released by its own commit.
-            constexpr int kGroup = 4;
+            // each stage's slot released by its own commit.  Wide mode: groups of
+            // two (each stage is twice the MMA work, and only four activation
+            // slots exist, so a group of four would wait for all of them); the
+            // activation slots have their own ring and their own release commit.
+            constexpr int kGroupMax = 4;
+            const int grp = wide ? 2 : kGroupMax;
+            Ring ar;                          // wide mode: activation-slot ring
             for (int i = 0; i < my_items && ok && !split; ++i) {
-                const uint32_t buf = i & 1;
-                for (int kp = 0; kp < KT; kp += kGroup) {
-                    if (kp == 0 && !warp_wait_bounded(&acc_empty[buf], ((i >> 1) & 1) ^ 1,
-                                                      abort_flag, p.status, lim)) {
+                const uint32_t buf = wide ? 0u : static_cast<uint32_t>(i & 1);
+                const uint32_t acc_par = (wide ? static_cast<uint32_t>(i) : static_cast<uint32_t>(i >> 1)) & 1u;
+                for (int kp = 0; kp < KT; kp += grp) {
+                    if (kp == 0 && !warp_wait_bounded(&acc_empty[buf], acc_par ^ 1u, abort_flag,
+                                                      p.status, lim)) {
                         ok = false;
                         break;
                     }
-                    uint32_t sl[kGroup], ph[kGroup];
+                    uint32_t sl[kGroupMax], ph[kGroupMax], al[kGroupMax], aph[kGroupMax];
                     bool ready = true;
 #pragma unroll
-                    for (int h = 0; h < kGroup; ++h) {
+                    for (int h = 0; h < kGroupMax; ++h) {
+                        if (h >= grp) break;
                         sl[h] = sr.slot;
                         ph[h] = sr.phase;
                         sr.next(kSlots);
+                        if (wide) {
+                            al[h] = ar.slot;
+                            aph[h] = ar.phase;
+                            ar.next(n_act);
+                        } else {
+                            al[h] = sl[h];
+                            aph[h] = ph[h];
+                        }
                         ready = ready & mbar_try_wait(&a_full[sl[h]], ph[h]) &
-                                mbar_try_wait(&act_full[sl[h]], ph[h]);
+                                mbar_try_wait(&act_full[al[h]], aph[h]);
                     }
                     if (!__all_sync(0xffffffffu, ready)) {
 #pragma unroll
-                        for (int h = 0; h < kGroup; ++h)
-                            if (ok && (!warp_wait_bounded(&a_full[sl[h]], ph[h], abort_flag,
-                                                          p.status, lim) ||
-                                       !warp_wait_bounded(&act_full[sl[h]], ph[h], abort_flag,
-                                                          p.status, lim)))
+                        for (int h = 0; h < kGroupMax; ++h)
+                            if (h < grp && ok &&
+                                (!warp_wait_bounded(&a_full[sl[h]], ph[h], abort_flag, p.status, lim) ||
+                                 !warp_wait_bounded(&act_full[al[h]], aph[h], abort_flag, p.status,
+                                                    lim)))
                                 ok = false;
                         if (!ok) break;
                     }
@@ -469,10 +579,11 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
                     const uint32_t d_tmem = tmem_base + buf * acc_cols + c0;
                     if (elect_one()) {
 #pragma unroll
-                        for (int h = 0; h < kGroup; ++h) {
+                        for (int h = 0; h < kGroupMax; ++h) {
+                            if (h >= grp) break;
                             const uint32_t a_col = tmem_base + acol0 + sl[h] * kAColsPerSlot;
                             const uint64_t b0 =
-                                smem_desc_sw128(act_smem + sl[h] * act_stage_bytes + c0 * 128);
+                                smem_desc_sw128(act_smem + al[h] * act_stage_bytes + c0 * 128);
                             if (cn > 0)
 #pragma unroll
                             for (int kk = 0; kk < kStageK / 16; ++kk)
@@ -480,8 +591,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
                                             b0 + static_cast<uint64_t>(kk * 2), idesc,
                                             (kp == 0 && h == 0 && kk == 0) ? 0u : 1u);
                             mma_commit(&slot_empty[sl[h]]);
+                            if (wide) mma_commit(&act_empty[al[h]]);
                         }
-                        if (kp + kGroup >= KT) mma_commit(&acc_full[buf]);
+                        if (kp + grp >= KT) mma_commit(&acc_full[buf]);
                     }
                     __syncwarp();
                 }
@@ -561,6 +673,12 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
             if (split) tma_prefetch_map(use3d ? &tm_act3 : &tm_act);
             if (p.scale_tma) tma_prefetch_map(&tm_scales);
         }
+        // Fused SwiGLU: tile rows 32q .. 32q + 15 are gate rows n0 + 16q .. +15
+        // and 32q + 16 .. 32q + 31 the matching up rows (I further on).  The
+        // maps tm_codes / tm_scales then view each expert's rows as
+        // [16-row group q][half][row i] (5-D, x innermost), so one box of
+        // {x, 16 rows, 2 halves, 4 groups, 1 expert} lands the whole tile in
+        // that order; groups past I/16 are zero-filled.
         __syncwarp();
         Ring r;
         uint32_t issued = 0;
@@ -580,12 +698,20 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
                     mbar_arrive_expect_tx(&code_full[r.slot],
                                           kCodeStageBytes + (split ? it.nt * 512u : 0u) +
                                               (scales_here ? kScaleTileBytes : 0u));
-                    tma_load_2d(dst, &tm_codes, kc * 128, y, &code_full[r.slot]);
                     // 16 bytes a row: MXFP4 this code stage and its even/odd twin;
                     // NVFP4 this code stage's sixteen per-16 scales.
-                    if (scales_here)
-                        tma_load_2d(dst + scale_off, &tm_scales, kNv ? kc * 16 : (kc & ~1) * 8, y,
+                    const int sx = kNv ? kc * 16 : (kc & ~1) * 8;
+                    if (p.swiglu) {
+                        tma_load_5d(dst, &tm_codes, kc * 128, 0, 0, it.n0 >> 4, it.e,
                                     &code_full[r.slot]);
+                        if (scales_here)
+                            tma_load_5d(dst + scale_off, &tm_scales, sx, 0, 0, it.n0 >> 4, it.e,
+                                        &code_full[r.slot]);
+                    } else {
+                        tma_load_2d(dst, &tm_codes, kc * 128, y, &code_full[r.slot]);
+                        if (scales_here)
+                            tma_load_2d(dst + scale_off, &tm_scales, sx, y, &code_full[r.slot]);
+                    }
                     if (split) {
                         for (int grp = 0; grp < it.nt / 16; ++grp) {
                             if (use3d) {
@@ -618,8 +744,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
             bool ok = true;
             for (int i = 0; i < my_items && ok; ++i) {
                 const Item it = get_item(i);
-                for (int ks = 0; ks < KT; ++ks, r.next(kSlots), ++issued) {
-                    if (!wait_bounded(&slot_empty[r.slot], r.phase ^ 1u, abort_flag, p.status, lim)) {
+                for (int ks = 0; ks < KT; ++ks, r.next(n_act), ++issued) {
+                    if (!wait_bounded(&act_free[r.slot], r.phase ^ 1u, abort_flag, p.status, lim)) {
                         ok = false;
                         break;
                     }
@@ -632,9 +758,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
                 }
             }
             if (!ok) {
-                const uint32_t first = issued > kSlots ? issued - kSlots : 0;
+                const uint32_t first = issued > n_act ? issued - n_act : 0;
                 for (uint32_t h = first; h < issued; ++h)
-                    wait_bounded(&act_full[h % kSlots], (h / kSlots) & 1u, nullptr, p.status, lim);
+                    wait_bounded(&act_full[h % n_act], (h / n_act) & 1u, nullptr, p.status, lim);
             }
         }
     } else {
@@ -665,12 +791,18 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
             chunk_off[ch] = row * 128 + (((4 * half + ch) ^ (row & 7)) << 4);
         int bad_scale = 0;
         bool ok = true;
+        // Weight row of this thread's tile row in item `it` (fused SwiGLU: the
+        // gate/up interleave of the tile).
+        auto weight_row = [&](const Item &it) -> int {
+            return p.swiglu ? it.n0 + swiglu_row_offset(row) + (swiglu_row_is_up(row) ? p.I : 0)
+                            : it.n0 + row;
+        };
         // Scale bytes of code stage m for this row and half: blocks 8m + 4h ..
         // 8m + 4h + 3 of the row.  A tile row beyond N reads row N - 1 (its codes
         // are zero-filled, so the value never matters).
         auto scale_base = [&](int j) -> const uint8_t * {
             const Item it = get_item(j);
-            const int n = min(it.n0 + row, p.N - 1);
+            const int n = min(weight_row(it), p.N - 1);
             return p.scales + (static_cast<size_t>(it.e) * p.N + n) * p.scale_row +
                    (kNv ? 8 : 4) * half;
         };
@@ -699,8 +831,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
             return make_uint2(v[0], v[1]);
         };
         auto epilogue = [&](int i) -> bool {
-            const uint32_t buf = i & 1;
-            if (!warp_wait_bounded(&acc_full[buf], (i >> 1) & 1, abort_flag, p.status, lim))
+            const uint32_t buf = wide ? 0u : static_cast<uint32_t>(i & 1);
+            const uint32_t par = (wide ? static_cast<uint32_t>(i) : static_cast<uint32_t>(i >> 1)) & 1u;
+            if (!warp_wait_bounded(&acc_full[buf], par, abort_flag, p.status, lim))
                 return false;
             tc_fence_after();
             const Item it = get_item(i);
@@ -725,7 +858,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
             cur_nt = it.nt;
             // Scale bytes of a tile row beyond N (read with the tile) never count
             // as errors: those rows are not part of the output.
-            row_ok = it.n0 + row < p.N;
+            row_ok = p.swiglu ? it.n0 + swiglu_row_offset(row) < p.I : it.n0 + row < p.N;
             if (!p.scale_tma) sb = scale_base(it_idx);
         };
         if (i < my_items) enter_item(i);
@@ -846,6 +979,17 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
                 mbar_arrive(&a_full[slot0]);
                 mbar_arrive(&a_full[slot0 + 1]);
             }
+            // Wide mode has one accumulator: the next item's first MMAs wait for
+            // this item's epilogue.  The slots this pair fills next were last
+            // read by its stage c, whose MMAs needed the epilogue of item i - 1,
+            // so that epilogue runs now, right after the pair's first stage of
+            // item i (its decode-ahead stays in flight meanwhile).
+            if (wide) {
+                while (ok && ep_next <= i - 1) {
+                    if (!epilogue(ep_next)) ok = false;
+                    ++ep_next;
+                }
+            }
             // Next code stage of this pair: c + 2.
             code.next(CS);
             code.next(CS);
@@ -959,18 +1103,43 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
 // Both weight formats.  kNv = false: `scales` are per-32 E8M0 bytes [E, N, K/32].
 // kNv = true: `scales` are per-16 E4M3 bytes [E, N, K/16] and ws2 the per-expert
 // f32 weight_scale_2.
+// swiglu: N = 2 * I weight rows ([gate | up]); `out` is h, bf16 [rows, I], in
+// the K8-interleaved order when h_k8.
 template <bool kNv>
 static moe_status launch_gemm(const uint16_t *act, int rows, int K, const uint8_t *codes,
                               const uint8_t *scales, const float *ws2, const int32_t *group_sizes,
-                              int E, int N, void *out, int out_bf16, int act_k8, int *status,
-                              uint64_t wait_limit_ns, cudaStream_t stream, int num_sms) {
+                              int E, int N, void *out, int out_bf16, int act_k8, int swiglu,
+                              int h_k8, int *status, uint64_t wait_limit_ns, cudaStream_t stream,
+                              int num_sms) {
     using namespace gemm;
     if (rows == 0) return MOE_OK;
+    const int I = N / 2;   // fused SwiGLU: gate rows [0, I), up rows [I, 2I); I % 16 == 0
     PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode_fn();
     if (!encode) return MOE_ERR_CUDA;
 
     CUtensorMap tm_codes, tm_act, tm_act3, tm_scales, tm_act64;
-    {
+    // Fused SwiGLU: the rows of a weight tensor with `row_bytes` bytes a row,
+    // seen as [E][I/16 groups][2 halves][16 rows][row_bytes] with the group
+    // and half dimensions swapped in the view, so one box holds the tile's
+    // rows in the order (group, half, row).
+    auto encode_swiglu_view = [&](CUtensorMap *map, const void *base, cuuint64_t row_bytes,
+                                  cuuint32_t box_x, CUtensorMapSwizzle swz) -> bool {
+        cuuint64_t dims[5] = {row_bytes, 16, 2, static_cast<cuuint64_t>(I / 16),
+                              static_cast<cuuint64_t>(E)};
+        cuuint64_t strides[4] = {row_bytes, static_cast<cuuint64_t>(I) * row_bytes, 16 * row_bytes,
+                                 static_cast<cuuint64_t>(N) * row_bytes};
+        cuuint32_t box[5] = {box_x, 16, 2, 4, 1};
+        cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+        return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void *>(base), dims, strides,
+                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    };
+    if (swiglu) {
+        if (!encode_swiglu_view(&tm_codes, codes, static_cast<cuuint64_t>(K / 2), 128,
+                                CU_TENSOR_MAP_SWIZZLE_128B))
+            return MOE_ERR_CUDA;
+    } else {
         cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2),
                               static_cast<cuuint64_t>(E) * static_cast<cuuint64_t>(N)};
         cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
@@ -1026,7 +1195,11 @@ static moe_status launch_gemm(const uint16_t *act, int rows, int K, const uint8_
     // covers one code stage.
     const int scale_row = kNv ? K / 16 : K / 32;
     const int scale_tma = (K % (kNv ? 256 : 512)) == 0 && (reinterpret_cast<uintptr_t>(scales) & 15) == 0;
-    if (scale_tma) {
+    if (scale_tma && swiglu) {
+        if (!encode_swiglu_view(&tm_scales, scales, static_cast<cuuint64_t>(scale_row), 16,
+                                CU_TENSOR_MAP_SWIZZLE_NONE))
+            return MOE_ERR_CUDA;
+    } else if (scale_tma) {
         cuuint64_t dims[2] = {static_cast<cuuint64_t>(scale_row),
                               static_cast<cuuint64_t>(E) * static_cast<cuuint64_t>(N)};
         cuuint64_t strides[1] = {static_cast<cuuint64_t>(scale_row)};
@@ -1065,8 +1238,12 @@ static moe_status launch_gemm(const uint16_t *act, int rows, int K, const uint8_
     p.K = K;
     p.N = N;
     p.E = E;
-    p.out_bf16 = out_bf16;
-    p.n_tiles = (N + kBN - 1) / kBN;
+    p.out_bf16 = swiglu ? 1 : out_bf16;
+    p.swiglu = swiglu;
+    p.I = swiglu ? N / 2 : 0;
+    p.h_k8 = h_k8;
+    p.allow_wide = act_k8;
+    p.n_tiles = swiglu ? (N / 2 + kBN / 2 - 1) / (kBN / 2) : (N + kBN - 1) / kBN;
     p.k_stages = 4 * ((K + kCodeK - 1) / kCodeK);
     p.scale_row = scale_row;
     p.scale_vec2 = ((K / 32) % 2 == 0) && ((reinterpret_cast<uintptr_t>(scales) & 1) == 0);
@@ -1089,7 +1266,15 @@ moe_status launch_grouped_gemm(const uint16_t *act, int rows, int K, const uint8
                                void *out, int out_bf16, int act_k8, int *status,
                                uint64_t wait_limit_ns, cudaStream_t stream, int num_sms) {
     return launch_gemm<false>(act, rows, K, codes, scales, nullptr, group_sizes, E, N, out,
-                              out_bf16, act_k8, status, wait_limit_ns, stream, num_sms);
+                              out_bf16, act_k8, 0, 0, status, wait_limit_ns, stream, num_sms);
+}
+
+moe_status launch_grouped_gemm_swiglu(const uint16_t *act, int rows, int K, const uint8_t *codes,
+                                      const uint8_t *scales, const int32_t *group_sizes, int E,
+                                      int N, uint16_t *h, int act_k8, int h_k8, int *status,
+                                      uint64_t wait_limit_ns, cudaStream_t stream, int num_sms) {
+    return launch_gemm<false>(act, rows, K, codes, scales, nullptr, group_sizes, E, N, h, 1,
+                              act_k8, 1, h_k8, status, wait_limit_ns, stream, num_sms);
 }
 
 moe_status launch_grouped_gemm_nvfp4(const uint16_t *act, int rows, int K, const uint8_t *codes,
@@ -1098,7 +1283,7 @@ moe_status launch_grouped_gemm_nvfp4(const uint16_t *act, int rows, int K, const
                                      int out_bf16, int act_k8, int *status,
                                      uint64_t wait_limit_ns, cudaStream_t stream, int num_sms) {
     return launch_gemm<true>(act, rows, K, codes, scales16, weight_scale_2, group_sizes, E, N, out,
-                             out_bf16, act_k8, status, wait_limit_ns, stream, num_sms);
+                             out_bf16, act_k8, 0, 0, status, wait_limit_ns, stream, num_sms);
 }
 
 moe_status launch_decode_expert(const uint8_t *codes, const uint8_t *scales, int N, int K, int e,

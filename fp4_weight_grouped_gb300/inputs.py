@@ -202,8 +202,11 @@ def router_weights_uniform(seed: int, T: int, k: int) -> np.ndarray:
     return (w / w.sum(axis=1, keepdims=True)).astype(np.float32)
 
 
-WORKLOAD_TOKENS = {"decode_T64": (64, "uniform"), "decode_T256": (256, "uniform"),
-                   "prefill_T4096": (4096, "zipf"), "layer_T8192": (8192, "logits")}
+# name -> (tokens, routing, experts)
+WORKLOAD_TOKENS = {"decode_T64": (64, "uniform", 256), "decode_T256": (256, "uniform", 256),
+                   "prefill_T4096": (4096, "zipf", 256), "layer_T8192": (8192, "logits", 256),
+                   # the layer's band shape (about 192 rows per expert) on 64 experts
+                   "layer_E64_T2048": (2048, "logits", 64)}
 
 
 def layer_weights(seed: int = 0, E: int = 256, hidden: int = 4096, inter: int = 2048):
@@ -215,11 +218,11 @@ def layer_weights(seed: int = 0, E: int = 256, hidden: int = 4096, inter: int = 
     return dict(w13_codes=c13, w13_scales=s13, w2_codes=c2, w2_scales=s2)
 
 
-def workload_tokens(name: str, seed: int = 0, E: int = 256, k: int = 6, hidden: int = 4096) -> dict:
+def workload_tokens(name: str, seed: int = 0, k: int = 6, hidden: int = 4096) -> dict:
     """Routing ids, router weights and token activations of a named full-path
     workload (no weights): the draws layer_workload makes for the same name
     and seed."""
-    T, routing = WORKLOAD_TOKENS[name]
+    T, routing, E = WORKLOAD_TOKENS[name]
     if routing == "logits":
         ids, w = route_logits(seed, T, E, k)
     else:

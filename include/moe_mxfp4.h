@@ -217,6 +217,38 @@ MOE_API moe_status moe_mxfp4_grouped_gemm(const uint16_t *act, moe_act_layout ac
                                   void *stream);
 
 /*
+ * moe_mxfp4_grouped_gemm_swiglu — the w13 grouped matmul with the SwiGLU
+ * activation in its epilogue ([TPU] section 1: the w13 matmul and the
+ * fused-activation sweep that brought the 4,096-token w13 from 10.1 ms to
+ * 3.2 ms; [NVFP4]: w1 and w3 fused into one weight tensor, gate rows first).
+ *
+ *   y[r, n] = sum_k act[r, k] * e2m1(code[e, n, k]) * 2^(scale[e, n, k/32] - 127)
+ *   h[r, i] = silu(y[r, i]) * y[r, I + i],   silu(g) = g / (1 + e^-g)
+ *
+ * for every row r of band e, i < I.  y is formed in f32 exactly as
+ * moe_mxfp4_grouped_gemm forms it (same MMA order), h is computed in f32 as
+ * moe_swiglu computes it and rounded once to bf16: the output equals
+ * moe_swiglu(moe_mxfp4_grouped_gemm(...) in f32) bit for bit, and y is never
+ * written to memory.
+ *
+ * Arguments as for moe_mxfp4_grouped_gemm, except:
+ *  codes / scales  [E, 2*I, K/2] / [E, 2*I, K/32]: rows [0, I) gate, [I, 2I) up.
+ *  I               output columns of h, a positive multiple of 16.
+ *  h               device bf16 [rows, I] out, 2-byte aligned.
+ *  h_layout        order of h's columns (K8-interleaved needs I % 8 == 0), so h
+ *                  can feed the w2 grouped matmul directly.
+ * Each 128-row weight tile holds 64 gate rows and the matching 64 up rows (an
+ * interleave in groups of 16 done by the tile loads, one 5-D TMA box per
+ * stage; the weights in memory keep the [gate | up] layout).
+ */
+MOE_API moe_status moe_mxfp4_grouped_gemm_swiglu(const uint16_t *act, moe_act_layout act_layout,
+                                                 int64_t rows, int32_t K, const uint8_t *codes,
+                                                 const uint8_t *scales, const int32_t *group_sizes,
+                                                 int32_t E, int32_t I, uint16_t *h,
+                                                 moe_act_layout h_layout, void *workspace,
+                                                 size_t workspace_bytes, void *stream);
+
+/*
  * moe_nvfp4_grouped_gemm — the same grouped matmul with NVFP4 weights ([TPU]
  * section 1: the NVFP4 kernel that decodes e2m1 weights and per-16 E4M3 scales;
  * [NVFP4] "The lossless weight cast": per-16 E4M3 block scales under a
@@ -282,9 +314,11 @@ MOE_API moe_status moe_combine(const float *y, const int32_t *slot_to_row, const
 
 /*
  * moe_layer_forward — the whole routed-expert path in one call:
- * route_sort (with gather) -> w13 grouped GEMM -> SwiGLU -> w2 grouped GEMM ->
- * combine, each stage as described above, all on `stream`.  x_sorted and h
- * are written in the K8-interleaved order.
+ * route_sort (with gather) -> w13 grouped GEMM with SwiGLU in its epilogue
+ * (moe_mxfp4_grouped_gemm_swiglu) -> w2 grouped GEMM -> combine, each stage as
+ * described above, all on `stream` (six kernel launches).  x_sorted and h are
+ * written in the K8-interleaved order; the f32 gate/up product is never
+ * written.
  *
  *  x            device bf16 [T, hidden]; topk_ids int32 [T, k]; topk_w f32 [T, k].
  *  w13_codes/scales  [E, 2*inter, hidden/2] / [E, 2*inter, hidden/32]
@@ -293,8 +327,8 @@ MOE_API moe_status moe_combine(const float *y, const int32_t *slot_to_row, const
  *  out          device f32 [T, hidden].
  *  Caller-owned intermediates (device): group_sizes int32 [E], group_offsets
  *  int32 [E+1], sorted_slot / slot_to_row int32 [T*k], x_sorted bf16
- *  [T*k, hidden], y13 f32 [T*k, 2*inter], h bf16 [T*k, inter], y2 f32
- *  [T*k, hidden], workspace >= moe_workspace_bytes(T, k, E).
+ *  [T*k, hidden], h bf16 [T*k, inter], y2 f32 [T*k, hidden], workspace >=
+ *  moe_workspace_bytes(T, k, E).
  * hidden and inter must be multiples of 32.
  */
 MOE_API moe_status moe_layer_forward(const uint16_t *x, const int32_t *topk_ids, const float *topk_w,
@@ -302,8 +336,8 @@ MOE_API moe_status moe_layer_forward(const uint16_t *x, const int32_t *topk_ids,
                              const uint8_t *w13_codes, const uint8_t *w13_scales,
                              const uint8_t *w2_codes, const uint8_t *w2_scales, float *out,
                              int32_t *group_sizes, int32_t *group_offsets, int32_t *sorted_slot,
-                             int32_t *slot_to_row, uint16_t *x_sorted, float *y13, uint16_t *h,
-                             float *y2, void *workspace, size_t workspace_bytes, void *stream);
+                             int32_t *slot_to_row, uint16_t *x_sorted, uint16_t *h, float *y2,
+                             void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * moe_mxfp4_decode_expert — debug view of the GEMM's weight decode: writes

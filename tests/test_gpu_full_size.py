@@ -6,9 +6,12 @@ configuration the benchmark times (one persistent CTA per SM).
   prefill w13 (T = 4096, 24576 rows, Zipf routing): 16 random elements of
       every (expert, 128-column tile) pair plus the first and last row of
       every band; the full product would take the oracle about a minute.
-  layer (T = 8192, 49152 rows): route sort and gather bit-exact in full; the
-      w13 and w2 GEMMs sampled as for prefill; SwiGLU (fed the GPU's y13) and
-      combine (fed the GPU's y2) compared element by element.
+  layer (T = 8192, 49152 rows, w13 with SwiGLU in its epilogue): route sort
+      and gather bit-exact in full; the fused h bit-identical in full to the
+      unfused w13 GEMM followed by the SwiGLU kernel, that SwiGLU within 1 bf16
+      ulp of the oracle in full, h sampled against the oracle's own w13 sums;
+      the w13 and w2 GEMMs sampled as for prefill; combine (fed the GPU's y2)
+      compared element by element.
 
 Bars as in test_gpu_parity: GEMM |gpu - oracle| <= 1e-5 * sum|a w| + 1e-6;
 SwiGLU within 1 bf16 ulp; combine within 1e-6 * sum|w y| + 1e-6.
@@ -19,6 +22,7 @@ import torch
 
 import oracle
 from fp4_weight_grouped_gb300 import inputs
+from parity_bounds import check_swiglu_from_gemm
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -132,19 +136,35 @@ def test_layer_full_size_stagewise(B):
     xs = oracle.gather(c["x"], ss, k)
     np.testing.assert_array_equal(k8_deinterleave(B.bits_from_bf16(bufs.x_sorted)), xs)
 
-    # w13: every (expert, column tile) pair sampled
-    y13 = bufs.y13.cpu().numpy()
+    # w13 with SwiGLU fused: (1) the unfused GEMM, every (expert, column tile)
+    # pair sampled against the oracle; (2) the fused h bit-identical, every
+    # element, to the SwiGLU kernel applied to that GEMM's f32 output; (3) the
+    # SwiGLU kernel within 1 bf16 ulp of the oracle fed the same f32 sums,
+    # every element; (4) h sampled against the oracle's SwiGLU of the
+    # oracle's own gate/up sums.
+    K8 = B.MOE_ACT_K8_INTERLEAVED
+    y13_d = B.grouped_gemm(bufs.x_sorted, d_w13c, d_w13s, bufs.group_sizes, act_layout=K8)
+    y13 = y13_d.cpu().numpy()
     assert np.isfinite(y13).all()
     r, col = tile_samples(gs, 2 * I, seed=1)
     ref, mag = oracle.grouped_gemm_sampled(xs, c["w13_codes"], c["w13_scales"], gs, r, col)
     _tol_check(y13[r, col], ref, mag, what="layer w13")
-
-    # SwiGLU: every element, the oracle fed the GPU's y13
+    h_unfused = B.swiglu(y13_d, layout=K8)
+    np.testing.assert_array_equal(B.bits_from_bf16(bufs.h), B.bits_from_bf16(h_unfused))
+    del y13_d, h_unfused
+    h_nat = k8_deinterleave(B.bits_from_bf16(bufs.h))
     h_ref = oracle.swiglu(y13)
     del y13
-    h_nat = k8_deinterleave(B.bits_from_bf16(bufs.h))
     assert np.abs(h_nat.astype(np.int64) - h_ref.astype(np.int64)).max() <= 1
     del h_ref
+    rh, ih = tile_samples(gs, I, per_tile=32, seed=3)
+    gu_ref, gu_mag = oracle.grouped_gemm_sampled(
+        xs, c["w13_codes"], c["w13_scales"], gs, np.concatenate([rh, rh]), np.concatenate([ih, I + ih]))
+    n = rh.size
+    y_pair = np.stack([gu_ref[:n], gu_ref[n:]], axis=1)
+    m_pair = np.stack([gu_mag[:n], gu_mag[n:]], axis=1)
+    check_swiglu_from_gemm(h_nat[rh, ih][:, None], y_pair, m_pair, oracle.swiglu(y_pair),
+                           what="layer h (fused) vs oracle")
 
     # w2: sampled, the oracle fed the GPU's h
     y2 = bufs.y2.cpu().numpy()

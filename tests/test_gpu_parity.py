@@ -12,6 +12,7 @@ import torch
 
 import oracle
 from fp4_weight_grouped_gb300 import inputs
+from parity_bounds import check_swiglu_from_gemm
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -440,21 +441,28 @@ def test_layer_forward_stagewise(B):
                           B.to_device(c["topk_w"], DEV), B.to_device(c["w13_codes"], DEV),
                           B.to_device(c["w13_scales"], DEV), B.to_device(c["w2_codes"], DEV),
                           B.to_device(c["w2_scales"], DEV), bufs)
+    assert B.last_launch_count() == 6
     assert B.read_status(bufs.workspace) == B.MOE_OK
     gs, off, ss, s2r = oracle.route_sort(c["ids"], E)
     np.testing.assert_array_equal(bufs.slot_to_row.cpu().numpy(), s2r)
     xs = oracle.gather(c["x"], ss, k)
     np.testing.assert_array_equal(k8_deinterleave(B.bits_from_bf16(bufs.x_sorted)), xs)
+    # w13 with SwiGLU in its epilogue: h against the oracle's SwiGLU of the
+    # oracle's w13 sums (SwiGLU-of-GEMM bound), and bit-identical to the
+    # unfused GEMM followed by the SwiGLU kernel.
     y13, m13 = oracle.grouped_gemm(xs, c["w13_codes"], c["w13_scales"], gs)
-    _tol_check(bufs.y13.cpu().numpy(), y13, m13, what="w13")
-    href = oracle.swiglu(bufs.y13.cpu().numpy().astype(np.float64))
     h_nat = k8_deinterleave(B.bits_from_bf16(bufs.h))
-    assert np.abs(h_nat.astype(np.int64) - href.astype(np.int64)).max() <= 1
+    check_swiglu_from_gemm(h_nat, y13, m13, oracle.swiglu(y13), what="fused w13 + SwiGLU")
+    y13_gpu = B.grouped_gemm(bufs.x_sorted, B.to_device(c["w13_codes"], DEV),
+                             B.to_device(c["w13_scales"], DEV), bufs.group_sizes,
+                             act_layout=B.MOE_ACT_K8_INTERLEAVED)
+    _tol_check(y13_gpu.cpu().numpy(), y13, m13, what="w13")
+    np.testing.assert_array_equal(B.bits_from_bf16(bufs.h),
+                                  B.bits_from_bf16(B.swiglu(y13_gpu, layout=B.MOE_ACT_K8_INTERLEAVED)))
     y2, m2 = oracle.grouped_gemm(h_nat, c["w2_codes"], c["w2_scales"], gs)
     _tol_check(bufs.y2.cpu().numpy(), y2, m2, what="w2")
     o, mo = oracle.combine(bufs.y2.cpu().numpy().astype(np.float64), s2r, c["topk_w"])
     _tol_check(out.cpu().numpy(), o, mo, rel=1e-6, what="combine")
-    assert B.last_launch_count() == 7
 
 
 # ------------------------------------------------------- failure detection
