@@ -452,8 +452,15 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
     // with every even code stage for itself and the next one].
     const uint32_t scale_off = kCodeStageBytes + (split ? 4u * act_stage_bytes : 0u);
     const uint32_t ring_stage_bytes = scale_off + (p.scale_tma ? kScaleTileBytes : 0u);
+    // The ring depth is even: the converter pairs take alternate code stages,
+    // so with an even depth each pair owns every other slot and the slot it
+    // waits on was last consumed by the pair itself.  With an odd depth the
+    // slot of stage c + 2 last held stage c - 1 of the other pair, whose copy
+    // may still be in flight; the barrier would then be two phases behind and
+    // its parity would read as complete.
     const uint32_t CS = min(static_cast<uint32_t>(kCodeStagesMax),
-                            (kRingBytes - (split ? 0u : n_act * act_stage_bytes)) / ring_stage_bytes);
+                            (kRingBytes - (split ? 0u : n_act * act_stage_bytes)) / ring_stage_bytes) &
+                        ~1u;
     const uint32_t act_off = CS * ring_stage_bytes;     // single/wide mode: activation slots
     // TMEM columns: the accumulator buffers (two; one in wide mode), then the
     // eight A slots (two sets of four, one set per code-stage parity).  With
