@@ -317,6 +317,22 @@ __host__ __device__ __forceinline__ uint32_t idesc_bf16_f32(uint32_t M, uint32_t
            | ((M >> 4) << 24);  // M / 16
 }
 
+// silu(g) = g / (1 + e^-g) = s(g) / (1 + t) with t = e^-|g| = 2^(-|g| log2 e),
+// s(g) = g for g >= 0 and g * t for g < 0 (the same value, and no overflow:
+// t <= 1).  t comes from the hardware base-2 exponential (ex2.approx.f32, with
+// subnormal results kept, so silu stays nonzero down to g of about -103) and
+// the quotient from the hardware reciprocal (rcp.approx.f32): a few f32 ulps
+// of error, far below the half-ulp of the bf16 the result is rounded to.  Used
+// by the SwiGLU kernel and the fused w13 epilogue alike, so both round the
+// same f32 value.
+__device__ __forceinline__ float silu_f32(float g) {
+    const float x = -1.4426950408889634f * fabsf(g);   // -|g| * log2(e)
+    float t, r;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(t) : "f"(x));
+    asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(1.0f + t));
+    return (g >= 0.0f ? g : g * t) * r;
+}
+
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t d;
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));

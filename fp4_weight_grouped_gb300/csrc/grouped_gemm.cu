@@ -16,13 +16,13 @@
 // How (GB300 design, not the page's TPU design):
 //  * Swap-AB: the decoded weight tile (128 output columns n x K) is the MMA's A
 //    operand, held in tensor memory; the band's token rows are the B operand
-//    in shared memory (MMA N = 16..128).  Decode-sized bands thus fill the
+//    in shared memory (MMA N = 16..256).  Decode-sized bands thus fill the
 //    128-wide tensor-core dimension with weights, not with padding.
 //  * A ring of code stages in shared memory, filled by TMA: each holds the
 //    codes of 128 rows x 256 k (128-byte swizzle), the block-scale bytes when
 //    K % 512 == 0, and for narrow bands the band's activation tile of the same
 //    256 k, so activations arrive as early as the codes.  Wider bands take
-//    their activations through eight 64-k slots of their own.
+//    their activations through 64-k slots of their own.
 //  * Four converter warpgroups decode in pairs on alternate code stages: each
 //    warpgroup takes one 128-k half; a thread reads the 64 code bytes of its
 //    weight row, decodes them to bf16 pairs on the ALU and FMA pipes and
@@ -31,13 +31,18 @@
 //    adjacent 64-k sub-stages of every code stage into its own K-partial
 //    accumulator; the epilogue adds the partials in a fixed order (one issuer
 //    thread issues a small MMA only about every 50 cycles, so the work is
-//    shared).  Single mode (wider bands): the two issuers split the token
-//    columns of one accumulator and take four stages per barrier probe.
-//    Accumulators are double-buffered so the epilogue of one work item (done
-//    by the converter warps) overlaps the next item.
+//    shared).  Single mode (bands up to 128 rows): the two issuers split the
+//    token columns of one accumulator and take four stages per barrier probe;
+//    accumulators are double-buffered so the epilogue of one work item (done
+//    by the converter warps) overlaps the next item.  Wide mode (a band over
+//    128 rows, K8 activations): 256-token items, so each decoded weight feeds
+//    twice the MMA work; one issuer, one 256-column accumulator, five
+//    activation slots.
+//  * Fused SwiGLU (w13): a weight tile holds 64 gate rows and their 64 up
+//    rows, so the epilogue forms h = silu(g) * u and y13 is never stored.
 //  * Persistent CTAs (one per SM) walk a static list of work items (expert,
-//    128-token chunk, 128-column tile) built on the device from group_sizes;
-//    empty experts contribute no items and their weights are never read.
+//    token chunk, column tile) built on the device from group_sizes; empty
+//    experts contribute no items and their weights are never read.
 //  * Every wait is bounded (no unbounded barrier inside the pipeline); on
 //    timeout the kernel records MOE_ERR_TIMEOUT, drains its own copies and
 //    MMAs, frees tensor memory and returns.
@@ -58,10 +63,9 @@ namespace gemm {
 
 constexpr int kIssuerWarps = 2;               // warps 0..1: MMA issuers (one elected lane each)
 constexpr int kSingleIssuers = 2;             // single mode: issuers splitting the token columns
-#ifndef MOE_WIDE_ISSUERS
-#define MOE_WIDE_ISSUERS 2
-#endif
-constexpr int kWideIssuers = MOE_WIDE_ISSUERS;   // wide mode: issuers splitting the token columns
+// Wide mode: one issuer issues each stage as MMAs of N = the item's tokens
+// (up to 256), half the instructions of two issuers splitting the columns.
+constexpr int kWideIssuers = 1;
 constexpr int kConvWG = 4;                    // converter warpgroups: warps 2..17
 constexpr int kConvWarp0 = kIssuerWarps;
 constexpr int kActWarp = kConvWarp0 + 4 * kConvWG;    // warp 18: activation producer
@@ -70,10 +74,11 @@ constexpr int kThreads = 32 * (kCodeWarp + 1);        // 640
 constexpr int kBN = 128;                      // output columns per tile (MMA M)
 constexpr int kMaxNT = 128;                   // tokens per work item (MMA N)
 constexpr int kWideNT = 256;                  // wide mode: tokens per work item
-#ifndef MOE_WIDE_ACT_SLOTS
-#define MOE_WIDE_ACT_SLOTS 4
-#endif
-constexpr int kWideActSlots = MOE_WIDE_ACT_SLOTS;   // wide mode: activation slots (32 KB each)
+// Wide mode: activation slots (32 KB each).  Five leave room for two code
+// stages (the ring depth must be even), one per converter pair: the
+// converters run far ahead of the tensor core, while the activation tiles
+// (re-read from L2 for every column tile) need the deeper prefetch.
+constexpr int kWideActSlots = 5;
 constexpr int kStageK = 64;                   // K per decode / MMA stage
 constexpr int kSlots = 8;                     // A slots in TMEM (+ activation slots in smem)
 constexpr int kSlotsMax = 12;                 // bands <= 16 rows: three A slots per warpgroup
@@ -177,15 +182,6 @@ __device__ __forceinline__ int swiglu_row_offset(int row) {
 }
 __device__ __forceinline__ bool swiglu_row_is_up(int row) { return (row & 16) != 0; }
 
-// silu(g) = g / (1 + e^-g); for g < 0 the algebraically equal g*e^g / (1 + e^g)
-// avoids overflow of e^-g.  The same expression as the standalone SwiGLU
-// kernel, so the fused epilogue rounds to the same bf16 values.
-__device__ __forceinline__ float silu_f32(float g) {
-    if (g >= 0.f) return g / (1.f + expf(-g));
-    const float t = expf(g);
-    return g * t / (1.f + t);
-}
-
 // Column j of h in the K8-interleaved order: within each 8, element e is
 // stored at position 2e (e < 4) or 2(e - 4) + 1.
 __device__ __forceinline__ int k8_position(int j) {
@@ -264,6 +260,61 @@ __device__ __forceinline__ void store_item(const Params &p, const Item &it, uint
                         reinterpret_cast<__nv_bfloat16 *>(p.out)[off] = __float2bfloat16_rn(f[t]);
                     else
                         reinterpret_cast<float *>(p.out)[off] = f[t];
+                }
+            }
+        }
+    }
+}
+
+// Epilogue of one work item in wide mode (one accumulator, up to 64 columns a
+// warpgroup): the columns are read 16 at a time (one load, one wait), so at
+// most four load latencies are exposed per warp instead of one per four
+// columns.  The caller releases the accumulator afterwards.
+template <bool kNv>
+__device__ __forceinline__ void store_item_wide(const Params &p, const Item &it, uint32_t acc_base,
+                                                int wg, int row, float tensor_scale) {
+    const int qc = it.nt >> 2;                 // columns of this warpgroup: <= 64, multiple of 4
+    const int cb = wg * qc;
+    const bool up_lane = swiglu_row_is_up(row);
+    const int n = p.swiglu ? it.n0 + swiglu_row_offset(row) : it.n0 + row;
+    for (int c16 = 0; c16 < qc; c16 += 16) {
+        uint32_t v[16];
+        __syncwarp();
+        tmem_ld16(acc_base + cb + c16, v);
+        tmem_ld_wait();
+        {
+#pragma unroll
+            for (int t = 0; t < 16; t += 2) {
+                const int col = c16 + t;            // pair (col, col + 1): both < qc or both >= qc
+                if (col >= qc) break;
+                float a0 = __uint_as_float(v[t]), a1 = __uint_as_float(v[t + 1]);
+                if constexpr (kNv) {
+                    a0 = (a0 * 512.0f) * tensor_scale;
+                    a1 = (a1 * 512.0f) * tensor_scale;
+                }
+                if (p.swiglu) {
+                    const float recv = __shfl_xor_sync(0xffffffffu, up_lane ? a0 : a1, 16);
+                    const float g = up_lane ? recv : a0;
+                    const float u = up_lane ? a1 : recv;
+                    const int tok = cb + col + (up_lane ? 1 : 0);
+                    if (n < p.I && tok < it.nvalid) {
+                        const int hc = p.h_k8 ? k8_position(n) : n;
+                        reinterpret_cast<__nv_bfloat16 *>(p.out)[static_cast<size_t>(it.row0 + tok) * p.I + hc] =
+                            __float2bfloat16_rn(silu_f32(g) * u);
+                    }
+                } else if (n < p.N) {
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int tok = cb + col + e;
+                        if (tok < it.nvalid) {
+                            const size_t off = static_cast<size_t>(it.row0 + tok) * p.N + n;
+                            const float val = e ? a1 : a0;
+                            if (p.out_bf16)
+                                reinterpret_cast<__nv_bfloat16 *>(p.out)[off] = __float2bfloat16_rn(val);
+                            else
+                                reinterpret_cast<float *>(p.out)[off] = val;
+                        }
+                    }
                 }
             }
         }
@@ -436,7 +487,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
     // activations use eight 64-k slots of their own, released with the A
     // slot of the same stage.  Wide mode (a band over 128 rows, K8
     // activations): items of up to 256 tokens; one 256-column accumulator (the
-    // epilogue of an item runs before the next item's first MMA), and four
+    // epilogue of an item runs before the next item's first MMA), and five
     // 32 KB activation slots with their own ring, released by their own MMA
     // commits, because eight would not fit in shared memory.
     const int nt_max = *nt_max_slot;
@@ -510,9 +561,10 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
         // Split mode: issuer w issues the stages of converter warpgroup w
         // (every 4th stage) into K-partial w.  Single mode: issuers 0 and 1 issue
         // every stage, each for its own part of the item's token columns (the
-        // first a multiple of 16, about half), into one accumulator.  The whole warp runs the loop (its
-        // values stay warp-uniform); one elected lane issues the MMAs and the
-        // commits, always the same lane, so each commit covers its MMAs.
+        // first a multiple of 16, about half), into one accumulator.  Wide mode:
+        // issuer 0 alone, all of the item's columns.  The whole warp runs the
+        // loop (its values stay warp-uniform); one elected lane issues the MMAs
+        // and the commits, always the same lane, so each commit covers its MMAs.
         const int w = warp;
         if (split || w < n_iss) {
             Item it = get_item(0);
@@ -538,8 +590,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
             // the eight barriers of a group are probed together, so the probe
             // latency is paid once per group; the MMAs of the four stages follow,
             // each stage's slot released by its own commit.  Wide mode: groups of
-            // two (each stage is twice the MMA work, and only four activation
-            // slots exist, so a group of four would wait for all of them); the
+            // two (each stage is twice the MMA work, and only five activation
+            // slots exist, so a group of four would wait for most of them); the
             // activation slots have their own ring and their own release commit.
             constexpr int kGroupMax = 4;
             const int grp = wide ? 2 : kGroupMax;
@@ -844,8 +896,12 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
                 return false;
             tc_fence_after();
             const Item it = get_item(i);
-            store_item<kNv>(p, it, tmem_base + lane_off + buf * acc_cols, wg, row, split, part_cols,
-                            kNv ? __ldg(ws2 + it.e) : 0.0f);
+            const float ts = kNv ? __ldg(ws2 + it.e) : 0.0f;
+            if (wide)
+                store_item_wide<kNv>(p, it, tmem_base + lane_off, wg, row, ts);
+            else
+                store_item<kNv>(p, it, tmem_base + lane_off + buf * acc_cols, wg, row, split,
+                                part_cols, ts);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[buf]);

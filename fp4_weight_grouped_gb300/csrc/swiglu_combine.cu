@@ -2,7 +2,7 @@
 //
 // SwiGLU ("Running DeepSeek V4 Flash on TPU v6", section 1, the gate/up
 // activation left out of the grouped-matmul timings; "DeepSeek-V4-Flash-0731-
-// NVFP4": w1/w3 fused as GEMM1): h = silu(g) * u with g the first I columns and u
+// NVFP4": w1/w3 fused as GEMM1): h = silu_f32(g) * u with g the first I columns and u
 // the next I, in f32, rounded once to bf16.
 //
 // Combine ("DeepSeek-V4-Flash" (PocketLLM), "Correctness and precision": the MoE
@@ -21,14 +21,6 @@
 
 namespace moe {
 namespace ew {
-
-// silu(g) = g / (1 + e^-g); for g < 0 the algebraically equal g*e^g / (1 + e^g)
-// avoids overflow of e^-g.
-__device__ __forceinline__ float silu(float g) {
-    if (g >= 0.f) return g / (1.f + expf(-g));
-    const float t = expf(g);
-    return g * t / (1.f + t);
-}
 
 __device__ __forceinline__ void load8(const float *p, float (&v)[8]) {
     const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
@@ -65,10 +57,10 @@ __global__ void swiglu_vec8(const T *gu, long long rows, int I, uint16_t *h, int
         load8(row + i, g);
         load8(row + I + i, u);
         uint4 o;
-        o.x = pack_bf16x2(silu(g[0]) * u[0], silu(g[1]) * u[1]);
-        o.y = pack_bf16x2(silu(g[2]) * u[2], silu(g[3]) * u[3]);
-        o.z = pack_bf16x2(silu(g[4]) * u[4], silu(g[5]) * u[5]);
-        o.w = pack_bf16x2(silu(g[6]) * u[6], silu(g[7]) * u[7]);
+        o.x = pack_bf16x2(silu_f32(g[0]) * u[0], silu_f32(g[1]) * u[1]);
+        o.y = pack_bf16x2(silu_f32(g[2]) * u[2], silu_f32(g[3]) * u[3]);
+        o.z = pack_bf16x2(silu_f32(g[4]) * u[4], silu_f32(g[5]) * u[5]);
+        o.w = pack_bf16x2(silu_f32(g[6]) * u[6], silu_f32(g[7]) * u[7]);
         *reinterpret_cast<uint4 *>(h + r * I + i) = h_k8 ? interleave8(o) : o;
     }
 }
@@ -89,7 +81,7 @@ __global__ void swiglu_scalar(const T *gu, long long rows, int I, uint16_t *h) {
         const int i = static_cast<int>(idx - r * I);
         const float g = to_f32(gu[r * 2 * I + i]);
         const float u = to_f32(gu[r * 2 * I + I + i]);
-        const __nv_bfloat16 b = __float2bfloat16_rn(silu(g) * u);
+        const __nv_bfloat16 b = __float2bfloat16_rn(silu_f32(g) * u);
         h[idx] = *reinterpret_cast<const uint16_t *>(&b);
     }
 }
