@@ -235,7 +235,7 @@ class Workload:
             ev[2].record(stream)
         B.combine(b.y2, s2r, self.w, out=b.out)
 
-    LAUNCHES_PER_STEP = 6     # count, scan, scatter, w13 + SwiGLU, w2, combine
+    LAUNCHES_PER_STEP = 8     # count, scan, scatter, w13 + SwiGLU (2 band classes), w2 (2), combine
 
     def warm(self, n):
         import torch

@@ -186,7 +186,7 @@ moe_status moe_mxfp4_grouped_gemm(const uint16_t *act, moe_act_layout act_layout
                                   out, out_dtype == MOE_BF16, act_layout == MOE_ACT_K8_INTERLEAVED,
                                   status_word(workspace), kWaitLimitNs,
                                   static_cast<cudaStream_t>(stream), sms);
-    g_last_launches = rows > 0 ? 1 : 0;
+    g_last_launches = rows > 0 ? moe::kGemmLaunches : 0;
     return st;
 }
 
@@ -209,7 +209,7 @@ moe_status moe_mxfp4_grouped_gemm_swiglu(const uint16_t *act, moe_act_layout act
                                          h_layout == MOE_ACT_K8_INTERLEAVED,
                                          status_word(workspace), kWaitLimitNs,
                                          static_cast<cudaStream_t>(stream), sms);
-    g_last_launches = rows > 0 ? 1 : 0;
+    g_last_launches = rows > 0 ? moe::kGemmLaunches : 0;
     return st;
 }
 
@@ -230,7 +230,7 @@ moe_status moe_nvfp4_grouped_gemm(const uint16_t *act, moe_act_layout act_layout
                                         act_layout == MOE_ACT_K8_INTERLEAVED,
                                         status_word(workspace), kWaitLimitNs,
                                         static_cast<cudaStream_t>(stream), sms);
-    g_last_launches = rows > 0 ? 1 : 0;
+    g_last_launches = rows > 0 ? moe::kGemmLaunches : 0;
     return st;
 }
 
@@ -304,13 +304,13 @@ moe_status moe_layer_forward(const uint16_t *x, const int32_t *topk_ids, const f
         st = moe::launch_grouped_gemm_swiglu(x_sorted, static_cast<int>(rows), hidden, w13_codes,
                                              w13_scales, group_sizes, E, 2 * inter, h, 1, 1,
                                              status, kWaitLimitNs, s, sms);
-        ++launches;
+        launches += moe::kGemmLaunches;
     }
     if (st == MOE_OK && rows > 0) {
         st = moe::launch_grouped_gemm(h, static_cast<int>(rows), inter, w2_codes, w2_scales,
                                       group_sizes, E, hidden, y2, 0, 1, status, kWaitLimitNs, s,
                                       sms);
-        ++launches;
+        launches += moe::kGemmLaunches;
     }
     if (st == MOE_OK && T > 0) {
         st = moe::launch_combine(y2, slot_to_row, topk_w, T, k, hidden, out, 0, s, sms);

@@ -144,6 +144,12 @@ struct Params {
     int I;
     int h_k8;
     int allow_wide;    // K8 activations: bands over 128 rows take 256-token items
+    // Band class of this launch: only experts with band_lo <= rows <= band_hi
+    // get work items (row offsets still count every expert).  A grouped GEMM
+    // is two launches, bands up to 32 rows (split mode, weight streaming) and
+    // longer ones (single or wide mode), so a mix of short and long bands
+    // runs each in the mode made for it.
+    int band_lo, band_hi;
     uint64_t wait_limit_ns;
 };
 
@@ -403,7 +409,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
             const int e = base + lane;
             const int gs = e < E ? p.group_sizes[e] : 0;
             if (gs < 0) *bad_flag = 1;
-            g_max = max(g_max, gs);
+            if (gs >= p.band_lo && gs <= p.band_hi) g_max = max(g_max, gs);
         }
         g_max = __reduce_max_sync(0xffffffffu, g_max);
         const int chunk = (p.allow_wide && g_max > kMaxNT) ? kWideNT : kMaxNT;
@@ -413,8 +419,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
             const int e = base + lane;
             const int gs = e < E ? p.group_sizes[e] : 0;
             const int g = gs > 0 ? gs : 0;
-            const long long items = ((static_cast<long long>(g) + chunk - 1) / chunk) * p.n_tiles;
-            nt_max = max(nt_max, g >= chunk ? chunk : (g + 15) & ~15);
+            const int gw = (g >= p.band_lo && g <= p.band_hi) ? g : 0;   // rows with work here
+            const long long items = ((static_cast<long long>(gw) + chunk - 1) / chunk) * p.n_tiles;
+            nt_max = max(nt_max, gw >= chunk ? chunk : (gw + 15) & ~15);
             long long incl_r = g, incl_i = items;
 #pragma unroll
             for (int d = 1; d < 32; d <<= 1) {
@@ -1315,13 +1322,20 @@ static moe_status launch_gemm(const uint16_t *act, int rows, int K, const uint8_
     p.act_k8 = act_k8;
     p.act3d = act3d;
     p.scale_tma = scale_tma;
-    if constexpr (kNv)
-        grouped_gemm_nvfp4_kernel<<<num_sms, kThreads, smem_bytes, stream>>>(
-            tm_codes, tm_act, tm_act3, tm_scales, tm_act64, p, ws2);
-    else
-        grouped_gemm_kernel<<<num_sms, kThreads, smem_bytes, stream>>>(tm_codes, tm_act, tm_act3,
-                                                                       tm_scales, tm_act64, p);
-    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    // Two launches: bands of 1..32 rows, then bands of 33 or more (a launch
+    // whose class has no band returns from its prologue).
+    for (int cls = 0; cls < 2; ++cls) {
+        p.band_lo = cls == 0 ? 1 : kPartCols + 1;
+        p.band_hi = cls == 0 ? kPartCols : INT32_MAX;
+        if constexpr (kNv)
+            grouped_gemm_nvfp4_kernel<<<num_sms, kThreads, smem_bytes, stream>>>(
+                tm_codes, tm_act, tm_act3, tm_scales, tm_act64, p, ws2);
+        else
+            grouped_gemm_kernel<<<num_sms, kThreads, smem_bytes, stream>>>(tm_codes, tm_act, tm_act3,
+                                                                           tm_scales, tm_act64, p);
+        if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
 }
 
 moe_status launch_grouped_gemm(const uint16_t *act, int rows, int K, const uint8_t *codes,

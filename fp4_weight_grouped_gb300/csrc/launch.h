@@ -10,6 +10,10 @@
 
 namespace moe {
 
+// Kernel launches per grouped GEMM call: one per band class (bands of up to 32
+// rows, and longer bands).
+constexpr int kGemmLaunches = 2;
+
 size_t route_sort_scratch_bytes(int T, int k, int E);
 
 moe_status launch_route_sort(const int32_t *ids, int T, int k, int E, int32_t *group_sizes,

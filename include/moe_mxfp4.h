@@ -201,6 +201,9 @@ MOE_API moe_status moe_route_sort_noalloc(const int32_t *topk_ids, int32_t T, in
  *  E            1..1024 experts.  N >= 1 output columns.
  *  out          device [rows, N], f32 (4-byte aligned) or bf16 (RNE).
  *  workspace    device, >= 256 bytes (status word).
+ * Each call enqueues two kernel launches: bands of 1..32 rows (streamed
+ * weights, split accumulators) and bands of more rows (128- or 256-token
+ * work items); a launch whose class has no band exits at once.
  * Every weight is decoded exactly to bf16.  With scale bytes >= 2 every
  * nonzero weight is a normal bf16 number, its products with bf16 activations
  * are exact in f32, and results differ from an exact sum only by f32
@@ -316,7 +319,7 @@ MOE_API moe_status moe_combine(const float *y, const int32_t *slot_to_row, const
  * moe_layer_forward — the whole routed-expert path in one call:
  * route_sort (with gather) -> w13 grouped GEMM with SwiGLU in its epilogue
  * (moe_mxfp4_grouped_gemm_swiglu) -> w2 grouped GEMM -> combine, each stage as
- * described above, all on `stream` (six kernel launches).  x_sorted and h are
+ * described above, all on `stream` (eight kernel launches).  x_sorted and h are
  * written in the K8-interleaved order; the f32 gate/up product is never
  * written.
  *

@@ -441,7 +441,7 @@ def test_layer_forward_stagewise(B):
                           B.to_device(c["topk_w"], DEV), B.to_device(c["w13_codes"], DEV),
                           B.to_device(c["w13_scales"], DEV), B.to_device(c["w2_codes"], DEV),
                           B.to_device(c["w2_scales"], DEV), bufs)
-    assert B.last_launch_count() == 6
+    assert B.last_launch_count() == 8   # route sort 3, w13 2 (band classes), w2 2, combine 1
     assert B.read_status(bufs.workspace) == B.MOE_OK
     gs, off, ss, s2r = oracle.route_sort(c["ids"], E)
     np.testing.assert_array_equal(bufs.slot_to_row.cpu().numpy(), s2r)
