@@ -358,8 +358,11 @@ __device__ __forceinline__ void decode16_scaled(uint32_t c0, uint32_t c1, uint32
 // The kernel body for both weight formats.  kNv = false: MXFP4 (per-32 E8M0
 // scales).  kNv = true: NVFP4 (per-16 E4M3 scales `p.scales`, per-expert f32
 // weight_scale_2 `ws2`): each decoded weight is e2m1 * E4M3 * 2^-9, exact in
-// bf16, and the epilogue multiplies by 2^9 * weight_scale_2.
-template <bool kNv>
+// bf16, and the epilogue multiplies by 2^9 * weight_scale_2.  kSplit: the
+// launch for bands of at most 32 rows (split mode only); otherwise the launch
+// for longer bands (single or wide mode).  Separate instantiations keep each
+// mode's loops free of the other modes' code.
+template <bool kNv, bool kSplit>
 __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUtensorMap &tm_act,
                                           const CUtensorMap &tm_act3, const CUtensorMap &tm_scales,
                                           const CUtensorMap &tm_act64, const Params &p,
@@ -498,8 +501,10 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
     // 32 KB activation slots with their own ring, released by their own MMA
     // commits, because eight would not fit in shared memory.
     const int nt_max = *nt_max_slot;
-    const bool split = nt_max <= kPartCols;
-    const bool wide = chunk == kWideNT;
+    // The band class of the launch fixes the mode: nt_max <= 32 exactly when
+    // band_hi <= 32.
+    constexpr bool split = kSplit;
+    const bool wide = !kSplit && chunk == kWideNT;
     // One 64-k activation tile: split mode nt_max rows (16-row boxes); single
     // and wide mode nt_max rounded up to 64 rows (64-row boxes, up to four
     // copies a stage).
@@ -1093,15 +1098,17 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
     }
 }
 
+template <bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
                     const __grid_constant__ CUtensorMap tm_act,
                     const __grid_constant__ CUtensorMap tm_act3,
                     const __grid_constant__ CUtensorMap tm_scales,
                     const __grid_constant__ CUtensorMap tm_act64, const Params p) {
-    gemm_body<false>(tm_codes, tm_act, tm_act3, tm_scales, tm_act64, p, nullptr);
+    gemm_body<false, kSplit>(tm_codes, tm_act, tm_act3, tm_scales, tm_act64, p, nullptr);
 }
 
+template <bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tm_codes,
                           const __grid_constant__ CUtensorMap tm_act,
@@ -1109,7 +1116,7 @@ grouped_gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tm_codes,
                           const __grid_constant__ CUtensorMap tm_scales,
                           const __grid_constant__ CUtensorMap tm_act64, const Params p,
                           const float *__restrict__ ws2) {
-    gemm_body<true>(tm_codes, tm_act, tm_act3, tm_scales, tm_act64, p, ws2);
+    gemm_body<true, kSplit>(tm_codes, tm_act, tm_act3, tm_scales, tm_act64, p, ws2);
 }
 
 // Debug view of the decode: one thread per (weight row n, 32-element block); the
@@ -1291,12 +1298,13 @@ static moe_status launch_gemm(const uint16_t *act, int rows, int K, const uint8_
     if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
     const uint64_t dev_bit = dev >= 0 && dev < 64 ? 1ull << dev : 0;
     if (!(attr_dev_mask.load(std::memory_order_acquire) & dev_bit) || !dev_bit) {
-        const cudaError_t rc =
-            kNv ? cudaFuncSetAttribute(grouped_gemm_nvfp4_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes)
-                : cudaFuncSetAttribute(grouped_gemm_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
-        if (rc != cudaSuccess) return MOE_ERR_CUDA;
+        const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
+        const bool ok =
+            kNv ? cudaFuncSetAttribute(grouped_gemm_nvfp4_kernel<true>, a, smem_bytes) == cudaSuccess &&
+                      cudaFuncSetAttribute(grouped_gemm_nvfp4_kernel<false>, a, smem_bytes) == cudaSuccess
+                : cudaFuncSetAttribute(grouped_gemm_kernel<true>, a, smem_bytes) == cudaSuccess &&
+                      cudaFuncSetAttribute(grouped_gemm_kernel<false>, a, smem_bytes) == cudaSuccess;
+        if (!ok) return MOE_ERR_CUDA;
         attr_dev_mask.fetch_or(dev_bit, std::memory_order_release);
     }
     Params p;
@@ -1327,12 +1335,21 @@ static moe_status launch_gemm(const uint16_t *act, int rows, int K, const uint8_
     for (int cls = 0; cls < 2; ++cls) {
         p.band_lo = cls == 0 ? 1 : kPartCols + 1;
         p.band_hi = cls == 0 ? kPartCols : INT32_MAX;
-        if constexpr (kNv)
-            grouped_gemm_nvfp4_kernel<<<num_sms, kThreads, smem_bytes, stream>>>(
-                tm_codes, tm_act, tm_act3, tm_scales, tm_act64, p, ws2);
-        else
-            grouped_gemm_kernel<<<num_sms, kThreads, smem_bytes, stream>>>(tm_codes, tm_act, tm_act3,
-                                                                           tm_scales, tm_act64, p);
+        if constexpr (kNv) {
+            if (cls == 0)
+                grouped_gemm_nvfp4_kernel<true><<<num_sms, kThreads, smem_bytes, stream>>>(
+                    tm_codes, tm_act, tm_act3, tm_scales, tm_act64, p, ws2);
+            else
+                grouped_gemm_nvfp4_kernel<false><<<num_sms, kThreads, smem_bytes, stream>>>(
+                    tm_codes, tm_act, tm_act3, tm_scales, tm_act64, p, ws2);
+        } else {
+            if (cls == 0)
+                grouped_gemm_kernel<true><<<num_sms, kThreads, smem_bytes, stream>>>(
+                    tm_codes, tm_act, tm_act3, tm_scales, tm_act64, p);
+            else
+                grouped_gemm_kernel<false><<<num_sms, kThreads, smem_bytes, stream>>>(
+                    tm_codes, tm_act, tm_act3, tm_scales, tm_act64, p);
+        }
         if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
     }
     return MOE_OK;

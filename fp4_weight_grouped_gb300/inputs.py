@@ -206,7 +206,9 @@ def router_weights_uniform(seed: int, T: int, k: int) -> np.ndarray:
 WORKLOAD_TOKENS = {"decode_T64": (64, "uniform", 256), "decode_T256": (256, "uniform", 256),
                    "prefill_T4096": (4096, "zipf", 256), "layer_T8192": (8192, "logits", 256),
                    # the layer's band shape (about 192 rows per expert) on 64 experts
-                   "layer_E64_T2048": (2048, "logits", 64)}
+                   "layer_E64_T2048": (2048, "logits", 64),
+                   # decode-sized bands (one or two rows per expert) on 64 experts
+                   "decode_E64_T16": (16, "uniform", 64)}
 
 
 def layer_weights(seed: int = 0, E: int = 256, hidden: int = 4096, inter: int = 2048):
