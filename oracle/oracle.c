@@ -29,7 +29,11 @@
  *    bfloat16 for the larger codes, 255 is the E8M0 NaN);
  *  - stable sort: within an expert, slots keep ascending s = t*k + j;
  *  - w13 output columns [0, I) are the gate, [I, 2I) the up projection;
- *  - SwiGLU h = silu(g) * u, silu(g) = g / (1 + e^-g), rounded once to bf16.
+ *  - SwiGLU h = silu(g) * u, silu(g) = g / (1 + e^-g), rounded once to bf16;
+ *  - "block 32" and "block 512" ([TPU] section 1, the two measured kernel
+ *    variants) are read as the number of consecutive k sharing one E8M0 scale:
+ *    the scale of weight (e, n, k) is scales[e, n, k / block], with K / block
+ *    scale bytes per row.  MXFP4 proper is block 32.
  */
 #include <math.h>
 #include <pthread.h>
@@ -123,16 +127,23 @@ static void run_parallel(void (*fn)(void *, long), void *ctx, long n_items, int 
 
 /* ------------------------------------------------------------ weight decode */
 
-/* Exact value of weight (e, n, k): e2m1(code) * 2^(scale - 127).
- * Returns 0 on success, -1 if the scale byte is outside 0..252. */
-static int weight_value(const uint8_t *codes, const uint8_t *scales, long N, long K,
-                        long e, long n, long k, double *w) {
+/* Exact value of weight (e, n, k): e2m1(code) * 2^(scale - 127), with one
+ * scale byte per `block` consecutive k.  Returns 0 on success, -1 if the scale
+ * byte is outside 0..252. */
+static int weight_value_block(const uint8_t *codes, const uint8_t *scales, long N, long K,
+                              long block, long e, long n, long k, double *w) {
     uint8_t byte = codes[(e * N + n) * (K / 2) + k / 2];
     int code = (k & 1) ? (byte >> 4) : (byte & 15);
-    int s = scales[(e * N + n) * (K / 32) + k / 32];
+    int s = scales[(e * N + n) * (K / block) + k / block];
     if (s > 252) return -1;
     *w = ldexp(E2M1_VALUE[code], s - 127);
     return 0;
+}
+
+/* MXFP4: one scale per 32 k. */
+static int weight_value(const uint8_t *codes, const uint8_t *scales, long N, long K,
+                        long e, long n, long k, double *w) {
+    return weight_value_block(codes, scales, N, K, 32, e, n, k, w);
 }
 
 /* Decoded weights of expert e as bfloat16 bits [N, K].  Every e2m1 value times
@@ -194,6 +205,7 @@ typedef struct {
     long n_blocks_per_e;
     double *out, *abs_out;
     int bad_scale;
+    long block;                                 /* k per scale byte */
 } gemm_ctx;
 
 #define N_BLOCK 32
@@ -208,7 +220,8 @@ static void gemm_item(void *vctx, long item) {
     double *w = (double *)malloc(sizeof(double) * (size_t)K);
     for (long n = n0; n < n0 + N_BLOCK && n < N; ++n) {
         for (long k = 0; k < K; ++k)
-            if (weight_value(c->codes, c->scales, N, K, e, n, k, &w[k])) c->bad_scale = 1;
+            if (weight_value_block(c->codes, c->scales, N, K, c->block, e, n, k, &w[k]))
+                c->bad_scale = 1;
         for (long r = r0; r < r1; ++r) {
             const uint16_t *a = c->act + r * K;
             double acc = 0.0, mag = 0.0;
@@ -240,7 +253,30 @@ int oracle_grouped_gemm(const uint16_t *act, long rows, long K, const uint8_t *c
         off[e + 1] = off[e] + group_sizes[e];
     }
     if (off[E] != rows) { free(off); return -1; }
-    gemm_ctx c = {act, codes, scales, off, K, N, N_BLOCK, (N + N_BLOCK - 1) / N_BLOCK, out, abs_out, 0};
+    gemm_ctx c = {act, codes, scales, off, K, N, N_BLOCK, (N + N_BLOCK - 1) / N_BLOCK, out, abs_out, 0,
+                  32};
+    run_parallel(gemm_item, &c, E * c.n_blocks_per_e, n_threads);
+    free(off);
+    return c.bad_scale ? -1 : 0;
+}
+
+/* The grouped GEMM with one scale byte per `block` consecutive k (scales
+ * [E, N, K / block]); block 32 is oracle_grouped_gemm.  Returns -1 if block
+ * is not 32 or 512, K is not a multiple of block, or as oracle_grouped_gemm. */
+int oracle_grouped_gemm_block(const uint16_t *act, long rows, long K, long block,
+                              const uint8_t *codes, const uint8_t *scales,
+                              const int32_t *group_sizes, long E, long N, double *out,
+                              double *abs_out, int n_threads) {
+    if ((block != 32 && block != 512) || K % block) return -1;
+    int32_t *off = (int32_t *)malloc(sizeof(int32_t) * (size_t)(E + 1));
+    off[0] = 0;
+    for (long e = 0; e < E; ++e) {
+        if (group_sizes[e] < 0) { free(off); return -1; }
+        off[e + 1] = off[e] + group_sizes[e];
+    }
+    if (off[E] != rows) { free(off); return -1; }
+    gemm_ctx c = {act, codes, scales, off, K, N, N_BLOCK, (N + N_BLOCK - 1) / N_BLOCK, out, abs_out, 0,
+                  block};
     run_parallel(gemm_item, &c, E * c.n_blocks_per_e, n_threads);
     free(off);
     return c.bad_scale ? -1 : 0;

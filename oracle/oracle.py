@@ -53,6 +53,8 @@ def _load():
             lib.oracle_gather.restype = None
             lib.oracle_grouped_gemm.argtypes = [P, L, L, P, P, P, L, L, P, P, I]
             lib.oracle_grouped_gemm.restype = I
+            lib.oracle_grouped_gemm_block.argtypes = [P, L, L, L, P, P, P, L, L, P, P, I]
+            lib.oracle_grouped_gemm_block.restype = I
             lib.oracle_grouped_gemm_sampled.argtypes = [P, L, L, P, P, P, L, L, P, P, L, P, P, I]
             lib.oracle_grouped_gemm_sampled.restype = I
             lib.oracle_swiglu.argtypes = [P, L, L, P]
@@ -138,6 +140,24 @@ def grouped_gemm(act, codes, scales, group_sizes, n_threads: int = 0, with_abs: 
                                      _p(mag) if with_abs else None, n_threads)
     if rc:
         raise ValueError("sum(group_sizes) != rows, a negative size, or a scale byte > 252")
+    return out, mag
+
+
+def grouped_gemm_block(act, codes, scales, group_sizes, block: int, n_threads: int = 0,
+                       with_abs: bool = True):
+    """The grouped GEMM with one E8M0 scale per `block` consecutive k (32 or
+    512): scales uint8 [E, N, K/block].  Returns (out[rows, N], abs[rows, N])."""
+    act = _c(act, np.uint16)
+    codes, scales, gs = _c(codes, np.uint8), _c(scales, np.uint8), _c(group_sizes, np.int32)
+    rows, K = act.shape
+    E, N, _ = codes.shape
+    out = np.zeros((rows, N), np.float64)
+    mag = np.zeros((rows, N), np.float64) if with_abs else None
+    rc = _load().oracle_grouped_gemm_block(_p(act), rows, K, int(block), _p(codes), _p(scales),
+                                           _p(gs), E, N, _p(out), _p(mag) if with_abs else None,
+                                           n_threads)
+    if rc:
+        raise ValueError("bad block, K % block, sizes, or a scale byte > 252")
     return out, mag
 
 

@@ -293,6 +293,79 @@ def test_gemm_sampled_matches_full():
     np.testing.assert_array_equal(m, mag[r, c])
 
 
+# ------------------------------------------------------- scale block of 512
+
+def test_gemm_block512_tiny_exact_rational():
+    # Two 512-k scale blocks per row, scales differing across the boundary;
+    # every weight is rebuilt from the OCP bit fields and 2^(s - 127) with the
+    # scale indexed by k // 512.
+    rng = np.random.default_rng(14)
+    E, N, K = 2, 3, 1024
+    gs = np.array([2, 1], np.int32)
+    rows = int(gs.sum())
+    codes = rng.integers(0, 256, size=(E, N, K // 2), dtype=np.uint8)
+    scales = rng.integers(120, 134, size=(E, N, K // 512)).astype(np.uint8)
+    act = inputs.f32_to_bf16_bits(rng.standard_normal((rows, K)).astype(np.float32))
+    out, mag = oracle.grouped_gemm_block(act, codes, scales, gs, 512, n_threads=2)
+    a = inputs.bf16_bits_to_f32(act)
+    band = np.repeat(np.arange(E), gs)
+    for r in range(rows):
+        e = band[r]
+        for n in range(N):
+            exact = Fraction(0)
+            for k in range(K):
+                byte = int(codes[e, n, k // 2])
+                c = byte & 15 if k % 2 == 0 else byte >> 4
+                sg, ee, m = (c >> 3) & 1, (c >> 1) & 3, c & 1
+                w = Fraction(m, 2) if ee == 0 else Fraction(2) ** (ee - 1) * (1 + Fraction(m, 2))
+                w = (-w if sg else w) * Fraction(2) ** (int(scales[e, n, k // 512]) - 127)
+                exact += Fraction(float(a[r, k])) * w
+            assert abs(Fraction(out[r, n]) - exact) <= Fraction(mag[r, n]) * Fraction(K, 2 ** 52)
+
+
+def test_gemm_block512_one_hot_at_the_block_boundary():
+    # act one-hot at k = 511 and k = 512 picks the last weight of scale block 0
+    # and the first of block 1; code 0x2 is 1.0, so the outputs are the scales.
+    K, N = 1024, 2
+    codes = np.zeros((1, N, K // 2), np.uint8)
+    codes[0, :, 255] = 0x20          # k = 511 (high nibble of byte 255)
+    codes[0, :, 256] = 0x02          # k = 512 (low nibble of byte 256)
+    scales = np.array([[[120, 131], [127, 100]]], np.uint8)
+    one = inputs.f32_to_bf16_bits(np.array([1.0], np.float32))[0]
+    act = np.zeros((2, K), np.uint16)
+    act[0, 511] = one
+    act[1, 512] = one
+    out, _ = oracle.grouped_gemm_block(act, codes, scales, np.array([2], np.int32), 512)
+    np.testing.assert_array_equal(out, [[2.0 ** -7, 1.0], [2.0 ** 4, 2.0 ** -27]])
+
+
+def test_gemm_block512_equals_block32_with_repeated_scales():
+    # A 512-block scale is the same scale on each of its sixteen 32-blocks, so
+    # the result must equal the (separately pinned) block-32 GEMM bit for bit.
+    case = inputs.gemm_case(dict(E=5, k=2, T=30, K=1024, N=64, exp=(-9, -3)), seed=3)
+    gs, *_ = oracle.route_sort(case["ids"], case["E"])
+    rng = np.random.default_rng(15)
+    s512 = rng.integers(115, 131, size=(case["E"], case["N"], case["K"] // 512)).astype(np.uint8)
+    out512, mag512 = oracle.grouped_gemm_block(case["act"], case["codes"], s512, gs, 512)
+    out32, mag32 = oracle.grouped_gemm(case["act"], case["codes"], np.repeat(s512, 16, axis=2), gs)
+    np.testing.assert_array_equal(out512, out32)
+    np.testing.assert_array_equal(mag512, mag32)
+    # block 32 through the block entry point is the block-32 GEMM itself
+    o32, _ = oracle.grouped_gemm_block(case["act"], case["codes"], case["scales"], gs, 32)
+    np.testing.assert_array_equal(o32, oracle.grouped_gemm(case["act"], case["codes"], case["scales"], gs)[0])
+
+
+def test_gemm_block_rejects_other_blocks_and_ragged_k():
+    act = np.zeros((2, 512), np.uint16)
+    codes = np.zeros((1, 8, 256), np.uint8)
+    with pytest.raises(ValueError):
+        oracle.grouped_gemm_block(act, codes, np.full((1, 8, 8), 127, np.uint8), np.array([2], np.int32), 64)
+    act = np.zeros((2, 768), np.uint16)
+    codes = np.zeros((1, 8, 384), np.uint8)
+    with pytest.raises(ValueError):      # K = 768 is not a multiple of 512
+        oracle.grouped_gemm_block(act, codes, np.full((1, 8, 2), 127, np.uint8), np.array([2], np.int32), 512)
+
+
 # --------------------------------------------------------------------- SwiGLU
 
 def test_swiglu_closed_forms():
