@@ -287,6 +287,72 @@ class Workload:
 
 
 SUB_WORKLOADS = ("decode_T64", "decode_T256", "prefill_T4096")
+FORMAT_WORKLOADS = ("decode_T64", "prefill_T4096")     # NVFP4 and block-512 w13 timings
+
+
+def time_launches(fn, reps, stream):
+    """Average milliseconds of fn() over `reps` back-to-back calls (CUDA events)."""
+    import torch
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def run_formats(args, dev, wts, B, inputs, hbm, bf16):
+    """w13 grouped GEMM (f32 out, K8 activations) in three weight formats on the
+    decode and prefill shapes: MXFP4 (per-32 E8M0), NVFP4 (per-16 E4M3 under a
+    per-expert f32 scale; the MXFP4 weights cast losslessly by the library's
+    own cast kernel, so the outputs are bit-identical to MXFP4) and MXFP4 with
+    one E8M0 scale per 512 k (random scale bytes in the same range)."""
+    import torch
+    E, N, Kh = wts["w13_codes"].shape
+    K = 2 * Kh
+    ws = B.make_workspace(0, 1, 1, dev)
+    nv_out = B.mxfp4_to_nvfp4(wts["w13_scales"])
+    e4m3, ws2 = nv_out[0], nv_out[1]
+    s512 = B.to_device(inputs.e8m0_scales(args.seed, (E, N, K // 512), 117, 125), dev)
+    res = {}
+    stream = torch.cuda.current_stream(dev)
+    K8 = B.MOE_ACT_K8_INTERLEAVED
+    for name in FORMAT_WORKLOADS:
+        wl = Workload(name, args.seed, dev, wts, B, inputs)
+        b = wl.bufs
+        gs, _, _, _, xs = B.route_sort(wl.ids, wl.E, wl.x, b.workspace,
+                                       out=(b.group_sizes, b.group_offsets, b.sorted_slot,
+                                            b.slot_to_row, b.x_sorted), x_layout=K8)
+        y = torch.empty((xs.shape[0], N), dtype=torch.float32, device=dev)
+        calls = {
+            "mxfp4": lambda: B.grouped_gemm(xs, wts["w13_codes"], wts["w13_scales"], gs, out=y,
+                                            workspace=ws, act_layout=K8),
+            "nvfp4": lambda: B.nvfp4_grouped_gemm(xs, wts["w13_codes"], e4m3, ws2, gs, out=y,
+                                                  workspace=ws, act_layout=K8),
+            "mxfp4_block512": lambda: B.grouped_gemm_block(xs, wts["w13_codes"], s512, gs, 512,
+                                                           out=y, workspace=ws, act_layout=K8),
+        }
+        gsn = gs.cpu().numpy()
+        flops, wb32, touched, rows = gemm_work(gsn, K, N)
+        wbytes = {"mxfp4": wb32, "nvfp4": touched * N * K * (0.5 + 1.0 / 16),
+                  "mxfp4_block512": touched * N * K * (0.5 + 1.0 / 512)}
+        reps = 200 if rows < 4096 else 40
+        entry = {"rows": rows, "touched_experts": touched}
+        for fmt, fn in calls.items():
+            for _ in range(3):
+                fn()
+            ms = time_launches(fn, reps, stream)
+            entry[fmt] = kernel_roofline(flops, wbytes[fmt], rows * K * 2 + rows * N * 4, ms, hbm, bf16)
+            entry[fmt]["weight_bytes_per_launch"] = wbytes[fmt]
+        st = B.read_status(ws)
+        if st != B.MOE_OK:
+            raise RuntimeError(f"{name}: device status after the format timings: {B.status_string(st)}")
+        res[name] = entry
+        wl.free()
+        del wl, y
+        torch.cuda.empty_cache()
+    return res
 SUB_STEPS = {"decode_T64": 300, "decode_T256": 300, "prefill_T4096": 100, "layer_T8192": 60}
 SUSTAIN_S = 1.0          # the clock record covers at least this much back-to-back work
 
@@ -320,6 +386,10 @@ def run_ours(args, rank, world, local):
             wl.free()
             del wl
             torch.cuda.empty_cache()
+
+    formats = {}
+    if not args.no_sub_workloads and E_head == 256:
+        formats = run_formats(args, dev, wts, B, inputs, hbm, bf16_burst)
 
     # ---- the headline workload: exactly K timed steps
     wl = Workload(args.workload, args.seed + rank, dev, wts, B, inputs)
@@ -427,6 +497,7 @@ def run_ours(args, rank, world, local):
         "sustained": {"steps": n_sus, "ms_per_step": round(ms_sus, 5),
                       "w13_ms": round(w13_sus, 5), "seconds": round(n_sus * ms_sus * 1e-3, 3)},
         "workloads": subs,
+        "w13_formats": formats,
         "e2e": {"value": round(whole_job_rate(flops, e2e_ms, world) / 1e12, 3), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "api": "moe_layer_forward with pinned host copies"},

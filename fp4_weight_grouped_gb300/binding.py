@@ -24,7 +24,7 @@ SYMBOLS = (
     "moe_route_sort", "moe_mxfp4_grouped_gemm", "moe_swiglu", "moe_combine", "moe_layer_forward",
     "moe_mxfp4_decode_expert", "moe_debug_bounded_wait", "moe_last_launch_count",
     "moe_route_sort_noalloc", "moe_nvfp4_cast_workspace_bytes", "moe_mxfp4_to_nvfp4",
-    "moe_nvfp4_grouped_gemm", "moe_mxfp4_grouped_gemm_swiglu",
+    "moe_nvfp4_grouped_gemm", "moe_mxfp4_grouped_gemm_swiglu", "moe_mxfp4_grouped_gemm_block",
 )
 
 _lock = threading.Lock()
@@ -61,6 +61,8 @@ def load(path: str | None = None):
                                            C.c_int),
                 "moe_mxfp4_grouped_gemm": ([P, C.c_int, I64, I32, P, P, P, I32, I32, P, C.c_int, P, SZ,
                                             P], C.c_int),
+                "moe_mxfp4_grouped_gemm_block": ([P, C.c_int, I64, I32, I32, P, P, P, I32, I32, P,
+                                                  C.c_int, P, SZ, P], C.c_int),
                 "moe_mxfp4_grouped_gemm_swiglu": ([P, C.c_int, I64, I32, P, P, P, I32, I32, P,
                                                    C.c_int, P, SZ, P], C.c_int),
                 "moe_swiglu": ([P, C.c_int, I64, I32, P, C.c_int, P], C.c_int),
@@ -198,6 +200,26 @@ def grouped_gemm(act: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor,
                                        _ptr(group_sizes), E, N, _ptr(out), _dtype_code(out.dtype),
                                        _ptr(workspace), workspace.numel(), _stream(stream))
     _check(rc, "moe_mxfp4_grouped_gemm")
+    return out
+
+
+def grouped_gemm_block(act: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor,
+                       group_sizes: torch.Tensor, scale_block: int, out: torch.Tensor | None = None,
+                       out_dtype=torch.float32, workspace: torch.Tensor | None = None, stream=None,
+                       act_layout: int = MOE_ACT_ROW_MAJOR):
+    """grouped_gemm with one E8M0 scale per `scale_block` (32 or 512)
+    consecutive k: scales uint8 [E, N, K / scale_block]."""
+    rows, K = act.shape
+    E, N, _ = codes.shape
+    if out is None:
+        out = torch.empty((rows, N), dtype=out_dtype, device=act.device)
+    if workspace is None:
+        workspace = make_workspace(0, 1, 1, act.device, stream)
+    rc = load().moe_mxfp4_grouped_gemm_block(_ptr(act), act_layout, rows, K, int(scale_block),
+                                             _ptr(codes), _ptr(scales), _ptr(group_sizes), E, N,
+                                             _ptr(out), _dtype_code(out.dtype), _ptr(workspace),
+                                             workspace.numel(), _stream(stream))
+    _check(rc, "moe_mxfp4_grouped_gemm_block")
     return out
 
 

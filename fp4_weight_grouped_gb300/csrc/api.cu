@@ -190,6 +190,28 @@ moe_status moe_mxfp4_grouped_gemm(const uint16_t *act, moe_act_layout act_layout
     return st;
 }
 
+moe_status moe_mxfp4_grouped_gemm_block(const uint16_t *act, moe_act_layout act_layout,
+                                        int64_t rows, int32_t K, int32_t scale_block,
+                                        const uint8_t *codes, const uint8_t *scales,
+                                        const int32_t *group_sizes, int32_t E, int32_t N,
+                                        void *out, moe_dtype out_dtype, void *workspace,
+                                        size_t workspace_bytes, void *stream) {
+    if ((scale_block != 32 && scale_block != 512) || K <= 0 || K % scale_block != 0)
+        return MOE_ERR_INVALID_ARG;
+    moe_status st = check_gemm_args(act, act_layout, rows, K, codes, scales, group_sizes, E, N,
+                                    out, out_dtype, workspace, workspace_bytes);
+    if (st != MOE_OK) return st;
+    int sms = 0;
+    if ((st = current_device(&sms)) != MOE_OK) return st;
+    st = moe::launch_grouped_gemm_block(act, static_cast<int>(rows), K, scale_block, codes, scales,
+                                        group_sizes, E, N, out, out_dtype == MOE_BF16,
+                                        act_layout == MOE_ACT_K8_INTERLEAVED,
+                                        status_word(workspace), kWaitLimitNs,
+                                        static_cast<cudaStream_t>(stream), sms);
+    g_last_launches = rows > 0 ? moe::kGemmLaunches : 0;
+    return st;
+}
+
 moe_status moe_mxfp4_grouped_gemm_swiglu(const uint16_t *act, moe_act_layout act_layout,
                                          int64_t rows, int32_t K, const uint8_t *codes,
                                          const uint8_t *scales, const int32_t *group_sizes,

@@ -129,7 +129,9 @@ struct Params {
     int out_bf16;
     int n_tiles;       // ceil(N / 128)
     int k_stages;      // 64-k stages per item: 4 * ceil(K / 256)
-    int scale_row;     // K / 32
+    int scale_row;     // scale bytes a weight row: K / block (MXFP4), K / 16 (NVFP4)
+    int k_blocks;      // K / 32: 32-k blocks a weight row
+    int scale_shift;   // MXFP4: log2(block / 32); 32-k block b takes scale byte b >> scale_shift
     int scale_vec2;    // scale rows 2-byte aligned: load a stage's 2 scale bytes at once
     int scale_full;    // scale_vec2 and K % 256 == 0: every stage has both scale bytes
     int scale_tma;     // K % 512 == 0, 16-byte aligned scales: scale tiles ride in the ring
@@ -868,14 +870,15 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
             return p.swiglu ? it.n0 + swiglu_row_offset(row) + (swiglu_row_is_up(row) ? p.I : 0)
                             : it.n0 + row;
         };
-        // Scale bytes of code stage m for this row and half: blocks 8m + 4h ..
-        // 8m + 4h + 3 of the row.  A tile row beyond N reads row N - 1 (its codes
-        // are zero-filled, so the value never matters).
+        // Scale bytes of code stage m for this row and half: 32-k blocks 8m + 4h
+        // .. 8m + 4h + 3 of the row, each reading scale byte blk >> scale_shift
+        // (one byte per 32 k, or per 512 k).  A tile row beyond N reads row N - 1
+        // (its codes are zero-filled, so the value never matters).
         auto scale_base = [&](int j) -> const uint8_t * {
             const Item it = get_item(j);
             const int n = min(weight_row(it), p.N - 1);
             return p.scales + (static_cast<size_t>(it.e) * p.N + n) * p.scale_row +
-                   (kNv ? 8 : 4) * half;
+                   (kNv ? 8 * half : 0);
         };
         auto load_scales = [&](const uint8_t *sb, int m) -> uint32_t {
             uint32_t v = 0;
@@ -883,7 +886,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
             for (int b = 0; b < 4; ++b) {
                 const int blk = 8 * m + 4 * half + b;
                 const uint32_t sbyte =
-                    blk < p.scale_row ? static_cast<uint32_t>(__ldg(sb + 8 * m + b)) : 127u;
+                    blk < p.k_blocks ? static_cast<uint32_t>(__ldg(sb + (blk >> p.scale_shift))) : 127u;
                 v |= sbyte << (8 * b);
             }
             return v;
@@ -1182,12 +1185,13 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
 // f32 weight_scale_2.
 // swiglu: N = 2 * I weight rows ([gate | up]); `out` is h, bf16 [rows, I], in
 // the K8-interleaved order when h_k8.
+// scale_block (MXFP4): consecutive k per E8M0 scale byte, 32 or 512.
 template <bool kNv>
 static moe_status launch_gemm(const uint16_t *act, int rows, int K, const uint8_t *codes,
                               const uint8_t *scales, const float *ws2, const int32_t *group_sizes,
                               int E, int N, void *out, int out_bf16, int act_k8, int swiglu,
                               int h_k8, int *status, uint64_t wait_limit_ns, cudaStream_t stream,
-                              int num_sms) {
+                              int num_sms, int scale_block = 32) {
     using namespace gemm;
     if (rows == 0) return MOE_OK;
     const int I = N / 2;   // fused SwiGLU: gate rows [0, I), up rows [I, 2I); I % 16 == 0
@@ -1269,9 +1273,11 @@ static moe_status launch_gemm(const uint16_t *act, int rows, int K, const uint8_
     // Scale tiles: [E*N rows][scale bytes a row], boxes of 16 bytes x 128 rows,
     // when the row pitch and the base allow 16-byte TMA rows.  MXFP4: K/32
     // bytes a row, a box covers two code stages.  NVFP4: K/16 bytes a row, a box
-    // covers one code stage.
-    const int scale_row = kNv ? K / 16 : K / 32;
-    const int scale_tma = (K % (kNv ? 256 : 512)) == 0 && (reinterpret_cast<uintptr_t>(scales) & 15) == 0;
+    // covers one code stage.  MXFP4 with one scale per 512 k: K/512 bytes a
+    // row, loaded by the converter threads.
+    const int scale_row = kNv ? K / 16 : K / scale_block;
+    const int scale_tma = (kNv || scale_block == 32) && (K % (kNv ? 256 : 512)) == 0 &&
+                          (reinterpret_cast<uintptr_t>(scales) & 15) == 0;
     if (scale_tma && swiglu) {
         if (!encode_swiglu_view(&tm_scales, scales, static_cast<cuuint64_t>(scale_row), 16,
                                 CU_TENSOR_MAP_SWIZZLE_NONE))
@@ -1324,6 +1330,8 @@ static moe_status launch_gemm(const uint16_t *act, int rows, int K, const uint8_
     p.n_tiles = swiglu ? (N / 2 + kBN / 2 - 1) / (kBN / 2) : (N + kBN - 1) / kBN;
     p.k_stages = 4 * ((K + kCodeK - 1) / kCodeK);
     p.scale_row = scale_row;
+    p.k_blocks = K / 32;
+    p.scale_shift = scale_block == 512 ? 4 : 0;
     p.scale_vec2 = ((K / 32) % 2 == 0) && ((reinterpret_cast<uintptr_t>(scales) & 1) == 0);
     p.scale_full = p.scale_vec2 && (K % kCodeK) == 0;
     p.wait_limit_ns = wait_limit_ns;
@@ -1361,6 +1369,16 @@ moe_status launch_grouped_gemm(const uint16_t *act, int rows, int K, const uint8
                                uint64_t wait_limit_ns, cudaStream_t stream, int num_sms) {
     return launch_gemm<false>(act, rows, K, codes, scales, nullptr, group_sizes, E, N, out,
                               out_bf16, act_k8, 0, 0, status, wait_limit_ns, stream, num_sms);
+}
+
+moe_status launch_grouped_gemm_block(const uint16_t *act, int rows, int K, int scale_block,
+                                     const uint8_t *codes, const uint8_t *scales,
+                                     const int32_t *group_sizes, int E, int N, void *out,
+                                     int out_bf16, int act_k8, int *status, uint64_t wait_limit_ns,
+                                     cudaStream_t stream, int num_sms) {
+    return launch_gemm<false>(act, rows, K, codes, scales, nullptr, group_sizes, E, N, out,
+                              out_bf16, act_k8, 0, 0, status, wait_limit_ns, stream, num_sms,
+                              scale_block);
 }
 
 moe_status launch_grouped_gemm_swiglu(const uint16_t *act, int rows, int K, const uint8_t *codes,

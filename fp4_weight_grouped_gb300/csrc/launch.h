@@ -32,6 +32,13 @@ moe_status launch_grouped_gemm(const uint16_t *act, int rows, int K, const uint8
                                void *out, int out_bf16, int act_k8, int *status,
                                uint64_t wait_limit_ns, cudaStream_t stream, int num_sms);
 
+// MXFP4 with one E8M0 scale per scale_block (32 or 512) consecutive k.
+moe_status launch_grouped_gemm_block(const uint16_t *act, int rows, int K, int scale_block,
+                                     const uint8_t *codes, const uint8_t *scales,
+                                     const int32_t *group_sizes, int E, int N, void *out,
+                                     int out_bf16, int act_k8, int *status, uint64_t wait_limit_ns,
+                                     cudaStream_t stream, int num_sms);
+
 // Fused w13 + SwiGLU: N = 2 * I weight rows ([gate | up]) -> h bf16 [rows, I].
 moe_status launch_grouped_gemm_swiglu(const uint16_t *act, int rows, int K, const uint8_t *codes,
                                       const uint8_t *scales, const int32_t *group_sizes, int E,

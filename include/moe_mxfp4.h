@@ -220,6 +220,27 @@ MOE_API moe_status moe_mxfp4_grouped_gemm(const uint16_t *act, moe_act_layout ac
                                   void *stream);
 
 /*
+ * moe_mxfp4_grouped_gemm_block — moe_mxfp4_grouped_gemm with a choice of how
+ * many consecutive k share one E8M0 scale ([TPU] section 1: the kernel is
+ * measured "with block 32" and "with block 512"; read here as the scale block).
+ *
+ *   out[r, n] = sum_k act[r, k] * e2m1(code[e, n, k]) * 2^(scale[e, n, k/scale_block] - 127)
+ *
+ *  scale_block  32 (MXFP4 proper: identical to moe_mxfp4_grouped_gemm) or 512.
+ *  K            a multiple of scale_block.
+ *  scales       device uint8 [E, N, K/scale_block].
+ * Everything else as for moe_mxfp4_grouped_gemm.  With scale_block 512 the
+ * scale bytes are read by the converter threads (a row of K/512 bytes is too
+ * short for a TMA box); the tensor-core path is the same.
+ */
+MOE_API moe_status moe_mxfp4_grouped_gemm_block(const uint16_t *act, moe_act_layout act_layout,
+                                                int64_t rows, int32_t K, int32_t scale_block,
+                                                const uint8_t *codes, const uint8_t *scales,
+                                                const int32_t *group_sizes, int32_t E, int32_t N,
+                                                void *out, moe_dtype out_dtype, void *workspace,
+                                                size_t workspace_bytes, void *stream);
+
+/*
  * moe_mxfp4_grouped_gemm_swiglu — the w13 grouped matmul with the SwiGLU
  * activation in its epilogue ([TPU] section 1: the w13 matmul and the
  * fused-activation sweep that brought the 4,096-token w13 from 10.1 ms to

@@ -148,3 +148,20 @@ def test_route_sort_rejects_bad_arguments_on_host(lib):
     assert f(fake, 16, 2, 8, fake, fake, fake, fake, fake, 12, fake, 0, fake, 1 << 20, None) == 1   # hidden % 8
     assert f(fake, 16, 2, 8, fake, fake, fake, fake, None, 0, None, 0, fake, 100, None) == 1        # small ws
     assert f(fake, 16, 2, 8, fake, fake, fake, fake, None, 0, None, 5, fake, 1 << 20, None) == 1    # bad layout
+
+
+def test_block_gemm_rejects_bad_block_on_host(lib):
+    f = lib.moe_mxfp4_grouped_gemm_block
+    P = C.c_void_p
+    f.argtypes = [P, C.c_int, C.c_int64, C.c_int32, C.c_int32, P, P, P, C.c_int32, C.c_int32, P,
+                  C.c_int, P, C.c_size_t, P]
+    f.restype = C.c_int
+    fake = P(4096)
+
+    def call(K=1024, block=512):
+        return f(fake, 0, 8, K, block, fake, fake, fake, 4, 128, fake, 0, fake, 1 << 12, None)
+
+    assert call(block=64) == 1
+    assert call(block=0) == 1
+    assert call(K=768) == 1          # K % 512
+    assert call(K=0) == 1
