@@ -12,12 +12,12 @@
 //
 // Every E4M3 byte depends on the expert's maximum, so the data is read, reduced
 // across the expert, then converted.  Two forms:
-//   * one pass (the usual shapes): one thread-block cluster of up to 8 CTAs per
-//     expert.  Every thread loads its 256 scale bytes into registers (16 loads
-//     of 16 bytes in flight), the CTAs of the cluster exchange their maxima
-//     through distributed shared memory, and each thread converts from its
-//     registers and stores.  The scales are read from HBM once: 3 bytes of
-//     traffic per scale byte, the algorithmic minimum.
+//   * one pass (the usual shapes): one thread-block cluster of up to 16 CTAs
+//     of 128 threads per expert.  Every thread loads its 256 scale bytes into
+//     registers (16 loads of 16 bytes in flight), the CTAs of the cluster
+//     exchange their maxima through distributed shared memory, and each thread
+//     converts from its registers and stores.  The scales are read from HBM
+//     once: 3 bytes of traffic per scale byte, the algorithmic minimum.
 //   * two passes (an expert over 512 KiB, or buffers off 16-byte boundaries):
 //     a per-expert maximum into scratch, then the conversion.
 // Four scale bytes are converted at a time with byte-parallel integer
@@ -39,8 +39,12 @@ constexpr int kThreads = 256;
 constexpr int kBlocksPerSM = 8;            // two-pass grid: blocks per SM
 constexpr long long kMinChunk = 4096;      // two-pass grid: smallest chunk
 constexpr int kRegVec = 16;                // one pass: 16-byte words per thread
-constexpr long long kSlice = static_cast<long long>(kThreads) * kRegVec * 16;   // 64 KiB per CTA
-constexpr int kMaxCluster = 8;             // portable cluster size
+// One pass: threads per CTA.  A CTA holds 32 KiB in registers and a cluster of
+// up to 16 CTAs (non-portable size, opted in) covers an expert's 512 KiB;
+// four or five CTAs fit an SM, so one expert's stores overlap another's loads.
+constexpr int kOneNT = 128;
+constexpr long long kSlice = static_cast<long long>(kOneNT) * kRegVec * 16;
+constexpr int kMaxCluster = kOneNT == 256 ? 8 : 16;
 constexpr uint32_t kOnes = 0x01010101u, kHigh = 0x80808080u;
 
 __device__ __forceinline__ uint32_t max_byte4(uint32_t w) {
@@ -116,7 +120,7 @@ __device__ __forceinline__ T block_reduce(T v, Op op, T *warp_vals) {
 // Grid (C, E) with clusters of (C, 1, 1): cluster e converts expert e; CTA c
 // holds bytes [c * kSlice, min((c + 1) * kSlice, per_expert)) in registers.
 // Needs per_expert % 16 == 0, per_expert <= C * kSlice, 16-byte aligned bases.
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kOneNT, kOneNT == 256 ? 2 : 4)
 onepass_kernel(const uint8_t *__restrict__ scales, long long per_expert, uint8_t *__restrict__ e4m3,
                float *__restrict__ weight_scale_2, unsigned long long *__restrict__ out_of_range,
                int *status) {
@@ -125,18 +129,22 @@ onepass_kernel(const uint8_t *__restrict__ scales, long long per_expert, uint8_t
     const unsigned rank = cluster.block_rank();
     const unsigned csize = cluster.num_blocks();
     __shared__ uint32_t expert_max, expert_in_range;   // gathered from the whole cluster
-    __shared__ uint32_t warp_vals[kThreads / 32];
+    __shared__ uint32_t warp_vals[kOneNT / 32];
     if (threadIdx.x == 0) {
         expert_max = 0;
         expert_in_range = 0;
     }
+    // Arrive now, wait after the loads: the peers' maxima are written into this
+    // CTA's expert_max only once every CTA of the cluster has started and
+    // initialised it, and the barrier's latency hides behind the loads.
+
     const long long lo = static_cast<long long>(rank) * kSlice;
     const long long nvec = max(0LL, min(kSlice, per_expert - lo)) / 16;
     const uint4 *src = reinterpret_cast<const uint4 *>(scales + static_cast<long long>(e) * per_expert + lo);
     uint4 w[kRegVec];
 #pragma unroll
     for (int u = 0; u < kRegVec; ++u) {
-        const long long j = threadIdx.x + static_cast<long long>(u) * kThreads;
+        const long long j = threadIdx.x + static_cast<long long>(u) * kOneNT;
         w[u] = j < nvec ? __ldcs(src + j) : make_uint4(0, 0, 0, 0);
     }
     uint32_t acc = 0;
@@ -144,17 +152,18 @@ onepass_kernel(const uint8_t *__restrict__ scales, long long per_expert, uint8_t
     for (int u = 0; u < kRegVec; ++u) acc = max_byte16(acc, w[u]);
     const uint32_t m_warp = __reduce_max_sync(0xffffffffu, max_byte4(acc));
     const uint32_t m_cta =
-        block_reduce<kThreads>(m_warp, [](uint32_t a, uint32_t b) { return max(a, b); }, warp_vals);
+        block_reduce<kOneNT>(m_warp, [](uint32_t a, uint32_t b) { return max(a, b); }, warp_vals);
     cluster.sync();                                 // every CTA's expert_max is initialised
     if (threadIdx.x < csize) atomicMax(cluster.map_shared_rank(&expert_max, threadIdx.x), m_cta);
-    cluster.sync();                                 // every CTA's maximum has arrived everywhere
+    cluster.sync();                                 // every CTA's maximum has arrived everywhere;
+                                                    // no shared memory of a peer is used after this
     const uint32_t m = expert_max;
     const uint32_t M = m * kOnes;
     uint4 *dst = reinterpret_cast<uint4 *>(e4m3 + 2 * (static_cast<long long>(e) * per_expert + lo));
     uint32_t in_range = 0;
 #pragma unroll
     for (int u = 0; u < kRegVec; ++u) {
-        const long long j = threadIdx.x + static_cast<long long>(u) * kThreads;
+        const long long j = threadIdx.x + static_cast<long long>(u) * kOneNT;
         if (j < nvec) {
             uint4 o0, o1;
             convert16(w[u], M, in_range, o0, o1);
@@ -165,7 +174,7 @@ onepass_kernel(const uint8_t *__restrict__ scales, long long per_expert, uint8_t
     const uint32_t r_warp = __reduce_add_sync(0xffffffffu, in_range);
     __syncthreads();                                // warp_vals reused
     const uint32_t r_cta =
-        block_reduce<kThreads>(r_warp, [](uint32_t a, uint32_t b) { return a + b; }, warp_vals);
+        block_reduce<kOneNT>(r_warp, [](uint32_t a, uint32_t b) { return a + b; }, warp_vals);
     if (threadIdx.x == 0) atomicAdd(cluster.map_shared_rank(&expert_in_range, 0), r_cta);
     cluster.sync();                                 // all counts are in CTA 0
     if (rank == 0 && threadIdx.x == 0) {
@@ -302,7 +311,13 @@ moe_status launch_mxfp4_to_nvfp4(const uint8_t *scales, int E, int N, int K, uin
         const unsigned csize = static_cast<unsigned>((per_expert + kSlice - 1) / kSlice);
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(csize, static_cast<unsigned>(E), 1);
-        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.blockDim = dim3(kOneNT, 1, 1);
+        if (kMaxCluster > 8) {
+            // Clusters beyond the portable 8 need the opt-in (set once per process).
+            static const cudaError_t opt = cudaFuncSetAttribute(
+                onepass_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (opt != cudaSuccess) return MOE_ERR_CUDA;
+        }
         cfg.dynamicSmemBytes = 0;
         cfg.stream = stream;
         cudaLaunchAttribute attr[1];

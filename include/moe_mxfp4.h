@@ -407,7 +407,7 @@ MOE_API size_t moe_nvfp4_cast_workspace_bytes(int32_t E);
  *                  16-byte aligned; its status word as for every call.
  * Launches one kernel when each expert's scale tensor (N * K/32 bytes) is a
  * multiple of 16 bytes and at most 512 KiB and both byte buffers are 16-byte
- * aligned: a cluster of up to 8 CTAs per expert reads the scales once.
+ * aligned: a cluster of up to 16 CTAs per expert reads the scales once.
  * Otherwise two kernels (per-expert maximum into the workspace, then the
  * conversion).  Results are exact integers, identical from run to run.
  */
