@@ -370,8 +370,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
                                           const CUtensorMap &tm_act64, const Params &p,
                                           const float *ws2) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    // 1024-byte aligned start, derived from the shared array itself so that the
+    // compiler keeps the shared address space (shared loads, not generic ones).
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     int *roff = reinterpret_cast<int *>(smem + kOffRowOff);
     int *ioff = reinterpret_cast<int *>(smem + kOffItemOff);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBars);
