@@ -378,6 +378,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBars);
     uint64_t *code_full = bars;                          // TMA -> converters (+ issuers, split)
     uint64_t *code_empty = code_full + kCodeStagesMax;   // 16 converter warps (+ 4 commits, split)
+    // a_full / slot_empty: one barrier per warpgroup, covering its two A slots
+    // (the warpgroup fills both in one stage and they are consumed together).
     uint64_t *a_full = code_empty + kCodeStagesMax;      // converters -> issuer (4 warps)
     uint64_t *act_full = a_full + kSlotsMax;             // TMA -> issuer (single mode)
     uint64_t *slot_empty = act_full + kSlotsMax;         // MMA commit -> converters, act producer
@@ -538,8 +540,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
     const uint32_t acc_cols =
         split ? kIssuerWarps * part_cols : (wide ? static_cast<uint32_t>(kWideNT) : kAccCols);
     const uint32_t acol0 = nbuf * acc_cols;
-    // Activation-slot barriers the act producer waits on: the A-slot
-    // barriers in single mode (one slot ring for both), their own in wide mode.
+    // Activation-slot barriers the act producer waits on: the A-slot pair
+    // barriers in single mode (activation slot s is released with A slot s),
+    // their own in wide mode.
     uint64_t *act_free = wide ? act_empty : slot_empty;
     // Issuers splitting the token columns of an item (single and wide mode).
     const int n_iss = wide ? kWideIssuers : kSingleIssuers;
@@ -636,14 +639,17 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
                             al[h] = sl[h];
                             aph[h] = ph[h];
                         }
-                        ready = ready & mbar_try_wait(&a_full[sl[h]], ph[h]) &
-                                mbar_try_wait(&act_full[al[h]], aph[h]);
+                        // A slots come in pairs (slot 2w, 2w + 1 of warpgroup w), and a
+                        // group starts at an even slot: one barrier per pair.
+                        if ((h & 1) == 0) ready = ready & mbar_try_wait(&a_full[sl[h] >> 1], ph[h]);
+                        ready = ready & mbar_try_wait(&act_full[al[h]], aph[h]);
                     }
                     if (!__all_sync(0xffffffffu, ready)) {
 #pragma unroll
                         for (int h = 0; h < kGroupMax; ++h)
                             if (h < grp && ok &&
-                                (!warp_wait_bounded(&a_full[sl[h]], ph[h], abort_flag, p.status, lim) ||
+                                (((h & 1) == 0 &&
+                                  !warp_wait_bounded(&a_full[sl[h] >> 1], ph[h], abort_flag, p.status, lim)) ||
                                  !warp_wait_bounded(&act_full[al[h]], aph[h], abort_flag, p.status,
                                                     lim)))
                                 ok = false;
@@ -664,7 +670,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
                                 mma_bf16_ts(d_tmem, a_col + kk * 8,
                                             b0 + static_cast<uint64_t>(kk * 2), idesc,
                                             (kp == 0 && h == 0 && kk == 0) ? 0u : 1u);
-                            mma_commit(&slot_empty[sl[h]]);
+                            if (h & 1) mma_commit(&slot_empty[sl[h] >> 1]);
                             if (wide) mma_commit(&act_empty[al[h]]);
                         }
                         if (kp + grp >= KT) mma_commit(&acc_full[buf]);
@@ -688,14 +694,12 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
                         break;
                     }
                     const uint32_t s0 = 2u * w + 4u * sr.slot, par = sr.phase;   // sub-stage 2w at slot set
-                    // One probe for the three barriers (the usual case: all complete).
+                    // One probe for both barriers (the usual case: both complete).
                     const bool ready = __all_sync(
-                        0xffffffffu, mbar_try_wait(&a_full[s0], par) &
-                                         mbar_try_wait(&a_full[s0 + 1], par) &
+                        0xffffffffu, mbar_try_wait(&a_full[s0 >> 1], par) &
                                          mbar_try_wait(&code_full[ring.slot], ring.phase));
                     if (!ready &&
-                        (!warp_wait_bounded(&a_full[s0], par, abort_flag, p.status, lim) ||
-                         !warp_wait_bounded(&a_full[s0 + 1], par, abort_flag, p.status, lim) ||
+                        (!warp_wait_bounded(&a_full[s0 >> 1], par, abort_flag, p.status, lim) ||
                          !warp_wait_bounded(&code_full[ring.slot], ring.phase, abort_flag,
                                             p.status, lim))) {
                         ok = false;
@@ -715,8 +719,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
                                 mma_bf16_ts(d_tmem, a_col + kk * 8,
                                             b0 + static_cast<uint64_t>(kk * 2), idesc,
                                             (m == 0 && h == 0 && kk == 0) ? 0u : 1u);
-                            mma_commit(&slot_empty[s0 + h]);
                         }
+                        mma_commit(&slot_empty[s0 >> 1]);
                         mma_commit(&code_empty[ring.slot]);
                         if (m + 1 == KT / 4) mma_commit(&acc_full[buf]);
                     }
@@ -819,7 +823,10 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
             for (int i = 0; i < my_items && ok; ++i) {
                 const Item it = get_item(i);
                 for (int ks = 0; ks < KT; ++ks, r.next(n_act), ++issued) {
-                    if (!wait_bounded(&act_free[r.slot], r.phase ^ 1u, abort_flag, p.status, lim)) {
+                    // Single mode: activation slot s is free with A slot s, whose
+                    // barrier is shared with the other slot of its pair.
+                    if (!wait_bounded(wide ? &act_free[r.slot] : &act_free[r.slot >> 1], r.phase ^ 1u,
+                                      abort_flag, p.status, lim)) {
                         ok = false;
                         break;
                     }
@@ -979,6 +986,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
                 cw[ch][2] = v.z;
                 cw[ch][3] = v.w;
             }
+            // The ring slot is refilled by TMA (the async proxy) once released:
+            // order these generic-proxy reads of it before that write.
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
             if (lane == 0) mbar_arrive(&code_empty[code.slot]);
             if (!p.act_k8) {
@@ -1002,8 +1012,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
                 }
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             }
-            const bool slots_ready = mbar_test_wait(&slot_empty[slot0], sphase ^ 1u) &
-                                     mbar_test_wait(&slot_empty[slot0 + 1], sphase ^ 1u);
+            const bool slots_ready = mbar_test_wait(&slot_empty[wg], sphase ^ 1u);
             {
                 Ring nx = code;
                 nx.next(CS);
@@ -1016,9 +1025,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
             const uint32_t big = sw & ((sw & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) & 0x80808080u;
             const bool slow = !kNv && __any_sync(0xffffffffu, big != 0);
             if (!__all_sync(0xffffffffu, slots_ready) &&
-                (!warp_wait_bounded(&slot_empty[slot0], sphase ^ 1u, abort_flag, p.status, lim) ||
-                 !warp_wait_bounded(&slot_empty[slot0 + 1], sphase ^ 1u, abort_flag, p.status,
-                                    lim))) {
+                !warp_wait_bounded(&slot_empty[wg], sphase ^ 1u, abort_flag, p.status, lim)) {
                 ok = false;
                 break;
             }
@@ -1055,8 +1062,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(&a_full[slot0]);
-                mbar_arrive(&a_full[slot0 + 1]);
+                mbar_arrive(&a_full[wg]);
             }
             // Wide mode has one accumulator: the next item's first MMAs wait for
             // this item's epilogue.  The slots this pair fills next were last

@@ -227,3 +227,28 @@ def test_repeated_launches_are_bitwise_equal(B, bands, K, k8):
     c = rng.integers(0, 4096, 4000)
     ref, mag = oracle.grouped_gemm_sampled(act, codes, scales, gs, r, c)
     _tol_check(first.cpu().numpy()[r, c], ref, mag, what="repeated launches")
+
+
+@pytest.mark.parametrize("fused", [False, True], ids=["gemm", "fused_swiglu"])
+def test_many_ctas_sharing_weight_tiles_are_bitwise_repeatable(B, fused):
+    # One band of 12 full 256-token chunks first, so every CTA's first work
+    # item is a full wide item and up to five CTAs read the same weight tile
+    # at once: its code-ring refills then hit L2 and land within a few hundred
+    # cycles of the slot's release.  The converters' shared-memory reads of a
+    # slot must be ordered before that TMA write (a proxy fence); without it,
+    # on the full-size Zipf prefill, about one launch in a hundred had a few
+    # weight rows of one CTA's first item decoded wrongly.  150 launches must
+    # agree bit for bit, and the
+    # first must match the oracle on sampled elements.
+    act, codes, scales, gs = _explicit([3072, 40, 0, 300], 4096, 4096, seed=9)
+    d = Dev(B, act, codes, scales, gs, k8=True)
+    run = (lambda: d.fused(True)) if fused else d.gemm
+    first = run().clone()
+    diffs = [int((run() != first).sum()) for _ in range(150)]
+    assert not any(diffs), f"launches differing from the first: {[i for i, n in enumerate(diffs) if n]}"
+    if not fused:
+        rng = np.random.default_rng(2)
+        r = rng.integers(0, act.shape[0], 4000)
+        c = rng.integers(0, 4096, 4000)
+        ref, mag = oracle.grouped_gemm_sampled(act, codes, scales, gs, r, c)
+        _tol_check(first.cpu().numpy()[r, c], ref, mag, what="shared weight tiles")
