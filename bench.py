@@ -353,6 +353,59 @@ def run_formats(args, dev, wts, B, inputs, hbm, bf16):
         del wl, y
         torch.cuda.empty_cache()
     return res
+ROW_MAP_WORKLOADS = ("decode_T64", "prefill_T4096", "layer_T8192")
+
+
+def run_row_maps(args, dev, wts, B, inputs):
+    """The routing permutations fused into the grouped GEMMs, against the
+    default path: w13 + SwiGLU reading the route sort's gathered copy vs the
+    same launch gathering its rows from x (four-row TMA gathers,
+    moe_mxfp4_grouped_gemm_swiglu_gather), and w2 writing sorted rows vs slot
+    order (moe_mxfp4_grouped_gemm_scatter).  Milliseconds per launch (CUDA
+    events); outputs are checked bit for bit against the default path."""
+    import torch
+    K8 = B.MOE_ACT_K8_INTERLEAVED
+    stream = torch.cuda.current_stream(dev)
+    res = {}
+    for name in ROW_MAP_WORKLOADS:
+        wl = Workload(name, args.seed, dev, wts, B, inputs)
+        b = wl.bufs
+        ws = B.make_workspace(0, 1, 1, dev)
+        gs, _, ss, _, xs = B.route_sort(wl.ids, wl.E, wl.x, b.workspace,
+                                        out=(b.group_sizes, b.group_offsets, b.sorted_slot,
+                                             b.slot_to_row, b.x_sorted), x_layout=K8)
+        xk = B.act_interleave_k8(wl.x)
+        h2 = torch.empty_like(b.h)
+        y2s = torch.empty_like(b.y2)
+        calls = {
+            "w13_copy": lambda: B.grouped_gemm_swiglu(xs, wts["w13_codes"], wts["w13_scales"], gs,
+                                                      out=b.h, workspace=ws, act_layout=K8, h_layout=K8),
+            "w13_gather": lambda: B.grouped_gemm_swiglu_gather(xk, wl.k, ss, wts["w13_codes"],
+                                                               wts["w13_scales"], gs, out=h2,
+                                                               workspace=ws, h_layout=K8),
+            "w2_sorted": lambda: B.grouped_gemm(b.h, wts["w2_codes"], wts["w2_scales"], gs, out=b.y2,
+                                                workspace=ws, act_layout=K8),
+            "w2_slot_order": lambda: B.grouped_gemm_scatter(b.h, wts["w2_codes"], wts["w2_scales"], gs,
+                                                            ss, out=y2s, workspace=ws, act_layout=K8),
+        }
+        reps = 100 if wl.T <= 256 else 20
+        entry = {}
+        for key, fn in calls.items():
+            for _ in range(3):
+                fn()
+            entry[key + "_ms"] = round(time_launches(fn, reps, stream), 5)
+        entry["gather_equal"] = bool(torch.equal(h2, b.h))
+        entry["scatter_equal"] = bool(torch.equal(y2s[ss.long()], b.y2))
+        st = B.read_status(ws)
+        if st != B.MOE_OK or not (entry["gather_equal"] and entry["scatter_equal"]):
+            raise RuntimeError(f"{name}: row-map launches: {B.status_string(st)}, {entry}")
+        res[name] = entry
+        wl.free()
+        del wl, xk, h2, y2s
+        torch.cuda.empty_cache()
+    return res
+
+
 SUB_STEPS = {"decode_T64": 300, "decode_T256": 300, "prefill_T4096": 100, "layer_T8192": 60}
 SUSTAIN_S = 1.0          # the clock record covers at least this much back-to-back work
 
@@ -387,9 +440,10 @@ def run_ours(args, rank, world, local):
             del wl
             torch.cuda.empty_cache()
 
-    formats = {}
+    formats, row_maps = {}, {}
     if not args.no_sub_workloads and E_head == 256:
         formats = run_formats(args, dev, wts, B, inputs, hbm, bf16_burst)
+        row_maps = run_row_maps(args, dev, wts, B, inputs)
 
     # ---- the headline workload: exactly K timed steps
     wl = Workload(args.workload, args.seed + rank, dev, wts, B, inputs)
@@ -498,6 +552,7 @@ def run_ours(args, rank, world, local):
                       "w13_ms": round(w13_sus, 5), "seconds": round(n_sus * ms_sus * 1e-3, 3)},
         "workloads": subs,
         "w13_formats": formats,
+        "row_maps": row_maps,
         "e2e": {"value": round(whole_job_rate(flops, e2e_ms, world) / 1e12, 3), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "api": "moe_layer_forward with pinned host copies"},

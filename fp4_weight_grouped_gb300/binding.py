@@ -17,7 +17,7 @@ from . import build_lib
  MOE_ERR_CAPACITY) = range(7)
 MOE_ROUTE_SORT_NOALLOC_SCRATCH_BYTES = 512 * 1024
 MOE_F32, MOE_BF16 = 0, 1
-MOE_ACT_ROW_MAJOR, MOE_ACT_K8_INTERLEAVED = 0, 1
+MOE_ACT_ROW_MAJOR, MOE_ACT_K8_INTERLEAVED, MOE_ACT_K8_TOKEN_ORDER = 0, 1, 2
 
 SYMBOLS = (
     "moe_status_string", "moe_workspace_bytes", "moe_clear_status", "moe_read_status",
@@ -25,6 +25,8 @@ SYMBOLS = (
     "moe_mxfp4_decode_expert", "moe_debug_bounded_wait", "moe_last_launch_count",
     "moe_route_sort_noalloc", "moe_nvfp4_cast_workspace_bytes", "moe_mxfp4_to_nvfp4",
     "moe_nvfp4_grouped_gemm", "moe_mxfp4_grouped_gemm_swiglu", "moe_mxfp4_grouped_gemm_block",
+    "moe_mxfp4_grouped_gemm_swiglu_gather", "moe_mxfp4_grouped_gemm_scatter", "moe_combine_slots",
+    "moe_act_interleave_k8",
 )
 
 _lock = threading.Lock()
@@ -65,6 +67,12 @@ def load(path: str | None = None):
                                                   C.c_int, P, SZ, P], C.c_int),
                 "moe_mxfp4_grouped_gemm_swiglu": ([P, C.c_int, I64, I32, P, P, P, I32, I32, P,
                                                    C.c_int, P, SZ, P], C.c_int),
+                "moe_mxfp4_grouped_gemm_swiglu_gather": ([P, I32, I32, P, I64, I32, P, P, P, I32,
+                                                          I32, P, C.c_int, P, SZ, P], C.c_int),
+                "moe_mxfp4_grouped_gemm_scatter": ([P, C.c_int, I64, I32, P, P, P, I32, I32, P, P,
+                                                    C.c_int, P, SZ, P], C.c_int),
+                "moe_combine_slots": ([P, P, P, I32, I32, I32, P, C.c_int, P], C.c_int),
+                "moe_act_interleave_k8": ([P, I64, I32, P, P], C.c_int),
                 "moe_swiglu": ([P, C.c_int, I64, I32, P, C.c_int, P], C.c_int),
                 "moe_combine": ([P, P, P, I32, I32, I32, P, C.c_int, P], C.c_int),
                 "moe_layer_forward": ([P, P, P, I32, I32, I32, I32, I32, P, P, P, P, P,
@@ -144,7 +152,8 @@ def route_sort(topk_ids: torch.Tensor, E: int, x: torch.Tensor | None = None,
                workspace: torch.Tensor | None = None, out=None, stream=None,
                x_layout: int = MOE_ACT_ROW_MAJOR):
     """Returns (group_sizes[E], group_offsets[E+1], sorted_slot[T*k],
-    slot_to_row[T*k], x_sorted or None); x_sorted in `x_layout` order."""
+    slot_to_row[T*k], x_sorted or None); x_sorted in `x_layout` order
+    (MOE_ACT_K8_TOKEN_ORDER: x itself [T, hidden] in the K8 order)."""
     T, k = topk_ids.shape
     dev = topk_ids.device
     rows = T * k
@@ -153,7 +162,8 @@ def route_sort(topk_ids: torch.Tensor, E: int, x: torch.Tensor | None = None,
         off = torch.empty(E + 1, dtype=torch.int32, device=dev)
         ss = torch.empty(rows, dtype=torch.int32, device=dev)
         s2r = torch.empty(rows, dtype=torch.int32, device=dev)
-        xs = None if x is None else torch.empty((rows, x.shape[1]), dtype=x.dtype, device=dev)
+        xs_rows = T if x_layout == MOE_ACT_K8_TOKEN_ORDER else rows
+        xs = None if x is None else torch.empty((xs_rows, x.shape[1]), dtype=x.dtype, device=dev)
     else:
         gs, off, ss, s2r, xs = out
     if workspace is None:
@@ -245,6 +255,60 @@ def grouped_gemm_swiglu(act: torch.Tensor, codes: torch.Tensor, scales: torch.Te
     return out
 
 
+def grouped_gemm_swiglu_gather(x_k8: torch.Tensor, top_k: int, sorted_slot: torch.Tensor,
+                               codes: torch.Tensor, scales: torch.Tensor,
+                               group_sizes: torch.Tensor, out: torch.Tensor | None = None,
+                               workspace: torch.Tensor | None = None, stream=None,
+                               h_layout: int = MOE_ACT_ROW_MAJOR):
+    """grouped_gemm_swiglu with the activation rows gathered in the load: sorted
+    row r reads row sorted_slot[r] // top_k of x_k8 bf16 [T, K] (K8-interleaved);
+    -> h bf16 [rows, I], rows = sorted_slot.numel()."""
+    T, K = x_k8.shape
+    rows = sorted_slot.numel()
+    E, two_i, _ = codes.shape
+    I = two_i // 2
+    if out is None:
+        out = torch.empty((rows, I), dtype=torch.bfloat16, device=x_k8.device)
+    if workspace is None:
+        workspace = make_workspace(0, 1, 1, x_k8.device, stream)
+    rc = load().moe_mxfp4_grouped_gemm_swiglu_gather(
+        _ptr(x_k8), T, int(top_k), _ptr(sorted_slot), rows, K, _ptr(codes), _ptr(scales),
+        _ptr(group_sizes), E, I, _ptr(out), h_layout, _ptr(workspace), workspace.numel(),
+        _stream(stream))
+    _check(rc, "moe_mxfp4_grouped_gemm_swiglu_gather")
+    return out
+
+
+def grouped_gemm_scatter(act: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor,
+                         group_sizes: torch.Tensor, out_row: torch.Tensor,
+                         out: torch.Tensor | None = None, out_dtype=torch.float32,
+                         workspace: torch.Tensor | None = None, stream=None,
+                         act_layout: int = MOE_ACT_ROW_MAJOR):
+    """grouped_gemm writing sorted row r to row out_row[r] of out [rows, N]."""
+    rows, K = act.shape
+    E, N, _ = codes.shape
+    if out is None:
+        out = torch.empty((rows, N), dtype=out_dtype, device=act.device)
+    if workspace is None:
+        workspace = make_workspace(0, 1, 1, act.device, stream)
+    rc = load().moe_mxfp4_grouped_gemm_scatter(_ptr(act), act_layout, rows, K, _ptr(codes),
+                                               _ptr(scales), _ptr(group_sizes), E, N,
+                                               _ptr(out_row), _ptr(out), _dtype_code(out.dtype),
+                                               _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "moe_mxfp4_grouped_gemm_scatter")
+    return out
+
+
+def act_interleave_k8(x: torch.Tensor, out: torch.Tensor | None = None, stream=None):
+    """bf16 [rows, hidden] -> the same rows in the K8-interleaved order."""
+    rows, hidden = x.shape
+    if out is None:
+        out = torch.empty_like(x)
+    rc = load().moe_act_interleave_k8(_ptr(x), rows, hidden, _ptr(out), _stream(stream))
+    _check(rc, "moe_act_interleave_k8")
+    return out
+
+
 def nvfp4_grouped_gemm(act: torch.Tensor, codes: torch.Tensor, scales16: torch.Tensor,
                        weight_scale_2: torch.Tensor, group_sizes: torch.Tensor,
                        out: torch.Tensor | None = None, out_dtype=torch.float32,
@@ -287,6 +351,19 @@ def combine(y: torch.Tensor, slot_to_row: torch.Tensor, topk_w: torch.Tensor,
     rc = load().moe_combine(_ptr(y), _ptr(slot_to_row), _ptr(topk_w), T, k, N, _ptr(out),
                             _dtype_code(out.dtype), _stream(stream))
     _check(rc, "moe_combine")
+    return out
+
+
+def combine_slots(y: torch.Tensor, slot_to_row: torch.Tensor, topk_w: torch.Tensor,
+                  out: torch.Tensor | None = None, out_dtype=torch.float32, stream=None):
+    """combine with y f32 [T*k, N] in slot order (slot_to_row marks valid slots)."""
+    T, k = topk_w.shape
+    N = y.shape[1]
+    if out is None:
+        out = torch.empty((T, N), dtype=out_dtype, device=y.device)
+    rc = load().moe_combine_slots(_ptr(y), _ptr(slot_to_row), _ptr(topk_w), T, k, N, _ptr(out),
+                                  _dtype_code(out.dtype), _stream(stream))
+    _check(rc, "moe_combine_slots")
     return out
 
 

@@ -72,7 +72,9 @@ moe_status check_route_args(const int32_t *ids, int32_t T, int32_t k, int32_t E,
     if (!gs || !off || !workspace) return MOE_ERR_INVALID_ARG;
     if (T > 0 && (!ids || !ss || !s2r)) return MOE_ERR_INVALID_ARG;
     if ((x == nullptr) != (xs == nullptr)) return MOE_ERR_INVALID_ARG;
-    if (layout != MOE_ACT_ROW_MAJOR && layout != MOE_ACT_K8_INTERLEAVED) return MOE_ERR_INVALID_ARG;
+    if (layout != MOE_ACT_ROW_MAJOR && layout != MOE_ACT_K8_INTERLEAVED &&
+        layout != MOE_ACT_K8_TOKEN_ORDER)
+        return MOE_ERR_INVALID_ARG;
     if (x && (hidden <= 0 || hidden % 8 != 0 || !aligned(x, 16) || !aligned(xs, 16)))
         return MOE_ERR_INVALID_ARG;
     if (!aligned(workspace, 16) || workspace_bytes < moe_workspace_bytes(T, k, E))
@@ -133,12 +135,13 @@ moe_status moe_route_sort(const int32_t *topk_ids, int32_t T, int32_t k, int32_t
     int sms = 0;
     if ((st = current_device(&sms)) != MOE_OK) return st;
     int launches = 0;
+    const bool tokens = x_sorted_layout == MOE_ACT_K8_TOKEN_ORDER;
     st = moe::launch_route_sort(topk_ids, T, k, E, group_sizes, group_offsets, sorted_slot,
-                                slot_to_row, x, hidden, x_sorted,
+                                slot_to_row, x, hidden, tokens ? nullptr : x_sorted,
                                 x_sorted_layout == MOE_ACT_K8_INTERLEAVED,
                                 static_cast<uint8_t *>(workspace) + kStatusBytes,
                                 status_word(workspace), static_cast<cudaStream_t>(stream),
-                                &launches);
+                                &launches, tokens ? x_sorted : nullptr);
     g_last_launches = launches;
     return st;
 }
@@ -235,6 +238,52 @@ moe_status moe_mxfp4_grouped_gemm_swiglu(const uint16_t *act, moe_act_layout act
     return st;
 }
 
+moe_status moe_mxfp4_grouped_gemm_swiglu_gather(const uint16_t *x_k8, int32_t T, int32_t top_k,
+                                                const int32_t *sorted_slot, int64_t rows, int32_t K,
+                                                const uint8_t *codes, const uint8_t *scales,
+                                                const int32_t *group_sizes, int32_t E, int32_t I,
+                                                uint16_t *h, moe_act_layout h_layout,
+                                                void *workspace, size_t workspace_bytes,
+                                                void *stream) {
+    if (I <= 0 || I % 16 != 0 || static_cast<int64_t>(I) * 2 > INT32_MAX) return MOE_ERR_INVALID_ARG;
+    if (T < 0 || top_k <= 0 || (rows > 0 && (T == 0 || !sorted_slot))) return MOE_ERR_INVALID_ARG;
+    moe_status st = check_gemm_args(x_k8, MOE_ACT_K8_INTERLEAVED, rows, K, codes, scales,
+                                    group_sizes, E, 2 * I, h, MOE_BF16, workspace, workspace_bytes);
+    if (st != MOE_OK) return st;
+    if (h_layout != MOE_ACT_ROW_MAJOR && (h_layout != MOE_ACT_K8_INTERLEAVED || I % 8 != 0))
+        return MOE_ERR_INVALID_ARG;
+    int sms = 0;
+    if ((st = current_device(&sms)) != MOE_OK) return st;
+    st = moe::launch_grouped_gemm_swiglu_gather(x_k8, T, top_k, sorted_slot, static_cast<int>(rows), K,
+                                                codes, scales, group_sizes, E, 2 * I, h,
+                                                h_layout == MOE_ACT_K8_INTERLEAVED,
+                                                status_word(workspace), kWaitLimitNs,
+                                                static_cast<cudaStream_t>(stream), sms);
+    g_last_launches = rows > 0 ? moe::kGemmLaunches : 0;
+    return st;
+}
+
+moe_status moe_mxfp4_grouped_gemm_scatter(const uint16_t *act, moe_act_layout act_layout,
+                                          int64_t rows, int32_t K, const uint8_t *codes,
+                                          const uint8_t *scales, const int32_t *group_sizes,
+                                          int32_t E, int32_t N, const int32_t *out_row, void *out,
+                                          moe_dtype out_dtype, void *workspace,
+                                          size_t workspace_bytes, void *stream) {
+    moe_status st = check_gemm_args(act, act_layout, rows, K, codes, scales, group_sizes, E, N,
+                                    out, out_dtype, workspace, workspace_bytes);
+    if (st != MOE_OK) return st;
+    if (rows > 0 && !out_row) return MOE_ERR_INVALID_ARG;
+    int sms = 0;
+    if ((st = current_device(&sms)) != MOE_OK) return st;
+    st = moe::launch_grouped_gemm_scatter(act, static_cast<int>(rows), K, codes, scales, group_sizes,
+                                          E, N, out_row, out, out_dtype == MOE_BF16,
+                                          act_layout == MOE_ACT_K8_INTERLEAVED,
+                                          status_word(workspace), kWaitLimitNs,
+                                          static_cast<cudaStream_t>(stream), sms);
+    g_last_launches = rows > 0 ? moe::kGemmLaunches : 0;
+    return st;
+}
+
 moe_status moe_nvfp4_grouped_gemm(const uint16_t *act, moe_act_layout act_layout, int64_t rows,
                                   int32_t K, const uint8_t *codes, const uint8_t *scales16,
                                   const float *weight_scale_2, const int32_t *group_sizes,
@@ -286,6 +335,36 @@ moe_status moe_combine(const float *y, const int32_t *slot_to_row, const float *
     st = moe::launch_combine(y, slot_to_row, topk_w, T, k, N, out, out_dtype == MOE_BF16,
                              static_cast<cudaStream_t>(stream), sms);
     g_last_launches = T > 0 ? 1 : 0;
+    return st;
+}
+
+moe_status moe_combine_slots(const float *y, const int32_t *slot_to_row, const float *topk_w,
+                             int32_t T, int32_t k, int32_t N, void *out, moe_dtype out_dtype,
+                             void *stream) {
+    if (T < 0 || k <= 0 || N <= 0 || (out_dtype != MOE_F32 && out_dtype != MOE_BF16))
+        return MOE_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(T) * k > INT32_MAX) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!y || !slot_to_row || !topk_w || !out || !aligned(y, 16) || !aligned(out, 16)))
+        return MOE_ERR_INVALID_ARG;
+    int sms = 0;
+    moe_status st = current_device(&sms);
+    if (st != MOE_OK) return st;
+    st = moe::launch_combine(y, slot_to_row, topk_w, T, k, N, out, out_dtype == MOE_BF16,
+                             static_cast<cudaStream_t>(stream), sms, 1);
+    g_last_launches = T > 0 ? 1 : 0;
+    return st;
+}
+
+moe_status moe_act_interleave_k8(const uint16_t *x, int64_t rows, int32_t hidden, uint16_t *x_k8,
+                                 void *stream) {
+    if (rows < 0 || hidden <= 0 || hidden % 8 != 0) return MOE_ERR_INVALID_ARG;
+    if (rows > 0 && (!x || !x_k8 || !aligned(x, 16) || !aligned(x_k8, 16)))
+        return MOE_ERR_INVALID_ARG;
+    int sms = 0;
+    moe_status st = current_device(&sms);
+    if (st != MOE_OK) return st;
+    st = moe::launch_interleave_k8(x, rows, hidden, x_k8, static_cast<cudaStream_t>(stream), sms);
+    g_last_launches = rows > 0 ? 1 : 0;
     return st;
 }
 

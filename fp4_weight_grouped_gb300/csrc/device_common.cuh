@@ -168,6 +168,20 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// Gather of four rows r0..r3 of a 2-D tensor, columns [x, x + box width), into
+// four consecutive rows of shared memory at dst (tile::gather4; the map's box
+// is one row high).  Rows outside the tensor read the fill value (zero).
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *map, int32_t x,
+                                            int32_t r0, int32_t r1, int32_t r2, int32_t r3,
+                                            uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
+        "r"(smem_u32(bar))
+        : "memory");
+}
+
 // 5-D tiled load of one box into shared memory (x innermost, then d1 .. d4).
 __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map, int32_t x,
                                             int32_t d1, int32_t d2, int32_t d3, int32_t d4,

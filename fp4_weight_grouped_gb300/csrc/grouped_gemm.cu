@@ -152,8 +152,45 @@ struct Params {
     // longer ones (single or wide mode), so a mix of short and long bands
     // runs each in the mode made for it.
     int band_lo, band_hi;
+    // Activation gather (the routing permutation fused into the activation
+    // load; the kGather instantiation): sorted row r reads row gather_slot[r] /
+    // gather_k of a [act_rows, K] activation tensor, four rows per TMA (tm_act
+    // and tm_act64 are then one-row gather maps).
+    const int32_t *gather_slot;
+    int gather_k;
+    int act_rows;
+    // Output scatter (the kScatter instantiation): sorted row r is written to
+    // row out_row[r] of the output; an entry outside [0, rows) is skipped and
+    // recorded as MOE_ERR_DATA.
+    const int32_t *out_row;
     uint64_t wait_limit_ns;
 };
+
+// Row maps of a launch: none, the activation gather, or the output scatter.
+// Each is its own kernel instantiation, so the plain kernels carry no trace of
+// the other two.
+enum RowMap { kMapNone = 0, kMapGather = 1, kMapScatter = 2 };
+
+// Activation row of sorted row r under the gather: gather_slot[r] / gather_k,
+// clamped into [0, act_rows) (a row outside records MOE_ERR_DATA).
+__device__ __forceinline__ int gather_row(const Params &p, int r) {
+    const int a = __ldg(p.gather_slot + r) / p.gather_k;
+    if (a < 0 || a >= p.act_rows) {
+        set_status(p.status, MOE_ERR_DATA);
+        return a < 0 ? 0 : p.act_rows - 1;
+    }
+    return a;
+}
+
+// Scatter: output row of sorted row r, or -1 (recorded) when out of range.
+__device__ __forceinline__ int scatter_row(const Params &p, int r) {
+    const int o = __ldg(p.out_row + r);
+    if (o < 0 || o >= p.rows) {
+        set_status(p.status, MOE_ERR_DATA);
+        return -1;
+    }
+    return o;
+}
 
 struct Item {
     int e, row0, nvalid, nt, n0;
@@ -214,13 +251,20 @@ struct Ring {
 // SwiGLU: lanes l and l ^ 16 of a warp hold the gate and up sums of the same
 // output column, so one shuffle pairs them; lanes 0-15 finish token c, lanes
 // 16-31 token c + 1, and h is written as bf16.
-template <bool kNv>
+// kScatter: token t of the item goes to output row out_row[row0 + t]; lane l
+// holds that row for column wg * qc + l (qc <= 32) and shuffles it out.
+template <bool kNv, bool kScatter>
 __device__ __forceinline__ void store_item(const Params &p, const Item &it, uint32_t acc_base,
                                            int wg, int row, bool split, uint32_t part_cols,
                                            float tensor_scale) {
     const int qc = it.nt >> 2;                 // columns per warpgroup (multiple of 4)
     const bool up_lane = swiglu_row_is_up(row);
     const int n = p.swiglu ? it.n0 + swiglu_row_offset(row) : it.n0 + row;
+    int my_orow = -1;
+    if constexpr (kScatter) {
+        const int t = wg * qc + (threadIdx.x & 31);
+        if ((threadIdx.x & 31) < qc && t < it.nvalid) my_orow = scatter_row(p, it.row0 + t);
+    }
     for (int c = wg * qc; c < (wg + 1) * qc; c += 4) {
         uint32_t v[4];
         __syncwarp();
@@ -251,19 +295,23 @@ __device__ __forceinline__ void store_item(const Params &p, const Item &it, uint
                 const float g = up_lane ? recv : a0;
                 const float u = up_lane ? a1 : recv;
                 const int tok = c + 2 * pr + (up_lane ? 1 : 0);
-                if (n < p.I && tok < it.nvalid) {
+                int orow = it.row0 + tok;
+                if constexpr (kScatter) orow = __shfl_sync(0xffffffffu, my_orow, tok - wg * qc);
+                if (n < p.I && tok < it.nvalid && (!kScatter || orow >= 0)) {
                     const int col = p.h_k8 ? k8_position(n) : n;
-                    const size_t off = static_cast<size_t>(it.row0 + tok) * p.I + col;
+                    const size_t off = static_cast<size_t>(orow) * p.I + col;
                     reinterpret_cast<__nv_bfloat16 *>(p.out)[off] =
                         __float2bfloat16_rn(silu_f32(g) * u);
                 }
             }
-        } else if (n < p.N) {
+        } else if (kScatter || n < p.N) {     // scatter: every lane takes part in the shuffles
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
                 const int tok = c + t;
-                if (tok < it.nvalid) {
-                    const size_t off = static_cast<size_t>(it.row0 + tok) * p.N + n;
+                int orow = it.row0 + tok;
+                if constexpr (kScatter) orow = __shfl_sync(0xffffffffu, my_orow, tok - wg * qc);
+                if ((!kScatter || n < p.N) && tok < it.nvalid && (!kScatter || orow >= 0)) {
+                    const size_t off = static_cast<size_t>(orow) * p.N + n;
                     if (p.out_bf16)
                         reinterpret_cast<__nv_bfloat16 *>(p.out)[off] = __float2bfloat16_rn(f[t]);
                     else
@@ -278,13 +326,31 @@ __device__ __forceinline__ void store_item(const Params &p, const Item &it, uint
 // warpgroup): the columns are read 16 at a time (one load, one wait), so at
 // most four load latencies are exposed per warp instead of one per four
 // columns.  The caller releases the accumulator afterwards.
-template <bool kNv>
+// kScatter: as in store_item, with up to 64 columns a warpgroup (two rows a lane).
+template <bool kNv, bool kScatter>
 __device__ __forceinline__ void store_item_wide(const Params &p, const Item &it, uint32_t acc_base,
                                                 int wg, int row, float tensor_scale) {
     const int qc = it.nt >> 2;                 // columns of this warpgroup: <= 64, multiple of 4
     const int cb = wg * qc;
     const bool up_lane = swiglu_row_is_up(row);
     const int n = p.swiglu ? it.n0 + swiglu_row_offset(row) : it.n0 + row;
+    int orow_lo = -1, orow_hi = -1;            // scatter: rows of columns cb + lane, cb + 32 + lane
+    if constexpr (kScatter) {
+        const int l = threadIdx.x & 31;
+        if (l < qc && cb + l < it.nvalid) orow_lo = scatter_row(p, it.row0 + cb + l);
+        if (32 + l < qc && cb + 32 + l < it.nvalid) orow_hi = scatter_row(p, it.row0 + cb + 32 + l);
+    }
+    // Output row of token column tok (the warp executes it together).
+    auto out_row_of = [&](int tok) -> int {
+        if constexpr (kScatter) {
+            const int rel = tok - cb;
+            const int lo = __shfl_sync(0xffffffffu, orow_lo, rel & 31);
+            const int hi = __shfl_sync(0xffffffffu, orow_hi, rel & 31);
+            return rel < 32 ? lo : hi;
+        } else {
+            return it.row0 + tok;
+        }
+    };
     for (int c16 = 0; c16 < qc; c16 += 16) {
         uint32_t v[16];
         __syncwarp();
@@ -305,17 +371,19 @@ __device__ __forceinline__ void store_item_wide(const Params &p, const Item &it,
                     const float g = up_lane ? recv : a0;
                     const float u = up_lane ? a1 : recv;
                     const int tok = cb + col + (up_lane ? 1 : 0);
-                    if (n < p.I && tok < it.nvalid) {
+                    const int orow = out_row_of(tok);
+                    if (n < p.I && tok < it.nvalid && (!kScatter || orow >= 0)) {
                         const int hc = p.h_k8 ? k8_position(n) : n;
-                        reinterpret_cast<__nv_bfloat16 *>(p.out)[static_cast<size_t>(it.row0 + tok) * p.I + hc] =
+                        reinterpret_cast<__nv_bfloat16 *>(p.out)[static_cast<size_t>(orow) * p.I + hc] =
                             __float2bfloat16_rn(silu_f32(g) * u);
                     }
-                } else if (n < p.N) {
+                } else if (kScatter || n < p.N) {   // scatter: every lane takes part in the shuffles
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const int tok = cb + col + e;
-                        if (tok < it.nvalid) {
-                            const size_t off = static_cast<size_t>(it.row0 + tok) * p.N + n;
+                        const int orow = out_row_of(tok);
+                        if ((!kScatter || n < p.N) && tok < it.nvalid && (!kScatter || orow >= 0)) {
+                            const size_t off = static_cast<size_t>(orow) * p.N + n;
                             const float val = e ? a1 : a0;
                             if (p.out_bf16)
                                 reinterpret_cast<__nv_bfloat16 *>(p.out)[off] = __float2bfloat16_rn(val);
@@ -364,7 +432,7 @@ __device__ __forceinline__ void decode16_scaled(uint32_t c0, uint32_t c1, uint32
 // launch for bands of at most 32 rows (split mode only); otherwise the launch
 // for longer bands (single or wide mode).  Separate instantiations keep each
 // mode's loops free of the other modes' code.
-template <bool kNv, bool kSplit>
+template <bool kNv, bool kSplit, int kMap>
 __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUtensorMap &tm_act,
                                           const CUtensorMap &tm_act3, const CUtensorMap &tm_scales,
                                           const CUtensorMap &tm_act64, const Params &p,
@@ -746,6 +814,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
         // <= 16 rows and K % 256 == 0 it is one 3-D box (16 rows x 4 x 64 k,
         // stored as four 64-k tiles), else 2-D boxes of 16 rows x 64 k.
         const bool use3d = p.act3d && narrow;    // one 16-row group per code stage
+        constexpr bool gather = kMap == kMapGather;
         if (lane == 0) {
             tma_prefetch_map(&tm_codes);
             if (split) tma_prefetch_map(use3d ? &tm_act3 : &tm_act);
@@ -764,6 +833,12 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
         for (int i = 0; i < my_items && ok; ++i) {
             const Item it = get_item(i);
             const int y = it.e * p.N + it.n0;
+            // Gather (split mode, nt <= 32): lane l holds the activation row of
+            // the item's row l; rows past the band repeat its first row (their
+            // outputs are never written).
+            int act_row = 0;
+            if constexpr (split && gather)
+                act_row = gather_row(p, it.row0 + (lane < it.nvalid ? lane : 0));
             for (int kc = 0; kc < KT / 4; ++kc, r.next(CS), ++issued) {
                 if (!warp_wait_bounded(&code_empty[r.slot], r.phase ^ 1u, abort_flag, p.status,
                                        lim)) {
@@ -790,7 +865,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
                         if (scales_here)
                             tma_load_2d(dst + scale_off, &tm_scales, sx, y, &code_full[r.slot]);
                     }
-                    if (split) {
+                    if (split && !gather) {
                         for (int grp = 0; grp < it.nt / 16; ++grp) {
                             if (use3d) {
                                 tma_load_3d(dst + kCodeStageBytes + grp * 2048, &tm_act3, 0,
@@ -806,12 +881,76 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
                     }
                 }
                 __syncwarp();
+                if constexpr (split && gather) {
+                    // Lane l < nt / 4 gathers rows 4l .. 4l + 3 of the four 64-k
+                    // sub-stages (after the elected lane's expect_tx above).
+                    const int q = 4 * (lane & 7);
+                    const int r0 = __shfl_sync(0xffffffffu, act_row, q);
+                    const int r1 = __shfl_sync(0xffffffffu, act_row, q + 1);
+                    const int r2 = __shfl_sync(0xffffffffu, act_row, q + 2);
+                    const int r3 = __shfl_sync(0xffffffffu, act_row, q + 3);
+                    if (lane < it.nt / 4) {
+                        const uint32_t dst = code_smem + r.slot * ring_stage_bytes + kCodeStageBytes +
+                                             static_cast<uint32_t>(lane) * 512u;
+                        for (int sub = 0; sub < 4; ++sub)
+                            tma_gather4(dst + sub * act_stage_bytes, &tm_act, kc * kCodeK + sub * kStageK,
+                                        r0, r1, r2, r3, &code_full[r.slot]);
+                    }
+                    __syncwarp();
+                }
             }
         }
         if (!ok && lane == 0) {   // drain: every issued copy must land before the CTA exits
             const uint32_t first = issued > CS ? issued - CS : 0;
             for (uint32_t h = first; h < issued; ++h)
                 wait_bounded(&code_full[h % CS], (h / CS) & 1u, nullptr, p.status, lim);
+        }
+    } else if (warp == kActWarp && kMap == kMapGather) {
+        // ------------------- activation producer with the gather (single, wide)
+        // Lane 0 waits for the slot and posts the byte count; lane l then gathers
+        // rows 8l .. 8l + 7 of the item with two four-row TMA gathers.
+        if (!split) {
+            if (lane == 0) tma_prefetch_map(&tm_act64);
+            Ring r;
+            uint32_t issued = 0;
+            bool ok = true;
+            for (int i = 0; i < my_items && ok; ++i) {
+                const Item it = get_item(i);
+                int ar[8] = {0, 0, 0, 0, 0, 0, 0, 0};   // activation rows of rows 8l .. 8l + 7
+                if (8 * lane < it.nt) {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const int rr = 8 * lane + q;   // rows past the band repeat its first row
+                        ar[q] = gather_row(p, it.row0 + (rr < it.nvalid ? rr : 0));
+                    }
+                }
+                for (int ks = 0; ks < KT; ++ks, r.next(n_act), ++issued) {
+                    int free_ok = 1;
+                    if (lane == 0) {
+                        free_ok = wait_bounded(wide ? &act_free[r.slot] : &act_free[r.slot >> 1],
+                                               r.phase ^ 1u, abort_flag, p.status, lim);
+                        if (free_ok)
+                            mbar_arrive_expect_tx(&act_full[r.slot], static_cast<uint32_t>(it.nt) * 128u);
+                    }
+                    if (!__shfl_sync(0xffffffffu, free_ok, 0)) {
+                        ok = false;
+                        break;
+                    }
+                    if (8 * lane < it.nt) {   // nt is a multiple of 16: all eight rows exist
+                        const uint32_t d = act_smem + r.slot * act_stage_bytes +
+                                           static_cast<uint32_t>(lane) * 1024u;
+                        tma_gather4(d, &tm_act64, ks * kStageK, ar[0], ar[1], ar[2], ar[3],
+                                    &act_full[r.slot]);
+                        tma_gather4(d + 512u, &tm_act64, ks * kStageK, ar[4], ar[5], ar[6], ar[7],
+                                    &act_full[r.slot]);
+                    }
+                }
+            }
+            if (!ok && lane == 0) {   // drain: every issued copy must land before the CTA exits
+                const uint32_t first = issued > n_act ? issued - n_act : 0;
+                for (uint32_t h = first; h < issued; ++h)
+                    wait_bounded(&act_full[h % n_act], (h / n_act) & 1u, nullptr, p.status, lim);
+            }
         }
     } else if (warp == kActWarp) {
         // ------------------------------------- activation producer (single mode)
@@ -921,9 +1060,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
             const Item it = get_item(i);
             const float ts = kNv ? __ldg(ws2 + it.e) : 0.0f;
             if (wide)
-                store_item_wide<kNv>(p, it, tmem_base + lane_off, wg, row, ts);
+                store_item_wide<kNv, kMap == kMapScatter>(p, it, tmem_base + lane_off, wg, row, ts);
             else
-                store_item<kNv>(p, it, tmem_base + lane_off + buf * acc_cols, wg, row, split,
+                store_item<kNv, kMap == kMapScatter>(p, it, tmem_base + lane_off + buf * acc_cols, wg, row, split,
                                 part_cols, ts);
             tc_fence_before();
             __syncwarp();
@@ -1108,14 +1247,14 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
     }
 }
 
-template <bool kSplit>
+template <bool kSplit, int kMap>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
                     const __grid_constant__ CUtensorMap tm_act,
                     const __grid_constant__ CUtensorMap tm_act3,
                     const __grid_constant__ CUtensorMap tm_scales,
                     const __grid_constant__ CUtensorMap tm_act64, const Params p) {
-    gemm_body<false, kSplit>(tm_codes, tm_act, tm_act3, tm_scales, tm_act64, p, nullptr);
+    gemm_body<false, kSplit, kMap>(tm_codes, tm_act, tm_act3, tm_scales, tm_act64, p, nullptr);
 }
 
 template <bool kSplit>
@@ -1126,7 +1265,7 @@ grouped_gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tm_codes,
                           const __grid_constant__ CUtensorMap tm_scales,
                           const __grid_constant__ CUtensorMap tm_act64, const Params p,
                           const float *__restrict__ ws2) {
-    gemm_body<true, kSplit>(tm_codes, tm_act, tm_act3, tm_scales, tm_act64, p, ws2);
+    gemm_body<true, kSplit, kMapNone>(tm_codes, tm_act, tm_act3, tm_scales, tm_act64, p, ws2);
 }
 
 // Debug view of the decode: one thread per (weight row n, 32-element block); the
@@ -1193,12 +1332,18 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
 // swiglu: N = 2 * I weight rows ([gate | up]); `out` is h, bf16 [rows, I], in
 // the K8-interleaved order when h_k8.
 // scale_block (MXFP4): consecutive k per E8M0 scale byte, 32 or 512.
-template <bool kNv>
+// kMap == kMapGather: sorted row r reads activation row gather_slot[r] /
+// gather_k of act [act_rows, K] (K8-interleaved).  kMap == kMapScatter: sorted
+// row r is written to output row out_row[r].
+template <bool kNv, int kMap = gemm::kMapNone>
 static moe_status launch_gemm(const uint16_t *act, int rows, int K, const uint8_t *codes,
                               const uint8_t *scales, const float *ws2, const int32_t *group_sizes,
                               int E, int N, void *out, int out_bf16, int act_k8, int swiglu,
                               int h_k8, int *status, uint64_t wait_limit_ns, cudaStream_t stream,
-                              int num_sms, int scale_block = 32) {
+                              int num_sms, int scale_block = 32,
+                              const int32_t *gather_slot = nullptr, int gather_k = 1,
+                              int act_rows = 0, const int32_t *out_row = nullptr) {
+    static_assert(!kNv || kMap == gemm::kMapNone, "row maps are built for MXFP4 only");
     using namespace gemm;
     if (rows == 0) return MOE_OK;
     const int I = N / 2;   // fused SwiGLU: gate rows [0, I), up rows [I, 2I); I % 16 == 0
@@ -1239,10 +1384,14 @@ static moe_status launch_gemm(const uint16_t *act, int rows, int K, const uint8_
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return MOE_ERR_CUDA;
     }
+    // Activation boxes of 64 k by 16 rows (split mode) and by 64 rows (single
+    // and wide mode); with the gather both maps are one row high (gather4).
+    constexpr bool gather = kMap == kMapGather;
+    const cuuint64_t map_rows = static_cast<cuuint64_t>(gather ? act_rows : rows);
     {
-        cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+        cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), map_rows};
         cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-        cuuint32_t box[2] = {64, 16};
+        cuuint32_t box[2] = {64, gather ? 1u : 16u};
         cuuint32_t estr[2] = {1, 1};
         if (encode(&tm_act, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(act), dims,
                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -1251,9 +1400,9 @@ static moe_status launch_gemm(const uint16_t *act, int rows, int K, const uint8_
             return MOE_ERR_CUDA;
     }
     {   // 64-row boxes for wide bands
-        cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+        cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), map_rows};
         cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-        cuuint32_t box[2] = {64, 64};
+        cuuint32_t box[2] = {64, gather ? 1u : 64u};
         cuuint32_t estr[2] = {1, 1};
         if (encode(&tm_act64, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(act), dims,
                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -1263,7 +1412,7 @@ static moe_status launch_gemm(const uint16_t *act, int rows, int K, const uint8_
     }
     // The same activations seen as [K/64 chunks][rows][64]: one box holds 16
     // rows x 4 chunks and lands as four consecutive 64-k tiles of 16 rows.
-    const int act3d = (K % kCodeK) == 0;
+    const int act3d = (K % kCodeK) == 0 && !gather;
     if (act3d) {
         cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(K / 64)};
         cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, 128};
@@ -1305,7 +1454,7 @@ static moe_status launch_gemm(const uint16_t *act, int rows, int K, const uint8_
     }
     // Devices (0..63) whose shared-memory attribute is set (one mask per format);
     // others set it on every call.
-    static std::atomic<uint64_t> attr_dev_mask{0};
+    static std::atomic<uint64_t> attr_dev_mask{0};   // one per instantiation
     const int smem_bytes = kNv ? kSmemBytesNv : kSmemBytes;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
@@ -1315,8 +1464,8 @@ static moe_status launch_gemm(const uint16_t *act, int rows, int K, const uint8_
         const bool ok =
             kNv ? cudaFuncSetAttribute(grouped_gemm_nvfp4_kernel<true>, a, smem_bytes) == cudaSuccess &&
                       cudaFuncSetAttribute(grouped_gemm_nvfp4_kernel<false>, a, smem_bytes) == cudaSuccess
-                : cudaFuncSetAttribute(grouped_gemm_kernel<true>, a, smem_bytes) == cudaSuccess &&
-                      cudaFuncSetAttribute(grouped_gemm_kernel<false>, a, smem_bytes) == cudaSuccess;
+                : cudaFuncSetAttribute(grouped_gemm_kernel<true, kMap>, a, smem_bytes) == cudaSuccess &&
+                      cudaFuncSetAttribute(grouped_gemm_kernel<false, kMap>, a, smem_bytes) == cudaSuccess;
         if (!ok) return MOE_ERR_CUDA;
         attr_dev_mask.fetch_or(dev_bit, std::memory_order_release);
     }
@@ -1345,6 +1494,10 @@ static moe_status launch_gemm(const uint16_t *act, int rows, int K, const uint8_
     p.act_k8 = act_k8;
     p.act3d = act3d;
     p.scale_tma = scale_tma;
+    p.gather_slot = gather_slot;
+    p.gather_k = gather_k;
+    p.act_rows = act_rows;
+    p.out_row = out_row;
     // Two launches: bands of 1..32 rows, then bands of 33 or more (a launch
     // whose class has no band returns from its prologue).
     for (int cls = 0; cls < 2; ++cls) {
@@ -1359,10 +1512,10 @@ static moe_status launch_gemm(const uint16_t *act, int rows, int K, const uint8_
                     tm_codes, tm_act, tm_act3, tm_scales, tm_act64, p, ws2);
         } else {
             if (cls == 0)
-                grouped_gemm_kernel<true><<<num_sms, kThreads, smem_bytes, stream>>>(
+                grouped_gemm_kernel<true, kMap><<<num_sms, kThreads, smem_bytes, stream>>>(
                     tm_codes, tm_act, tm_act3, tm_scales, tm_act64, p);
             else
-                grouped_gemm_kernel<false><<<num_sms, kThreads, smem_bytes, stream>>>(
+                grouped_gemm_kernel<false, kMap><<<num_sms, kThreads, smem_bytes, stream>>>(
                     tm_codes, tm_act, tm_act3, tm_scales, tm_act64, p);
         }
         if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
@@ -1394,6 +1547,27 @@ moe_status launch_grouped_gemm_swiglu(const uint16_t *act, int rows, int K, cons
                                       uint64_t wait_limit_ns, cudaStream_t stream, int num_sms) {
     return launch_gemm<false>(act, rows, K, codes, scales, nullptr, group_sizes, E, N, h, 1,
                               act_k8, 1, h_k8, status, wait_limit_ns, stream, num_sms);
+}
+
+moe_status launch_grouped_gemm_swiglu_gather(const uint16_t *x_k8, int act_rows, int top_k,
+                                             const int32_t *sorted_slot, int rows, int K,
+                                             const uint8_t *codes, const uint8_t *scales,
+                                             const int32_t *group_sizes, int E, int N, uint16_t *h,
+                                             int h_k8, int *status, uint64_t wait_limit_ns,
+                                             cudaStream_t stream, int num_sms) {
+    return launch_gemm<false, gemm::kMapGather>(x_k8, rows, K, codes, scales, nullptr, group_sizes, E, N,
+                                          h, 1, 1, 1, h_k8, status, wait_limit_ns, stream, num_sms,
+                                          32, sorted_slot, top_k, act_rows, nullptr);
+}
+
+moe_status launch_grouped_gemm_scatter(const uint16_t *act, int rows, int K, const uint8_t *codes,
+                                       const uint8_t *scales, const int32_t *group_sizes, int E,
+                                       int N, const int32_t *out_row, void *out, int out_bf16,
+                                       int act_k8, int *status, uint64_t wait_limit_ns,
+                                       cudaStream_t stream, int num_sms) {
+    return launch_gemm<false, gemm::kMapScatter>(act, rows, K, codes, scales, nullptr, group_sizes, E, N,
+                                           out, out_bf16, act_k8, 0, 0, status, wait_limit_ns,
+                                           stream, num_sms, 32, nullptr, 1, 0, out_row);
 }
 
 moe_status launch_grouped_gemm_nvfp4(const uint16_t *act, int rows, int K, const uint8_t *codes,

@@ -19,7 +19,8 @@ size_t route_sort_scratch_bytes(int T, int k, int E);
 moe_status launch_route_sort(const int32_t *ids, int T, int k, int E, int32_t *group_sizes,
                              int32_t *offsets, int32_t *sorted_slot, int32_t *slot_to_row,
                              const uint16_t *x, int hidden, uint16_t *x_sorted, int x_k8,
-                             void *scratch, int *status, cudaStream_t stream, int *launches);
+                             void *scratch, int *status, cudaStream_t stream, int *launches,
+                             uint16_t *x_tok = nullptr);
 
 moe_status launch_route_sort_noalloc(const int32_t *ids, int T, int k, int E,
                                      int32_t *group_sizes, int32_t *offsets,
@@ -45,6 +46,23 @@ moe_status launch_grouped_gemm_swiglu(const uint16_t *act, int rows, int K, cons
                                       int N, uint16_t *h, int act_k8, int h_k8, int *status,
                                       uint64_t wait_limit_ns, cudaStream_t stream, int num_sms);
 
+// Fused w13 + SwiGLU with the routing permutation in the activation load:
+// sorted row r reads row sorted_slot[r] / top_k of x_k8 [act_rows, K]
+// (K8-interleaved token activations).
+moe_status launch_grouped_gemm_swiglu_gather(const uint16_t *x_k8, int act_rows, int top_k,
+                                             const int32_t *sorted_slot, int rows, int K,
+                                             const uint8_t *codes, const uint8_t *scales,
+                                             const int32_t *group_sizes, int E, int N, uint16_t *h,
+                                             int h_k8, int *status, uint64_t wait_limit_ns,
+                                             cudaStream_t stream, int num_sms);
+
+// Grouped GEMM writing sorted row r to output row out_row[r].
+moe_status launch_grouped_gemm_scatter(const uint16_t *act, int rows, int K, const uint8_t *codes,
+                                       const uint8_t *scales, const int32_t *group_sizes, int E,
+                                       int N, const int32_t *out_row, void *out, int out_bf16,
+                                       int act_k8, int *status, uint64_t wait_limit_ns,
+                                       cudaStream_t stream, int num_sms);
+
 moe_status launch_grouped_gemm_nvfp4(const uint16_t *act, int rows, int K, const uint8_t *codes,
                                      const uint8_t *scales16, const float *weight_scale_2,
                                      const int32_t *group_sizes, int E, int N, void *out,
@@ -64,7 +82,13 @@ moe_status launch_bounded_wait(uint64_t limit_ns, int *status, cudaStream_t stre
 moe_status launch_swiglu(const void *gu, int in_bf16, long long rows, int I, uint16_t *h,
                          int h_k8, cudaStream_t stream, int num_sms);
 
+// x_k8 [rows, hidden] = x with every 8 bf16 in the K8-interleaved order.
+moe_status launch_interleave_k8(const uint16_t *x, long long rows, int hidden, uint16_t *x_k8,
+                                cudaStream_t stream, int num_sms);
+
+// slot_order: y row of slot s is s (s2r only marks the slots that count).
 moe_status launch_combine(const float *y, const int32_t *s2r, const float *w, int T, int k, int N,
-                          void *out, int out_bf16, cudaStream_t stream, int num_sms);
+                          void *out, int out_bf16, cudaStream_t stream, int num_sms,
+                          int slot_order = 0);
 
 }  // namespace moe

@@ -108,13 +108,51 @@ scan_kernel(int32_t *chunk_tot, int n_chunks, int E, int32_t *group_sizes, int32
     if (tid == 0) offsets[E] = carry;
 }
 
+// One warp copies a row of `hidden` bf16 (16-byte vectors), optionally into the
+// K8-interleaved order (a permutation inside each 16 bytes).
+__device__ __forceinline__ void copy_row(const uint16_t *src_row, uint16_t *dst_row, int hidden,
+                                         int k8, int lane) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(src_row);
+    uint4 *dst = reinterpret_cast<uint4 *>(dst_row);
+    const int nvec = hidden / 8;
+    int i = lane;
+    if (k8) {
+        for (; i + 96 < nvec; i += 128) {   // four independent 16-byte loads in flight
+            const uint4 a = __ldg(src + i), b = __ldg(src + i + 32), c = __ldg(src + i + 64),
+                        d = __ldg(src + i + 96);
+            dst[i] = interleave8(a);
+            dst[i + 32] = interleave8(b);
+            dst[i + 64] = interleave8(c);
+            dst[i + 96] = interleave8(d);
+        }
+        for (; i < nvec; i += 32) dst[i] = interleave8(__ldg(src + i));
+    } else {
+        for (; i + 96 < nvec; i += 128) {
+            const uint4 a = __ldg(src + i), b = __ldg(src + i + 32), c = __ldg(src + i + 64),
+                        d = __ldg(src + i + 96);
+            dst[i] = a;
+            dst[i + 32] = b;
+            dst[i + 64] = c;
+            dst[i + 96] = d;
+        }
+        for (; i < nvec; i += 32) dst[i] = __ldg(src + i);
+    }
+}
+
+// One warp per routing slot s: its sorted row, and the activation copies.
+// x_sorted (gather): row `row` <- x[s / k].  x_tok (token order, K8): the warp
+// of slot t*k copies x[t], once per token and whatever its ids.
 __global__ void __launch_bounds__(256)
 scatter_kernel(const int32_t *ids, int rows, int k, int E, const int32_t *chunk_base,
                const int32_t *offsets, const int32_t *rank, int32_t *sorted_slot,
-               int32_t *slot_to_row, const uint16_t *x, int hidden, uint16_t *x_sorted, int x_k8) {
+               int32_t *slot_to_row, const uint16_t *x, int hidden, uint16_t *x_sorted, int x_k8,
+               uint16_t *x_tok) {
     const int lane = threadIdx.x & 31;
     const int s = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (s >= rows) return;
+    if (x_tok && s % k == 0)
+        copy_row(x + static_cast<size_t>(s / k) * hidden, x_tok + static_cast<size_t>(s / k) * hidden,
+                 hidden, 1, lane);
     const int e = ids[s];
     if (e < 0 || e >= E) {                 // recorded by the count kernel
         if (lane == 0) slot_to_row[s] = -1;   // no row: the combine skips this slot
@@ -126,33 +164,9 @@ scatter_kernel(const int32_t *ids, int rows, int k, int E, const int32_t *chunk_
         sorted_slot[row] = s;
         slot_to_row[s] = row;
     }
-    if (x_sorted) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(x + static_cast<size_t>(s / k) * hidden);
-        uint4 *dst = reinterpret_cast<uint4 *>(x_sorted + static_cast<size_t>(row) * hidden);
-        const int nvec = hidden / 8;
-        int i = lane;
-        if (x_k8) {   // write the K8-interleaved order: a permutation inside each 16 bytes
-            for (; i + 96 < nvec; i += 128) {
-                const uint4 a = __ldg(src + i), b = __ldg(src + i + 32), c = __ldg(src + i + 64),
-                            d = __ldg(src + i + 96);
-                dst[i] = interleave8(a);
-                dst[i + 32] = interleave8(b);
-                dst[i + 64] = interleave8(c);
-                dst[i + 96] = interleave8(d);
-            }
-            for (; i < nvec; i += 32) dst[i] = interleave8(__ldg(src + i));
-        } else {
-            for (; i + 96 < nvec; i += 128) {  // four independent 16-byte loads in flight
-                const uint4 a = __ldg(src + i), b = __ldg(src + i + 32), c = __ldg(src + i + 64),
-                            d = __ldg(src + i + 96);
-                dst[i] = a;
-                dst[i + 32] = b;
-                dst[i + 64] = c;
-                dst[i + 96] = d;
-            }
-            for (; i < nvec; i += 32) dst[i] = __ldg(src + i);
-        }
-    }
+    if (x_sorted)
+        copy_row(x + static_cast<size_t>(s / k) * hidden, x_sorted + static_cast<size_t>(row) * hidden,
+                 hidden, x_k8, lane);
 }
 
 }  // namespace rs
@@ -167,7 +181,8 @@ size_t route_sort_scratch_bytes(int T, int k, int E) {
 moe_status launch_route_sort(const int32_t *ids, int T, int k, int E, int32_t *group_sizes,
                              int32_t *offsets, int32_t *sorted_slot, int32_t *slot_to_row,
                              const uint16_t *x, int hidden, uint16_t *x_sorted, int x_k8,
-                             void *scratch, int *status, cudaStream_t stream, int *launches) {
+                             void *scratch, int *status, cudaStream_t stream, int *launches,
+                             uint16_t *x_tok) {
     const int rows = T * k;
     const int chunks = (rows + rs::kChunk - 1) / rs::kChunk;
     auto up = [](size_t b) { return (b + 255) & ~static_cast<size_t>(255); };
@@ -197,7 +212,7 @@ moe_status launch_route_sort(const int32_t *ids, int T, int k, int E, int32_t *g
     if (rows > 0) {
         rs::scatter_kernel<<<(rows + 7) / 8, 256, 0, stream>>>(ids, rows, k, E, chunk_tot, offsets,
                                                                rank, sorted_slot, slot_to_row, x,
-                                                               hidden, x_sorted, x_k8);
+                                                               hidden, x_sorted, x_k8, x_tok);
         ++*launches;
     }
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;

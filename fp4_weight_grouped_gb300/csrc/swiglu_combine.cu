@@ -9,7 +9,12 @@
 // expert reduction is deterministic, without atomicAdd): out[t] = sum_j
 // w[t,j] * y[slot_to_row[t*k+j]] as an f32 FMA chain in ascending j.
 //
-// Both are HBM-bound streams: 16-byte vector loads and stores, grid-stride loops
+// With y in slot order (the w2 GEMM's scatter), y row t*k+j is read directly.
+//
+// K8 interleave of activation rows (the layout the grouped GEMM's decode order
+// wants): a permutation inside every 8 bf16.
+//
+// All are HBM-bound streams: 16-byte vector loads and stores, grid-stride loops
 // over a grid sized to a multiple of the SM count.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -87,18 +92,22 @@ __global__ void swiglu_scalar(const T *gu, long long rows, int I, uint16_t *h) {
 }
 
 // One token row per block iteration; each thread owns 4 consecutive columns.
+// y rows in sorted order (row s2r[slot]) or, with slot_order, in slot order
+// (row = slot); either way a slot with s2r outside [0, T*k) adds nothing.
 template <bool OUT_BF16>
 __global__ void combine_vec4(const float *y, const int32_t *s2r, const float *w, int T, int k,
-                             int N, void *out) {
+                             int N, void *out, int slot_order) {
     const int n4 = N / 4;
     const int rows = T * k;
     for (int t = blockIdx.x; t < T; t += gridDim.x) {
         for (int c = threadIdx.x; c < n4; c += blockDim.x) {
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int j = 0; j < k; ++j) {
-                const int row = __ldg(s2r + static_cast<size_t>(t) * k + j);
+                const int slot = t * k + j;
+                const int r = __ldg(s2r + slot);
                 // A slot whose id was out of range has no row (-1): it adds nothing.
-                if (static_cast<unsigned>(row) >= static_cast<unsigned>(rows)) continue;
+                if (static_cast<unsigned>(r) >= static_cast<unsigned>(rows)) continue;
+                const int row = slot_order ? slot : r;
                 const float wj = __ldg(w + static_cast<size_t>(t) * k + j);
                 const float4 v = __ldg(reinterpret_cast<const float4 *>(y + static_cast<size_t>(row) * N) + c);
                 acc.x = fmaf(wj, v.x, acc.x);
@@ -120,14 +129,16 @@ __global__ void combine_vec4(const float *y, const int32_t *s2r, const float *w,
 
 template <bool OUT_BF16>
 __global__ void combine_scalar(const float *y, const int32_t *s2r, const float *w, int T, int k,
-                               int N, void *out) {
+                               int N, void *out, int slot_order) {
     const int rows = T * k;
     for (int t = blockIdx.x; t < T; t += gridDim.x) {
         for (int n = threadIdx.x; n < N; n += blockDim.x) {
             float acc = 0.f;
             for (int j = 0; j < k; ++j) {
-                const int row = s2r[static_cast<size_t>(t) * k + j];
-                if (static_cast<unsigned>(row) >= static_cast<unsigned>(rows)) continue;
+                const int slot = t * k + j;
+                const int r = s2r[slot];
+                if (static_cast<unsigned>(r) >= static_cast<unsigned>(rows)) continue;
+                const int row = slot_order ? slot : r;
                 acc = fmaf(w[static_cast<size_t>(t) * k + j], y[static_cast<size_t>(row) * N + n], acc);
             }
             if (OUT_BF16) {
@@ -141,7 +152,25 @@ __global__ void combine_scalar(const float *y, const int32_t *s2r, const float *
     }
 }
 
+__global__ void interleave_k8_vec8(const uint4 *x, long long n16, uint4 *out) {
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n16;
+         i += static_cast<long long>(gridDim.x) * blockDim.x)
+        out[i] = interleave8(__ldg(x + i));
+}
+
 }  // namespace ew
+
+moe_status launch_interleave_k8(const uint16_t *x, long long rows, int hidden, uint16_t *x_k8,
+                                cudaStream_t stream, int num_sms) {
+    const long long n16 = rows * (hidden / 8);
+    if (n16 == 0) return MOE_OK;
+    long long blocks = (n16 + 255) / 256;
+    const long long cap = static_cast<long long>(num_sms) * 8;
+    if (blocks > cap) blocks = cap;
+    ew::interleave_k8_vec8<<<static_cast<int>(blocks), 256, 0, stream>>>(
+        reinterpret_cast<const uint4 *>(x), n16, reinterpret_cast<uint4 *>(x_k8));
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
 
 moe_status launch_swiglu(const void *gu, int in_bf16, long long rows, int I, uint16_t *h,
                          int h_k8, cudaStream_t stream, int num_sms) {
@@ -170,17 +199,18 @@ moe_status launch_swiglu(const void *gu, int in_bf16, long long rows, int I, uin
 }
 
 moe_status launch_combine(const float *y, const int32_t *s2r, const float *w, int T, int k, int N,
-                          void *out, int out_bf16, cudaStream_t stream, int num_sms) {
+                          void *out, int out_bf16, cudaStream_t stream, int num_sms,
+                          int slot_order) {
     if (T == 0 || N == 0) return MOE_OK;
     int blocks = T < num_sms * 16 ? T : num_sms * 16;
     const bool vec = (N % 4) == 0;
     const int threads = vec ? (N / 4 < 256 ? ((N / 4 + 31) / 32) * 32 : 256) : 256;
     if (vec) {
-        if (out_bf16) ew::combine_vec4<true><<<blocks, threads, 0, stream>>>(y, s2r, w, T, k, N, out);
-        else ew::combine_vec4<false><<<blocks, threads, 0, stream>>>(y, s2r, w, T, k, N, out);
+        if (out_bf16) ew::combine_vec4<true><<<blocks, threads, 0, stream>>>(y, s2r, w, T, k, N, out, slot_order);
+        else ew::combine_vec4<false><<<blocks, threads, 0, stream>>>(y, s2r, w, T, k, N, out, slot_order);
     } else {
-        if (out_bf16) ew::combine_scalar<true><<<blocks, threads, 0, stream>>>(y, s2r, w, T, k, N, out);
-        else ew::combine_scalar<false><<<blocks, threads, 0, stream>>>(y, s2r, w, T, k, N, out);
+        if (out_bf16) ew::combine_scalar<true><<<blocks, threads, 0, stream>>>(y, s2r, w, T, k, N, out, slot_order);
+        else ew::combine_scalar<false><<<blocks, threads, 0, stream>>>(y, s2r, w, T, k, N, out, slot_order);
     }
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

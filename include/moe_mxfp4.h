@@ -73,10 +73,18 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
  *  MOE_ACT_ROW_MAJOR      element k of a row at position k.
  *  MOE_ACT_K8_INTERLEAVED within every group of 8 consecutive k (8g .. 8g+7)
  *                         the stored order is 8g + {0,4,1,5,2,6,3,7}; K % 8 == 0.
+ *  MOE_ACT_K8_TOKEN_ORDER (moe_route_sort's x output only) x itself, in token
+ *                         order [T, hidden], K8-interleaved, instead of the
+ *                         gathered copy: the input of
+ *                         moe_mxfp4_grouped_gemm_swiglu_gather.
  * The grouped GEMM reduces in the interleaved order (its weight decode pairs
  * codes j and j+4 of every 8); route sort and SwiGLU can write it at no cost,
  * and the GEMM interleaves row-major input itself in shared memory. */
-typedef enum { MOE_ACT_ROW_MAJOR = 0, MOE_ACT_K8_INTERLEAVED = 1 } moe_act_layout;
+typedef enum {
+    MOE_ACT_ROW_MAJOR = 0,
+    MOE_ACT_K8_INTERLEAVED = 1,
+    MOE_ACT_K8_TOKEN_ORDER = 2
+} moe_act_layout;
 
 /* Human-readable name of a status code (static string). */
 MOE_API const char *moe_status_string(moe_status status);
@@ -111,6 +119,8 @@ MOE_API moe_status moe_read_status(const void *workspace, void *stream);
  *  hidden       row length of x (multiple of 8 when x is given).
  *  x_sorted     device bf16 [T*k, hidden] out, or NULL: x_sorted[row] =
  *               x[sorted_slot[row] / k] (the activation permutation), x row-major.
+ *               With MOE_ACT_K8_TOKEN_ORDER: [T, hidden], x_sorted[t] = x[t] in
+ *               the K8 order (no permutation; the gather GEMM does it).
  *  x_sorted_layout  order of the reduction dimension written to x_sorted.
  *  workspace    device, >= moe_workspace_bytes(T, k, E) bytes, 16-byte aligned.
  * Ids outside [0, E) set MOE_ERR_DATA.  Such a slot is left out of every
@@ -273,6 +283,52 @@ MOE_API moe_status moe_mxfp4_grouped_gemm_swiglu(const uint16_t *act, moe_act_la
                                                  size_t workspace_bytes, void *stream);
 
 /*
+ * moe_mxfp4_grouped_gemm_swiglu_gather — moe_mxfp4_grouped_gemm_swiglu with the
+ * activation permutation fused into the activation load ([TPU] section 1: the
+ * activation permutation that the grouped-matmul timings leave out).  Sorted
+ * row r (of band e, in the order of moe_route_sort) takes its activations from
+ * token row sorted_slot[r] / top_k of x_k8, fetched by four-row TMA gathers, so
+ * no [rows, K] copy of the activations is ever written.  Outputs are identical,
+ * bit for bit, to moe_mxfp4_grouped_gemm_swiglu on the gathered rows.
+ *
+ *  x_k8         device bf16 [T, K], K8-interleaved (moe_act_interleave_k8, or
+ *               moe_layer_forward's route step), 16-byte aligned.
+ *  T, top_k     token rows of x_k8 and routing choices per token.
+ *  sorted_slot  device int32 [rows] from moe_route_sort (row -> slot).  An
+ *               entry whose token lies outside [0, T) sets MOE_ERR_DATA (the
+ *               row then reads the nearest token row; its outputs are wrong).
+ *  Other arguments as for moe_mxfp4_grouped_gemm_swiglu; h is written in the
+ *  sorted row order.
+ */
+MOE_API moe_status moe_mxfp4_grouped_gemm_swiglu_gather(const uint16_t *x_k8, int32_t T,
+                                                        int32_t top_k, const int32_t *sorted_slot,
+                                                        int64_t rows, int32_t K,
+                                                        const uint8_t *codes, const uint8_t *scales,
+                                                        const int32_t *group_sizes, int32_t E,
+                                                        int32_t I, uint16_t *h,
+                                                        moe_act_layout h_layout, void *workspace,
+                                                        size_t workspace_bytes, void *stream);
+
+/*
+ * moe_mxfp4_grouped_gemm_scatter — moe_mxfp4_grouped_gemm writing sorted row r
+ * of the result to row out_row[r] of `out` ([TPU] section 1: the permutation
+ * back to slot order, here fused into the epilogue).  With out_row =
+ * sorted_slot from moe_route_sort, out is in slot order (row t*k + j for token
+ * t's j-th choice) and moe_combine_slots reads it without an index.
+ *
+ *  out_row      device int32 [rows].  An entry outside [0, rows) is skipped and
+ *               sets MOE_ERR_DATA; rows of `out` that no entry names are not
+ *               written.
+ *  Other arguments as for moe_mxfp4_grouped_gemm.
+ */
+MOE_API moe_status moe_mxfp4_grouped_gemm_scatter(const uint16_t *act, moe_act_layout act_layout,
+                                                  int64_t rows, int32_t K, const uint8_t *codes,
+                                                  const uint8_t *scales, const int32_t *group_sizes,
+                                                  int32_t E, int32_t N, const int32_t *out_row,
+                                                  void *out, moe_dtype out_dtype, void *workspace,
+                                                  size_t workspace_bytes, void *stream);
+
+/*
  * moe_nvfp4_grouped_gemm — the same grouped matmul with NVFP4 weights ([TPU]
  * section 1: the NVFP4 kernel that decodes e2m1 weights and per-16 E4M3 scales;
  * [NVFP4] "The lossless weight cast": per-16 E4M3 block scales under a
@@ -335,6 +391,31 @@ MOE_API moe_status moe_swiglu(const void *gu, moe_dtype in_dtype, int64_t rows, 
 MOE_API moe_status moe_combine(const float *y, const int32_t *slot_to_row, const float *topk_w,
                        int32_t T, int32_t k, int32_t N, void *out, moe_dtype out_dtype,
                        void *stream);
+
+/*
+ * moe_combine_slots — moe_combine with y in slot order:
+ *
+ *   out[t, n] = sum_{j = 0..k-1} topk_w[t, j] * y[t*k + j, n]
+ *
+ * over the slots whose slot_to_row entry lies in [0, T*k) (moe_route_sort
+ * writes -1 for an id out of range; such a slot adds nothing and its y row is
+ * never read).  Same f32 FMA chain in ascending j as moe_combine, so for y
+ * permuted to slot order the results are identical bit for bit.
+ *  y            device f32 [T*k, N] in slot order, 16-byte aligned.
+ *  Other arguments as for moe_combine.
+ */
+MOE_API moe_status moe_combine_slots(const float *y, const int32_t *slot_to_row, const float *topk_w,
+                                     int32_t T, int32_t k, int32_t N, void *out, moe_dtype out_dtype,
+                                     void *stream);
+
+/*
+ * moe_act_interleave_k8 — activations in the K8-interleaved order the grouped
+ * GEMMs consume: within every 8 consecutive bf16 of a row, element e moves to
+ * position 2e (e < 4) or 2(e - 4) + 1.
+ *  x, x_k8      device bf16 [rows, hidden], 16-byte aligned, hidden % 8 == 0.
+ */
+MOE_API moe_status moe_act_interleave_k8(const uint16_t *x, int64_t rows, int32_t hidden,
+                                         uint16_t *x_k8, void *stream);
 
 /*
  * moe_layer_forward — the whole routed-expert path in one call:
