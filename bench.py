@@ -418,6 +418,8 @@ def run_ours(args, rank, world, local):
     ge.build()
     from fp4_weight_grouped_gb300 import binding as B
     from fp4_weight_grouped_gb300 import inputs
+    B.set_gemm_pairing({"auto": B.MOE_PAIRING_AUTO, "off": B.MOE_PAIRING_OFF,
+                        "on": B.MOE_PAIRING_ON}[args.pairing])
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -835,6 +837,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="layer_T8192")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--pairing", choices=["auto", "off", "on"], default="auto",
+                    help="CTA pairs for bands over 32 rows (moe_set_gemm_pairing)")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle leg")
     ap.add_argument("--no-sub-workloads", action="store_true",
                     help="time only --workload (skip the other shapes)")

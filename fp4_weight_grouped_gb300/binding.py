@@ -26,7 +26,7 @@ SYMBOLS = (
     "moe_route_sort_noalloc", "moe_nvfp4_cast_workspace_bytes", "moe_mxfp4_to_nvfp4",
     "moe_nvfp4_grouped_gemm", "moe_mxfp4_grouped_gemm_swiglu", "moe_mxfp4_grouped_gemm_block",
     "moe_mxfp4_grouped_gemm_swiglu_gather", "moe_mxfp4_grouped_gemm_scatter", "moe_combine_slots",
-    "moe_act_interleave_k8",
+    "moe_act_interleave_k8", "moe_set_gemm_pairing",
 )
 
 _lock = threading.Lock()
@@ -73,6 +73,7 @@ def load(path: str | None = None):
                                                     C.c_int, P, SZ, P], C.c_int),
                 "moe_combine_slots": ([P, P, P, I32, I32, I32, P, C.c_int, P], C.c_int),
                 "moe_act_interleave_k8": ([P, I64, I32, P, P], C.c_int),
+                "moe_set_gemm_pairing": ([I32], C.c_int),
                 "moe_swiglu": ([P, C.c_int, I64, I32, P, C.c_int, P], C.c_int),
                 "moe_combine": ([P, P, P, I32, I32, I32, P, C.c_int, P], C.c_int),
                 "moe_layer_forward": ([P, P, P, I32, I32, I32, I32, I32, P, P, P, P, P,
@@ -120,6 +121,14 @@ def _dtype_code(dt) -> int:
     if dt == torch.bfloat16:
         return MOE_BF16
     raise ValueError(f"unsupported dtype {dt}")
+
+
+MOE_PAIRING_AUTO, MOE_PAIRING_OFF, MOE_PAIRING_ON = 0, 1, 2
+
+
+def set_gemm_pairing(mode: int):
+    """CTA pairs for bands over 32 rows: MOE_PAIRING_AUTO / _OFF / _ON (process-wide)."""
+    _check(load().moe_set_gemm_pairing(int(mode)), "moe_set_gemm_pairing")
 
 
 def last_launch_count() -> int:

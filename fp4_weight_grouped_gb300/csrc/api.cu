@@ -421,6 +421,12 @@ moe_status moe_layer_forward(const uint16_t *x, const int32_t *topk_ids, const f
     return st;
 }
 
+moe_status moe_set_gemm_pairing(int32_t mode) {
+    if (mode < MOE_PAIRING_AUTO || mode > MOE_PAIRING_ON) return MOE_ERR_INVALID_ARG;
+    moe::set_gemm_pairing(mode);
+    return MOE_OK;
+}
+
 moe_status moe_mxfp4_decode_expert(const uint8_t *codes, const uint8_t *scales, int32_t E,
                                    int32_t N, int32_t K, int32_t e, uint16_t *out,
                                    void *workspace, size_t workspace_bytes, void *stream) {

@@ -79,6 +79,8 @@ constexpr int kWideNT = 256;                  // wide mode: tokens per work item
 // converters run far ahead of the tensor core, while the activation tiles
 // (re-read from L2 for every column tile) need the deeper prefetch.
 constexpr int kWideActSlots = 5;
+// Pair mode: activation slots of up to 16 KB (a CTA's half of 256 tokens).
+constexpr int kPairActSlots = 8;
 constexpr int kStageK = 64;                   // K per decode / MMA stage
 constexpr int kSlots = 8;                     // A slots in TMEM (+ activation slots in smem)
 constexpr int kSlotsMax = 12;                 // bands <= 16 rows: three A slots per warpgroup
@@ -432,7 +434,7 @@ __device__ __forceinline__ void decode16_scaled(uint32_t c0, uint32_t c1, uint32
 // launch for bands of at most 32 rows (split mode only); otherwise the launch
 // for longer bands (single or wide mode).  Separate instantiations keep each
 // mode's loops free of the other modes' code.
-template <bool kNv, bool kSplit, int kMap>
+template <bool kNv, bool kSplit, int kMap, bool kPair = false>
 __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUtensorMap &tm_act,
                                           const CUtensorMap &tm_act3, const CUtensorMap &tm_scales,
                                           const CUtensorMap &tm_act64, const Params &p,
@@ -466,6 +468,30 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const int E = p.E;
+    // CTA pair (kPair, wide mode only): the two CTAs of a cluster share every
+    // work item.  Each takes 128 weight rows of the pair's 256-row tile (tile
+    // 2t + rank of pair tile t) and half of the item's token rows; the even CTA
+    // issues M = 256 MMAs over both, so each SM loads half of the activations.
+    static_assert(!kPair || (!kSplit && !kNv && kMap == kMapNone), "pair mode: MXFP4 wide bands");
+    const uint32_t rank = kPair ? cluster_rank() : 0u;
+    const int cta = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+    const int n_cta = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+    const int item_tiles = kPair ? p.n_tiles / 2 : p.n_tiles;    // column tiles a work item list has
+    // Tensor-core issue in the instantiation's CTA granularity (a kernel uses
+    // the single-CTA or the pair forms throughout).  Pair commits arrive on the
+    // barrier in both CTAs, except for the issuer's own final barrier.
+    auto mma_issue = [](uint32_t d, uint32_t a, uint64_t b, uint32_t id, uint32_t acc) {
+        if constexpr (kPair) mma_bf16_ts_pair(d, a, b, id, acc);
+        else mma_bf16_ts(d, a, b, id, acc);
+    };
+    auto mma_commit_all = [](uint64_t *bar) {
+        if constexpr (kPair) mma_commit_pair(bar, 3);
+        else mma_commit(bar);
+    };
+    auto mma_commit_own = [](uint64_t *bar) {
+        if constexpr (kPair) mma_commit_pair(bar, 1);
+        else mma_commit(bar);
+    };
 
     // ---------------------------------------------------------------- prologue
     if (tid == 0) {
@@ -488,7 +514,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
             if (gs >= p.band_lo && gs <= p.band_hi) g_max = max(g_max, gs);
         }
         g_max = __reduce_max_sync(0xffffffffu, g_max);
-        const int chunk = (p.allow_wide && g_max > kMaxNT) ? kWideNT : kMaxNT;
+        const int chunk = (kPair || (p.allow_wide && g_max > kMaxNT)) ? kWideNT : kMaxNT;
         long long run_rows = 0, run_items = 0;
         int nt_max = 0;
         for (int base = 0; base < E; base += 32) {
@@ -496,8 +522,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
             const int gs = e < E ? p.group_sizes[e] : 0;
             const int g = gs > 0 ? gs : 0;
             const int gw = (g >= p.band_lo && g <= p.band_hi) ? g : 0;   // rows with work here
-            const long long items = ((static_cast<long long>(gw) + chunk - 1) / chunk) * p.n_tiles;
-            nt_max = max(nt_max, gw >= chunk ? chunk : (gw + 15) & ~15);
+            const long long items = ((static_cast<long long>(gw) + chunk - 1) / chunk) * item_tiles;
+            nt_max = max(nt_max, gw >= chunk ? chunk : (gw + (kPair ? 31 : 15)) & (kPair ? ~31 : ~15));
             long long incl_r = g, incl_i = items;
 #pragma unroll
             for (int d = 1; d < 32; d <<= 1) {
@@ -532,15 +558,26 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
         return;
     }
     const int total_items = ioff[E];
-    if (static_cast<int>(blockIdx.x) >= total_items) return;
-    const int my_items = (total_items - static_cast<int>(blockIdx.x) + gridDim.x - 1) / gridDim.x;
+    if (cta >= total_items) return;                 // the same for both CTAs of a pair
+    const int my_items = (total_items - cta + n_cta - 1) / n_cta;
     const int chunk = *chunk_slot;
     const int tile_cols = p.swiglu ? kBN / 2 : kBN;
+    // Work item i of this CTA.  Pair: the pair tile covers two column tiles;
+    // this CTA's is the one of its rank, and nt is a multiple of 32 so that
+    // each CTA's half of the token rows is a multiple of 16.
+    auto make_item = [&](int i) -> Item {
+        Item it = decode_item(cta + i * n_cta, roff, ioff, E, item_tiles, chunk,
+                              kPair ? 2 * tile_cols : tile_cols);
+        if constexpr (kPair) {
+            it.n0 += static_cast<int>(rank) * tile_cols;
+            it.nt = (it.nvalid + 31) & ~31;
+        }
+        return it;
+    };
     // The CTA's first kItemCache work items, decoded once (visible after the
     // barrier set-up's __syncthreads below); later ones are decoded on demand.
     for (int t = tid; t < my_items && t < kItemCache; t += kThreads) {
-        const Item it = decode_item(blockIdx.x + t * gridDim.x, roff, ioff, E, p.n_tiles, chunk,
-                                    tile_cols);
+        const Item it = make_item(t);
         item_cache[t] = make_int4(it.e, it.row0, it.n0, it.nvalid | (it.nt << 16));
     }
     uint32_t *nv_tab = reinterpret_cast<uint32_t *>(smem + kOffNvTab);
@@ -548,8 +585,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
         for (int t = tid; t < 256; t += kThreads) nv_tab[t] = e4m3_scaled_pair(static_cast<uint32_t>(t));
     }
     auto get_item = [&](int i) -> Item {
-        if (i >= kItemCache)
-            return decode_item(blockIdx.x + i * gridDim.x, roff, ioff, E, p.n_tiles, chunk, tile_cols);
+        if (i >= kItemCache) return make_item(i);
         const int4 v = item_cache[i];
         Item it;
         it.e = v.x;
@@ -579,11 +615,13 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
     constexpr bool split = kSplit;
     const bool wide = !kSplit && chunk == kWideNT;
     // One 64-k activation tile: split mode nt_max rows (16-row boxes); single
-    // and wide mode nt_max rounded up to 64 rows (64-row boxes, up to four
-    // copies a stage).
+    // and wide mode nt_max rounded up to 64 rows (64- and 32-row boxes, up to
+    // four copies a stage); pair mode this CTA's half, nt_max / 2 rounded up to
+    // 64 rows, so twice the slots fit.
     const uint32_t act_stage_bytes =
-        static_cast<uint32_t>(nt_max <= kPartCols ? nt_max : (nt_max + 63) & ~63) * 128u;
-    const uint32_t n_act = wide ? kWideActSlots : kSlots;   // activation slots (single, wide)
+        kPair ? static_cast<uint32_t>(((nt_max / 2) + 63) & ~63) * 128u
+              : static_cast<uint32_t>(nt_max <= kPartCols ? nt_max : (nt_max + 63) & ~63) * 128u;
+    const uint32_t n_act = kPair ? kPairActSlots : (wide ? kWideActSlots : kSlots);
     // Ring slot: codes (16 KB), [split: activation tile], [scale tile, loaded
     // with every even code stage for itself and the next one].
     const uint32_t scale_off = kCodeStageBytes + (split ? 4u * act_stage_bytes : 0u);
@@ -615,27 +653,36 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
     // Issuers splitting the token columns of an item (single and wide mode).
     const int n_iss = wide ? kWideIssuers : kSingleIssuers;
 
-    if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
+    if (warp == 0) {
+        if constexpr (kPair) tmem_alloc_pair(tmem_slot, kTmemCols);   // both CTAs, same address
+        else tmem_alloc(tmem_slot, kTmemCols);
+    }
+    // Pair: the even CTA's a_full, act_full and acc_empty also count the odd
+    // CTA's arrivals (its converter warps, its activation relay, its epilogue
+    // warps); the pair commits arrive on both CTAs' slot_empty, act_empty and
+    // acc_full.
+    const uint32_t peer_arrivals = (kPair && rank == 0) ? 1u : 0u;
     if (tid == 0) {
         for (uint32_t i = 0; i < CS; ++i) {
             mbar_init(&code_full[i], 1);
             mbar_init(&code_empty[i], 4 * kConvWG / 2 + (split ? kIssuerWarps : 0));
         }
         for (int i = 0; i < kSlotsMax; ++i) {
-            mbar_init(&a_full[i], 4);
-            mbar_init(&act_full[i], 1);
+            mbar_init(&a_full[i], 4 * (1 + peer_arrivals));
+            mbar_init(&act_full[i], 1 + peer_arrivals);
             mbar_init(&slot_empty[i], split ? 1 : n_iss);
             mbar_init(&act_empty[i], n_iss);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&acc_full[i], split ? kIssuerWarps : n_iss);
-            mbar_init(&acc_empty[i], 4 * kConvWG);
+            mbar_init(&acc_empty[i], 4 * kConvWG * (1 + peer_arrivals));
         }
         for (int i = 0; i < kIssuerWarps; ++i) mbar_init(&final_bar[i], 1);
         mbar_fence_init();
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (kPair) cluster_sync();   // the peer's barriers exist before any remote arrival
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const uint32_t code_smem = smem_u32(smem + kOffCode);
@@ -652,7 +699,20 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
         // loop (its values stay warp-uniform); one elected lane issues the MMAs
         // and the commits, always the same lane, so each commit covers its MMAs.
         const int w = warp;
-        if (split || w < n_iss) {
+        if (kPair && rank == 1 && w == 0) {
+            // Pair, odd CTA: relay of its activation halves.  Once its own half
+            // of a stage has landed, arrive on the even CTA's barrier of that
+            // stage (which the issuer there waits on), in the producer's order.
+            const uint32_t peer_act_full = cluster_addr(act_full, 0);
+            Ring r;
+            bool ok = true;
+            for (int i = 0; i < my_items && ok; ++i)
+                for (int ks = 0; ks < KT && ok; ++ks, r.next(n_act)) {
+                    ok = warp_wait_bounded(&act_full[r.slot], r.phase, abort_flag, p.status, lim);
+                    if (ok && lane == 0) mbar_arrive_cluster(peer_act_full + 8u * r.slot);
+                    __syncwarp();
+                }
+        } else if (kPair ? (rank == 0 && w == 0) : (split || w < n_iss)) {
             Item it = get_item(0);
             // This issuer's token columns [c0, c0 + cn) of the item (single mode).
             auto my_cols = [&](int nt, uint32_t &c0, uint32_t &cn) {
@@ -667,7 +727,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
             };
             uint32_t c0, cn;
             my_cols(it.nt, c0, cn);
-            uint32_t idesc = idesc_bf16_f32(128, cn ? cn : 16);
+            constexpr uint32_t kM = kPair ? 256u : 128u;      // pair: both CTAs' 128 weight rows
+            uint32_t idesc = idesc_bf16_f32(kM, cn ? cn : 16);
             Ring ring;                        // split mode: code stage of this issuer's stage
             const uint32_t d_part = split ? w * part_cols : 0;
             Ring sr;                          // this issuer's A-slot sequence
@@ -735,20 +796,20 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
                             if (cn > 0)
 #pragma unroll
                             for (int kk = 0; kk < kStageK / 16; ++kk)
-                                mma_bf16_ts(d_tmem, a_col + kk * 8,
+                                mma_issue(d_tmem, a_col + kk * 8,
                                             b0 + static_cast<uint64_t>(kk * 2), idesc,
                                             (kp == 0 && h == 0 && kk == 0) ? 0u : 1u);
-                            if (h & 1) mma_commit(&slot_empty[sl[h] >> 1]);
-                            if (wide) mma_commit(&act_empty[al[h]]);
+                            if (h & 1) mma_commit_all(&slot_empty[sl[h] >> 1]);
+                            if (wide) mma_commit_all(&act_empty[al[h]]);
                         }
-                        if (kp + grp >= KT) mma_commit(&acc_full[buf]);
+                        if (kp + grp >= KT) mma_commit_all(&acc_full[buf]);
                     }
                     __syncwarp();
                 }
                 if (ok && i + 1 < my_items) {
                     it = get_item(i + 1);
                     my_cols(it.nt, c0, cn);
-                    idesc = idesc_bf16_f32(128, cn ? cn : 16);
+                    idesc = idesc_bf16_f32(kM, cn ? cn : 16);
                 }
             }
             // Split mode: issuer w issues sub-stages 2w and 2w + 1 of every code
@@ -784,13 +845,13 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
                             const uint64_t b0 = smem_desc_sw128(b_base + h * act_stage_bytes);
 #pragma unroll
                             for (int kk = 0; kk < kStageK / 16; ++kk)
-                                mma_bf16_ts(d_tmem, a_col + kk * 8,
+                                mma_issue(d_tmem, a_col + kk * 8,
                                             b0 + static_cast<uint64_t>(kk * 2), idesc,
                                             (m == 0 && h == 0 && kk == 0) ? 0u : 1u);
                         }
-                        mma_commit(&slot_empty[s0 >> 1]);
-                        mma_commit(&code_empty[ring.slot]);
-                        if (m + 1 == KT / 4) mma_commit(&acc_full[buf]);
+                        mma_commit_all(&slot_empty[s0 >> 1]);
+                        mma_commit_all(&code_empty[ring.slot]);
+                        if (m + 1 == KT / 4) mma_commit_all(&acc_full[buf]);
                     }
                     __syncwarp();
                     ring.next(CS);
@@ -803,7 +864,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
                 }
             }
             // All MMAs issued by the elected lane must finish before TMEM is freed.
-            if (elect_one()) mma_commit(&final_bar[w]);
+            if (elect_one()) mma_commit_own(&final_bar[w]);
             __syncwarp();
             warp_wait_bounded(&final_bar[w], 0, nullptr, p.status, lim);
         }
@@ -956,6 +1017,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
         // ------------------------------------- activation producer (single mode)
         if (lane == 0 && !split) {
             tma_prefetch_map(&tm_act64);
+            tma_prefetch_map(&tm_act3);
             Ring r;
             uint32_t issued = 0;
             bool ok = true;
@@ -969,11 +1031,26 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
                         ok = false;
                         break;
                     }
-                    const int groups = (it.nt + 63) / 64;
-                    mbar_arrive_expect_tx(&act_full[r.slot], static_cast<uint32_t>(groups) * 8192u);
+                    // The stage's token rows (pair: this CTA's half of them) in 64-row
+                    // boxes.  Pair: a last part of at most 32 rows takes a 32-row box
+                    // (tm_act3 holds the 32-row map in these launches); copies cost
+                    // the SM per request as well as per byte, so smaller boxes would
+                    // lose more than the at most 16 rows they save.  One CTA: whole
+                    // 64-row boxes (measured faster there).
                     const uint32_t dst = act_smem + r.slot * act_stage_bytes;
-                    for (int grp = 0; grp < groups; ++grp)
-                        tma_load_2d(dst + grp * 8192, &tm_act64, ks * kStageK, it.row0 + grp * 64,
+                    const int n = kPair ? it.nt / 2 : it.nt;
+                    const int r0 = it.row0 + static_cast<int>(rank) * n;
+                    const int full64 = n & ~63, tail = n - full64;
+                    const int fetched =
+                        full64 + (tail == 0 ? 0 : ((kPair && tail <= 32) ? 32 : 64));
+                    mbar_arrive_expect_tx(&act_full[r.slot], static_cast<uint32_t>(fetched) * 128u);
+                    for (int g = 0; g < full64; g += 64)
+                        tma_load_2d(dst + g * 128, &tm_act64, ks * kStageK, r0 + g, &act_full[r.slot]);
+                    if (tail > 32 || (!kPair && tail > 0))
+                        tma_load_2d(dst + full64 * 128, &tm_act64, ks * kStageK, r0 + full64,
+                                    &act_full[r.slot]);
+                    else if (tail > 0)
+                        tma_load_2d(dst + full64 * 128, &tm_act3, ks * kStageK, r0 + full64,
                                     &act_full[r.slot]);
                 }
             }
@@ -1066,7 +1143,10 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
                                 part_cols, ts);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[buf]);
+            if (lane == 0) {
+                if (kPair && rank == 1) mbar_arrive_cluster(cluster_addr(&acc_empty[buf], 0));
+                else mbar_arrive(&acc_empty[buf]);
+            }
             return true;
         };
         const uint32_t total_cs = static_cast<uint32_t>(my_items) * KT4;
@@ -1201,7 +1281,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(&a_full[wg]);
+                if (kPair && rank == 1) mbar_arrive_cluster(cluster_addr(&a_full[wg], 0));
+                else mbar_arrive(&a_full[wg]);
             }
             // Wide mode has one accumulator: the next item's first MMAs wait for
             // this item's epilogue.  The slots this pair fills next were last
@@ -1238,13 +1319,18 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
     }
 
     // ---------------------------------------------------------------- teardown
+    // Pair: neither CTA frees its tensor memory or leaves while the pair's MMAs,
+    // commits or the peer's arrivals may still reach it.
     tc_fence_before();
     __syncthreads();
+    if constexpr (kPair) cluster_sync();
     tc_fence_after();
     if (warp == 0) {
         __syncwarp();
-        tmem_dealloc(tmem_base, kTmemCols);
+        if constexpr (kPair) tmem_dealloc_pair(tmem_base, kTmemCols);
+        else tmem_dealloc(tmem_base, kTmemCols);
     }
+    if constexpr (kPair) cluster_sync();
 }
 
 template <bool kSplit, int kMap>
@@ -1255,6 +1341,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
                     const __grid_constant__ CUtensorMap tm_scales,
                     const __grid_constant__ CUtensorMap tm_act64, const Params p) {
     gemm_body<false, kSplit, kMap>(tm_codes, tm_act, tm_act3, tm_scales, tm_act64, p, nullptr);
+}
+
+// Wide bands in CTA pairs (clusters of two): M = 256 MMAs over two SMs.
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_codes,
+                         const __grid_constant__ CUtensorMap tm_act,
+                         const __grid_constant__ CUtensorMap tm_act3,
+                         const __grid_constant__ CUtensorMap tm_scales,
+                         const __grid_constant__ CUtensorMap tm_act64, const Params p) {
+    gemm_body<false, false, kMapNone, true>(tm_codes, tm_act, tm_act3, tm_scales, tm_act64, p,
+                                            nullptr);
 }
 
 template <bool kSplit>
@@ -1310,6 +1407,33 @@ __global__ void bounded_wait_kernel(uint64_t limit_ns, int *status) {
 }  // namespace gemm
 
 // ----------------------------------------------------------------- host side
+
+// CTA-pair use for the launch of longer bands (process-wide): 0 automatic,
+// 1 never, 2 whenever the shape allows it.
+static std::atomic<int> g_pair_mode{0};
+
+void set_gemm_pairing(int mode) { g_pair_mode.store(mode, std::memory_order_relaxed); }
+
+// Clusters of two that the device can keep resident at once with the pair
+// kernel's shared memory (looked up once per device).
+static int pair_clusters(int num_sms, int smem_bytes) {
+    static std::atomic<int> cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    int n = cached[dev].load(std::memory_order_acquire);
+    if (n == 0) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(num_sms & ~1));
+        cfg.blockDim = dim3(gemm::kThreads);
+        cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, gemm::grouped_gemm_pair_kernel, &cfg) != cudaSuccess)
+            clusters = 0;
+        n = clusters > 0 ? clusters : -1;
+        cached[dev].store(n, std::memory_order_release);
+    }
+    return n > 0 ? n : 0;
+}
 
 // The driver's tensor-map encoder, looked up once per process (a function-local
 // static is initialised once even when host threads race on the first call).
@@ -1410,6 +1534,22 @@ static moe_status launch_gemm(const uint16_t *act, int rows, int K, const uint8_
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return MOE_ERR_CUDA;
     }
+    // 32-row boxes: the last part of a stage's rows in the launches for longer
+    // bands (passed there in place of the split mode's 3-D map).
+    CUtensorMap tm_act32;
+    if (!gather) {
+        cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), map_rows};
+        cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+        cuuint32_t box[2] = {64, 32};
+        cuuint32_t estr[2] = {1, 1};
+        if (encode(&tm_act32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(act), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return MOE_ERR_CUDA;
+    } else {
+        tm_act32 = tm_act;
+    }
     // The same activations seen as [K/64 chunks][rows][64]: one box holds 16
     // rows x 4 chunks and lands as four consecutive 64-k tiles of 16 rows.
     const int act3d = (K % kCodeK) == 0 && !gather;
@@ -1467,6 +1607,10 @@ static moe_status launch_gemm(const uint16_t *act, int rows, int K, const uint8_
                 : cudaFuncSetAttribute(grouped_gemm_kernel<true, kMap>, a, smem_bytes) == cudaSuccess &&
                       cudaFuncSetAttribute(grouped_gemm_kernel<false, kMap>, a, smem_bytes) == cudaSuccess;
         if (!ok) return MOE_ERR_CUDA;
+        if (!kNv && kMap == kMapNone &&
+            cudaFuncSetAttribute(grouped_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 smem_bytes) != cudaSuccess)
+            return MOE_ERR_CUDA;
         attr_dev_mask.fetch_or(dev_bit, std::memory_order_release);
     }
     Params p;
@@ -1498,6 +1642,18 @@ static moe_status launch_gemm(const uint16_t *act, int rows, int K, const uint8_
     p.gather_k = gather_k;
     p.act_rows = act_rows;
     p.out_row = out_row;
+    // Bands over 32 rows in CTA pairs (each SM then loads half of every
+    // activation tile): with K8 activations and an even number of column
+    // tiles, when the bands average at least 64 rows (the wide mode's shapes)
+    // or when forced, and when the device keeps at least half its SMs' worth
+    // of pairs resident (the grid is that many pairs).
+    const int pmode = g_pair_mode.load(std::memory_order_relaxed);
+    int pair_grid = 0;
+    if (!kNv && kMap == kMapNone && act_k8 && p.n_tiles % 2 == 0 && pmode != 1 &&
+        (pmode == 2 || static_cast<long long>(rows) >= 64LL * E)) {
+        const int nc = pair_clusters(num_sms, smem_bytes);
+        if (2 * nc >= num_sms / 2) pair_grid = 2 * (nc < num_sms / 2 ? nc : num_sms / 2);
+    }
     // Two launches: bands of 1..32 rows, then bands of 33 or more (a launch
     // whose class has no band returns from its prologue).
     for (int cls = 0; cls < 2; ++cls) {
@@ -1509,14 +1665,17 @@ static moe_status launch_gemm(const uint16_t *act, int rows, int K, const uint8_
                     tm_codes, tm_act, tm_act3, tm_scales, tm_act64, p, ws2);
             else
                 grouped_gemm_nvfp4_kernel<false><<<num_sms, kThreads, smem_bytes, stream>>>(
-                    tm_codes, tm_act, tm_act3, tm_scales, tm_act64, p, ws2);
+                    tm_codes, tm_act, tm_act32, tm_scales, tm_act64, p, ws2);
         } else {
             if (cls == 0)
                 grouped_gemm_kernel<true, kMap><<<num_sms, kThreads, smem_bytes, stream>>>(
                     tm_codes, tm_act, tm_act3, tm_scales, tm_act64, p);
+            else if (pair_grid > 0)
+                grouped_gemm_pair_kernel<<<pair_grid, kThreads, smem_bytes, stream>>>(
+                    tm_codes, tm_act, tm_act32, tm_scales, tm_act64, p);
             else
                 grouped_gemm_kernel<false, kMap><<<num_sms, kThreads, smem_bytes, stream>>>(
-                    tm_codes, tm_act, tm_act3, tm_scales, tm_act64, p);
+                    tm_codes, tm_act, tm_act32, tm_scales, tm_act64, p);
         }
         if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
     }

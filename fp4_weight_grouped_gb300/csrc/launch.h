@@ -69,6 +69,10 @@ moe_status launch_grouped_gemm_nvfp4(const uint16_t *act, int rows, int K, const
                                      int out_bf16, int act_k8, int *status,
                                      uint64_t wait_limit_ns, cudaStream_t stream, int num_sms);
 
+// CTA-pair use for bands over 32 rows: 0 automatic, 1 never, 2 whenever the
+// shape allows (process-wide).
+void set_gemm_pairing(int mode);
+
 moe_status launch_decode_expert(const uint8_t *codes, const uint8_t *scales, int N, int K, int e,
                                 uint16_t *out, int *status, cudaStream_t stream);
 

@@ -445,6 +445,23 @@ MOE_API moe_status moe_layer_forward(const uint16_t *x, const int32_t *topk_ids,
                              void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * moe_set_gemm_pairing — how the MXFP4 grouped GEMMs (plain and fused SwiGLU)
+ * run bands of more than 32 rows; process-wide, for every later call.
+ *  MOE_PAIRING_AUTO  CTA pairs when K8 activations, an even number of column
+ *                    tiles (128 output rows, or 64 h columns, each) and rows
+ *                    >= 64 * E (the bands average at least 64 rows).
+ *  MOE_PAIRING_OFF   one CTA per work item.
+ *  MOE_PAIRING_ON    CTA pairs whenever K8 activations and an even tile count.
+ * In a CTA pair (a cluster of two CTAs on two SMs) each work item is a 256-row
+ * weight tile, 128 rows decoded by each CTA, and up to 256 token rows, half
+ * loaded by each CTA; the even CTA issues M = 256 tensor-core MMAs over both.
+ * Each SM thus loads half of every activation tile.  Results are identical
+ * either way (same products, same accumulation order).
+ */
+typedef enum { MOE_PAIRING_AUTO = 0, MOE_PAIRING_OFF = 1, MOE_PAIRING_ON = 2 } moe_pairing;
+MOE_API moe_status moe_set_gemm_pairing(int32_t mode);
+
+/*
  * moe_mxfp4_decode_expert — debug view of the GEMM's weight decode: writes
  * expert e's weights e2m1(code) * 2^(scale - 127) as bf16 [N, K], produced by
  * the same device routine the GEMM's converter warps run.  Used to check the

@@ -252,3 +252,67 @@ def test_many_ctas_sharing_weight_tiles_are_bitwise_repeatable(B, fused):
         c = rng.integers(0, 4096, 4000)
         ref, mag = oracle.grouped_gemm_sampled(act, codes, scales, gs, r, c)
         _tol_check(first.cpu().numpy()[r, c], ref, mag, what="shared weight tiles")
+
+
+# ------------------------------------------------------------- CTA pairs
+
+PAIR_CASES = {
+    # (bands, K, N, fused): even numbers of column tiles (pairs possible)
+    "bands_129_256_257": ([129, 0, 256, 257, 1], 512, 256, False),
+    "band_over_1000": ([1100, 3, 0, 200], 256, 512, False),
+    "k_tail_288": ([300, 40, 140], 288, 256, False),
+    "k_96": ([150, 7, 64], 96, 256, False),
+    "many_items": ([140, 260, 131, 500, 180, 129, 33, 48], 1024, 4096, False),
+    "scales_by_load": ([200, 0, 333], 768, 512, False),
+    "fused_wide": ([300, 129, 0, 40], 512, 2 * 256, True),
+    "fused_layer_like": ([190, 200, 0, 180, 230, 35], 1024, 2 * 2048, True),
+    "fused_partial_tiles": ([260, 7, 90], 288, 2 * 224, True),
+}
+
+
+@pytest.fixture
+def pairing(B):
+    yield B
+    B.set_gemm_pairing(B.MOE_PAIRING_AUTO)
+
+
+@pytest.mark.parametrize("name", sorted(PAIR_CASES))
+def test_cta_pairs_equal_single_ctas_and_match_oracle(pairing, name):
+    # The CTA-pair kernel (M = 256 MMAs over two SMs, each SM loading half of
+    # every activation tile) must give the single-CTA kernel's results bit for
+    # bit (same products, same accumulation order), and the oracle's.
+    B = pairing
+    gs, K, N, fused = PAIR_CASES[name]
+    act, codes, scales, gs = _explicit(gs, K, N, seed=13)
+    d = Dev(B, act, codes, scales, gs, k8=True)
+    run = (lambda: d.fused(True)) if fused else d.gemm
+    B.set_gemm_pairing(B.MOE_PAIRING_OFF)
+    single = run()
+    B.set_gemm_pairing(B.MOE_PAIRING_ON)
+    paired = run()
+    assert torch.equal(paired, single)
+    if fused:
+        h = k8_deinterleave(B.bits_from_bf16(paired))
+        y13, mag = oracle.grouped_gemm(act, codes, scales, gs)
+        check_swiglu_from_gemm(h, y13, mag, oracle.swiglu(y13), what=name)
+    else:
+        ref, mag = oracle.grouped_gemm(act, codes, scales, gs)
+        _tol_check(paired.cpu().numpy(), ref, mag, what=name)
+
+
+def test_cta_pairs_repeatable_with_many_ctas_per_weight_tile(pairing):
+    # As test_many_ctas_sharing_weight_tiles_are_bitwise_repeatable, in pairs.
+    B = pairing
+    act, codes, scales, gs = _explicit([3072, 40, 0, 300], 4096, 4096, seed=9)
+    d = Dev(B, act, codes, scales, gs, k8=True)
+    B.set_gemm_pairing(B.MOE_PAIRING_ON)
+    first = d.gemm().clone()
+    diffs = [int((d.gemm() != first).sum()) for _ in range(60)]
+    assert not any(diffs), f"launches differing from the first: {[i for i, n in enumerate(diffs) if n]}"
+    B.set_gemm_pairing(B.MOE_PAIRING_OFF)
+    assert torch.equal(d.gemm(), first)
+
+
+def test_pairing_mode_rejects_unknown_values(B):
+    with pytest.raises(B.MoeError):
+        B.set_gemm_pairing(3)
