@@ -64,8 +64,8 @@ FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
 # DRAM bytes (read + write) per launch of the w13 GEMM kernel measured by ncu for
 # each workload, with the hash of the kernel source they were taken on.  A
 # changed kernel reports traffic = null until re-measured.
-NCU_TRAFFIC = {"layer_T8192": 4 * (671395072 + 45165056)}   # the 64-expert, 2048-token capture x 4
-NCU_KERNEL_HASH = "9b07643e7dabd402"
+NCU_TRAFFIC = {"layer_T8192": 4 * (671368960 + 45664768)}   # the 64-expert, 2048-token capture x 4
+NCU_KERNEL_HASH = "f758ab7cbf2cf451"
 
 WEIGHT_BYTES_PER_ELEM = 17.0 / 32.0       # 4-bit code + one E8M0 byte per 32
 

@@ -79,8 +79,9 @@ constexpr int kWideNT = 256;                  // wide mode: tokens per work item
 // converters run far ahead of the tensor core, while the activation tiles
 // (re-read from L2 for every column tile) need the deeper prefetch.
 constexpr int kWideActSlots = 5;
-// Pair mode: activation slots of up to 16 KB (a CTA's half of 256 tokens).
-constexpr int kPairActSlots = 8;
+// Pair mode: activation slots of up to 16 KB (a CTA's half of 256 tokens); ten
+// leave room for two code stages, one per converter pair (measured best).
+constexpr int kPairActSlots = 10;
 constexpr int kStageK = 64;                   // K per decode / MMA stage
 constexpr int kSlots = 8;                     // A slots in TMEM (+ activation slots in smem)
 constexpr int kSlotsMax = 12;                 // bands <= 16 rows: three A slots per warpgroup
