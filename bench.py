@@ -536,7 +536,8 @@ def run_ours(args, rank, world, local):
         "gemm_flops_per_step": flops,
         "weight_bytes_per_step": wl.b13 + wl.b2,
         "roofline": {
-            "kernel": "grouped_gemm_kernel (w13 launch with SwiGLU epilogue)",
+            "kernel": "grouped GEMM, w13 launches with SwiGLU epilogue (bands over 32 rows: "
+                      "grouped_gemm_pair_kernel when CTA pairs apply, else grouped_gemm_kernel)",
             "bound": bound,
             "achieved": round(achieved_gb, 1) if bound == "hbm" else round(achieved_tf, 1),
             "peak": hbm if bound == "hbm" else bf16_burst,
