@@ -473,7 +473,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
     // work item.  Each takes 128 weight rows of the pair's 256-row tile (tile
     // 2t + rank of pair tile t) and half of the item's token rows; the even CTA
     // issues M = 256 MMAs over both, so each SM loads half of the activations.
-    static_assert(!kPair || (!kSplit && !kNv && kMap == kMapNone), "pair mode: MXFP4 wide bands");
+    static_assert(!kPair || (!kSplit && kMap == kMapNone), "pair mode: wide bands, no row maps");
     const uint32_t rank = kPair ? cluster_rank() : 0u;
     const int cta = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
     const int n_cta = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
@@ -1355,6 +1355,16 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_codes,
                                             nullptr);
 }
 
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+grouped_gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tm_codes,
+                               const __grid_constant__ CUtensorMap tm_act,
+                               const __grid_constant__ CUtensorMap tm_act3,
+                               const __grid_constant__ CUtensorMap tm_scales,
+                               const __grid_constant__ CUtensorMap tm_act64, const Params p,
+                               const float *__restrict__ ws2) {
+    gemm_body<true, false, kMapNone, true>(tm_codes, tm_act, tm_act3, tm_scales, tm_act64, p, ws2);
+}
+
 template <bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tm_codes,
@@ -1416,7 +1426,8 @@ static std::atomic<int> g_pair_mode{0};
 void set_gemm_pairing(int mode) { g_pair_mode.store(mode, std::memory_order_relaxed); }
 
 // Clusters of two that the device can keep resident at once with the pair
-// kernel's shared memory (looked up once per device).
+// kernel's shared memory (looked up once per device and weight format).
+template <bool kNv>
 static int pair_clusters(int num_sms, int smem_bytes) {
     static std::atomic<int> cached[64];
     int dev = 0;
@@ -1428,7 +1439,10 @@ static int pair_clusters(int num_sms, int smem_bytes) {
         cfg.blockDim = dim3(gemm::kThreads);
         cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
         int clusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&clusters, gemm::grouped_gemm_pair_kernel, &cfg) != cudaSuccess)
+        const cudaError_t e =
+            kNv ? cudaOccupancyMaxActiveClusters(&clusters, gemm::grouped_gemm_nvfp4_pair_kernel, &cfg)
+                : cudaOccupancyMaxActiveClusters(&clusters, gemm::grouped_gemm_pair_kernel, &cfg);
+        if (e != cudaSuccess)
             clusters = 0;
         n = clusters > 0 ? clusters : -1;
         cached[dev].store(n, std::memory_order_release);
@@ -1608,9 +1622,12 @@ static moe_status launch_gemm(const uint16_t *act, int rows, int K, const uint8_
                 : cudaFuncSetAttribute(grouped_gemm_kernel<true, kMap>, a, smem_bytes) == cudaSuccess &&
                       cudaFuncSetAttribute(grouped_gemm_kernel<false, kMap>, a, smem_bytes) == cudaSuccess;
         if (!ok) return MOE_ERR_CUDA;
-        if (!kNv && kMap == kMapNone &&
-            cudaFuncSetAttribute(grouped_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 smem_bytes) != cudaSuccess)
+        if (kMap == kMapNone &&
+            (kNv ? cudaFuncSetAttribute(grouped_gemm_nvfp4_pair_kernel,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes)
+                 : cudaFuncSetAttribute(grouped_gemm_pair_kernel,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes)) !=
+                cudaSuccess)
             return MOE_ERR_CUDA;
         attr_dev_mask.fetch_or(dev_bit, std::memory_order_release);
     }
@@ -1650,9 +1667,9 @@ static moe_status launch_gemm(const uint16_t *act, int rows, int K, const uint8_
     // of pairs resident (the grid is that many pairs).
     const int pmode = g_pair_mode.load(std::memory_order_relaxed);
     int pair_grid = 0;
-    if (!kNv && kMap == kMapNone && act_k8 && p.n_tiles % 2 == 0 && pmode != 1 &&
+    if (kMap == kMapNone && act_k8 && p.n_tiles % 2 == 0 && pmode != 1 &&
         (pmode == 2 || static_cast<long long>(rows) >= 64LL * E)) {
-        const int nc = pair_clusters(num_sms, smem_bytes);
+        const int nc = pair_clusters<kNv>(num_sms, smem_bytes);
         if (2 * nc >= num_sms / 2) pair_grid = 2 * (nc < num_sms / 2 ? nc : num_sms / 2);
     }
     // Two launches: bands of 1..32 rows, then bands of 33 or more (a launch
@@ -1664,6 +1681,9 @@ static moe_status launch_gemm(const uint16_t *act, int rows, int K, const uint8_
             if (cls == 0)
                 grouped_gemm_nvfp4_kernel<true><<<num_sms, kThreads, smem_bytes, stream>>>(
                     tm_codes, tm_act, tm_act3, tm_scales, tm_act64, p, ws2);
+            else if (pair_grid > 0)
+                grouped_gemm_nvfp4_pair_kernel<<<pair_grid, kThreads, smem_bytes, stream>>>(
+                    tm_codes, tm_act, tm_act32, tm_scales, tm_act64, p, ws2);
             else
                 grouped_gemm_nvfp4_kernel<false><<<num_sms, kThreads, smem_bytes, stream>>>(
                     tm_codes, tm_act, tm_act32, tm_scales, tm_act64, p, ws2);

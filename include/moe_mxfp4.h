@@ -445,8 +445,9 @@ MOE_API moe_status moe_layer_forward(const uint16_t *x, const int32_t *topk_ids,
                              void *workspace, size_t workspace_bytes, void *stream);
 
 /*
- * moe_set_gemm_pairing — how the MXFP4 grouped GEMMs (plain and fused SwiGLU)
- * run bands of more than 32 rows; process-wide, for every later call.
+ * moe_set_gemm_pairing — how the grouped GEMMs (MXFP4 plain, block 512 and
+ * fused SwiGLU, and NVFP4) run bands of more than 32 rows; process-wide, for
+ * every later call.
  *  MOE_PAIRING_AUTO  CTA pairs when K8 activations, an even number of column
  *                    tiles (128 output rows, or 64 h columns, each) and rows
  *                    >= 64 * E (the bands average at least 64 rows).

@@ -158,3 +158,29 @@ def test_nvfp4_gemm_repeatable(B):
     a, _ = _nv_gpu(B, act, codes, s16, ws2, gs)
     b, _ = _nv_gpu(B, act, codes, s16, ws2, gs)
     assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+def test_nvfp4_cta_pairs_equal_single_ctas(B):
+    # Bands over 32 rows with an even tile count run in CTA pairs: identical
+    # to one CTA per item, bit for bit.
+    rng = np.random.default_rng(21)
+    gs = np.array([300, 129, 0, 40, 257], np.int32)
+    K, N = 512, 512
+    act = inputs.normal_bf16(21, 1, (int(gs.sum()), K))
+    codes = rng.integers(0, 256, (len(gs), N, K // 2), dtype=np.uint8)
+    s16 = rng.integers(0x28, 0x48, (len(gs), N, K // 16), dtype=np.uint8)
+    ws2 = np.ldexp(1.0, rng.integers(-6, 3, len(gs))).astype(np.float32)
+    k8 = act.reshape(act.shape[0], K // 8, 2, 4).swapaxes(-1, -2).reshape(act.shape)
+    d = [B.bf16_from_bits(k8, DEV), B.to_device(codes, DEV), B.to_device(s16, DEV),
+         B.to_device(ws2, DEV), B.to_device(gs, DEV)]
+    try:
+        B.set_gemm_pairing(B.MOE_PAIRING_OFF)
+        single = B.nvfp4_grouped_gemm(*d, act_layout=B.MOE_ACT_K8_INTERLEAVED)
+        B.set_gemm_pairing(B.MOE_PAIRING_ON)
+        paired = B.nvfp4_grouped_gemm(*d, act_layout=B.MOE_ACT_K8_INTERLEAVED)
+    finally:
+        B.set_gemm_pairing(B.MOE_PAIRING_AUTO)
+    assert torch.equal(paired, single)
+    ref, mag = oracle.nvfp4_grouped_gemm(act, codes, s16, ws2, gs)
+    diff = np.abs(paired.cpu().numpy().astype(np.float64) - ref)
+    assert np.all(diff <= 1e-5 * mag + 1e-6), float((diff / (1e-5 * mag + 1e-6)).max())
