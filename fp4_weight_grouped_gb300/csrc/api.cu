@@ -462,7 +462,7 @@ moe_status moe_mxfp4_to_nvfp4(const uint8_t *scales, int32_t E, int32_t N, int32
         scales, E, N, K, e4m3_scales, weight_scale_2,
         reinterpret_cast<unsigned long long *>(out_of_range),
         reinterpret_cast<int *>(static_cast<uint8_t *>(workspace) + kStatusBytes),
-        status_word(workspace), static_cast<cudaStream_t>(stream), sms, &launches);
+        status_word(workspace), kWaitLimitNs, static_cast<cudaStream_t>(stream), sms, &launches);
     g_last_launches = launches;
     return st;
 }

@@ -194,6 +194,17 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// Untiled bulk copy of `bytes` contiguous bytes from global into shared memory;
+// both addresses 16-byte aligned, bytes a multiple of 16.  Completion is
+// signalled as transaction bytes on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // ------------------------------------------------------------ CTA clusters
 
 // Rank of this CTA in its cluster.
@@ -225,6 +236,19 @@ __device__ __forceinline__ uint32_t cluster_addr(const void *p, uint32_t rank) {
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
     asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
                  : "memory");
+}
+
+// Asynchronous store of two 32-bit words into shared memory of a CTA of the
+// cluster (addresses from cluster_addr); the 8 bytes complete as transaction
+// bytes on that CTA's barrier `cluster_bar`, so the receiver learns of the
+// data by waiting on its own barrier, with no cluster-wide fence or barrier.
+__device__ __forceinline__ void st_async_v2(uint32_t cluster_dst, uint32_t a, uint32_t b,
+                                            uint32_t cluster_bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.u32 [%0], {%1, %2}, [%3];" ::"r"(
+            cluster_dst),
+        "r"(a), "r"(b), "r"(cluster_bar)
+        : "memory");
 }
 
 // -------------------------------------------------------------------- tcgen05

@@ -78,8 +78,8 @@ moe_status launch_decode_expert(const uint8_t *codes, const uint8_t *scales, int
 
 moe_status launch_mxfp4_to_nvfp4(const uint8_t *scales, int E, int N, int K, uint8_t *e4m3,
                                  float *weight_scale_2, unsigned long long *out_of_range,
-                                 int *kmax_scratch, int *status, cudaStream_t stream, int num_sms,
-                                 int *launches);
+                                 int *kmax_scratch, int *status, uint64_t wait_limit_ns,
+                                 cudaStream_t stream, int num_sms, int *launches);
 
 moe_status launch_bounded_wait(uint64_t limit_ns, int *status, cudaStream_t stream);
 

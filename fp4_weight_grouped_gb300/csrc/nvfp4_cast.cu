@@ -12,20 +12,26 @@
 //
 // Every E4M3 byte depends on the expert's maximum, so the data is read, reduced
 // across the expert, then converted.  Two forms:
-//   * one pass (the usual shapes): one thread-block cluster of up to 16 CTAs
-//     of 128 threads per expert.  Every thread loads its 256 scale bytes into
-//     registers (16 loads of 16 bytes in flight), the CTAs of the cluster
-//     exchange their maxima through distributed shared memory, and each thread
-//     converts from its registers and stores.  The scales are read from HBM
-//     once: 3 bytes of traffic per scale byte, the algorithmic minimum.
+//   * one pass (the usual shapes): persistent thread-block clusters of C <= 8
+//     CTAs, each CTA owning one 64 KiB slice of an expert's scales, cluster c
+//     converting experts c, c + #clusters, ...  A slice arrives by bulk copy
+//     (cp.async.bulk) into shared memory, every thread moves its 256 bytes into
+//     registers, and the copy of the cluster's next expert starts at once, so it
+//     overlaps this expert's conversion and stores.  The CTAs of the cluster
+//     exchange their maxima (and the in-range counts of the previous expert) by
+//     asynchronous stores into each peer's shared memory that complete on the
+//     peer's mbarrier: no cluster barrier inside the loop, whose release would
+//     make every thread wait for its output stores.  The scales are read from
+//     HBM once: 3 bytes of traffic per scale byte, the algorithmic minimum.
 //   * two passes (an expert over 512 KiB, or buffers off 16-byte boundaries):
 //     a per-expert maximum into scratch, then the conversion.
 // Four scale bytes are converted at a time with byte-parallel integer
 // arithmetic in one 32-bit register (below, convert_word).  Results are
 // integers, identical from run to run.
-#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <atomic>
 
 #include "device_common.cuh"
 #include "launch.h"
@@ -33,18 +39,15 @@
 namespace moe {
 namespace cast {
 
-namespace cg = cooperative_groups;
-
 constexpr int kThreads = 256;
 constexpr int kBlocksPerSM = 8;            // two-pass grid: blocks per SM
 constexpr long long kMinChunk = 4096;      // two-pass grid: smallest chunk
-constexpr int kRegVec = 16;                // one pass: 16-byte words per thread
-// One pass: threads per CTA.  A CTA holds 32 KiB in registers and a cluster of
-// up to 16 CTAs (non-portable size, opted in) covers an expert's 512 KiB;
-// four or five CTAs fit an SM, so one expert's stores overlap another's loads.
-constexpr int kOneNT = 128;
-constexpr long long kSlice = static_cast<long long>(kOneNT) * kRegVec * 16;
-constexpr int kMaxCluster = kOneNT == 256 ? 8 : 16;
+// One pass: 256 threads per CTA, 32 eight-byte words each: a 64 KiB slice per
+// CTA, two CTAs per SM, clusters of up to 8 CTAs (512 KiB per expert).
+constexpr int kOneNT = 256;
+constexpr int kOneWords = 32;
+constexpr long long kSlice = static_cast<long long>(kOneNT) * kOneWords * 8;
+constexpr int kMaxCluster = 8;
 constexpr uint32_t kOnes = 0x01010101u, kHigh = 0x80808080u;
 
 __device__ __forceinline__ uint32_t max_byte4(uint32_t w) {
@@ -117,71 +120,133 @@ __device__ __forceinline__ T block_reduce(T v, Op op, T *warp_vals) {
 
 // ------------------------------------------------------------------ one pass
 
-// Grid (C, E) with clusters of (C, 1, 1): cluster e converts expert e; CTA c
-// holds bytes [c * kSlice, min((c + 1) * kSlice, per_expert)) in registers.
-// Needs per_expert % 16 == 0, per_expert <= C * kSlice, 16-byte aligned bases.
-__global__ void __launch_bounds__(kOneNT, kOneNT == 256 ? 2 : 4)
-onepass_kernel(const uint8_t *__restrict__ scales, long long per_expert, uint8_t *__restrict__ e4m3,
-               float *__restrict__ weight_scale_2, unsigned long long *__restrict__ out_of_range,
-               int *status) {
-    cg::cluster_group cluster = cg::this_cluster();
-    const int e = blockIdx.y;
-    const unsigned rank = cluster.block_rank();
-    const unsigned csize = cluster.num_blocks();
-    __shared__ uint32_t expert_max, expert_in_range;   // gathered from the whole cluster
-    __shared__ uint32_t warp_vals[kOneNT / 32];
-    if (threadIdx.x == 0) {
-        expert_max = 0;
-        expert_in_range = 0;
-    }
-    // Arrive now, wait after the loads: the peers' maxima are written into this
-    // CTA's expert_max only once every CTA of the cluster has started and
-    // initialised it, and the barrier's latency hides behind the loads.
+// Shared memory of the one-pass kernel.
+struct OnePassSmem {
+    uint8_t slice[kSlice];                 // this CTA's slice of the current expert
+    uint64_t full[2];                      // bulk copy of use k: full[k & 1], parity (k >> 1) & 1
+    uint64_t xfull[2];                     // exchange of use k: the same scheme
+    uint32_t xch[2][kMaxCluster][2];       // (maximum, in-range count) from each CTA
+    uint32_t wmax[kOneNT / 32], wcnt[kOneNT / 32];
+};
 
+// Grid (C * clusters) with clusters of (C, 1, 1), C = ceil(per_expert / kSlice):
+// CTA rank r holds bytes [r * kSlice, min((r + 1) * kSlice, per_expert)) of
+// every expert its cluster converts.  Needs per_expert % 16 == 0, 16-byte
+// aligned bases.
+__global__ void __launch_bounds__(kOneNT, 2)
+onepass_kernel(const uint8_t *__restrict__ scales, long long per_expert, int E, uint8_t *__restrict__ e4m3,
+               float *__restrict__ weight_scale_2, unsigned long long *__restrict__ out_of_range,
+               int *status, uint64_t limit_ns) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    OnePassSmem &sm = *reinterpret_cast<OnePassSmem *>(smem_raw);
+    uint32_t C;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(C));
+    const uint32_t rank = cluster_rank();
+    const int n_clusters = static_cast<int>(gridDim.x / C);
+    const int first = static_cast<int>(blockIdx.x / C);
+    const int tid = threadIdx.x;
     const long long lo = static_cast<long long>(rank) * kSlice;
-    const long long nvec = max(0LL, min(kSlice, per_expert - lo)) / 16;
-    const uint4 *src = reinterpret_cast<const uint4 *>(scales + static_cast<long long>(e) * per_expert + lo);
-    uint4 w[kRegVec];
-#pragma unroll
-    for (int u = 0; u < kRegVec; ++u) {
-        const long long j = threadIdx.x + static_cast<long long>(u) * kOneNT;
-        w[u] = j < nvec ? __ldcs(src + j) : make_uint4(0, 0, 0, 0);
-    }
-    uint32_t acc = 0;
-#pragma unroll
-    for (int u = 0; u < kRegVec; ++u) acc = max_byte16(acc, w[u]);
-    const uint32_t m_warp = __reduce_max_sync(0xffffffffu, max_byte4(acc));
-    const uint32_t m_cta =
-        block_reduce<kOneNT>(m_warp, [](uint32_t a, uint32_t b) { return max(a, b); }, warp_vals);
-    cluster.sync();                                 // every CTA's expert_max is initialised
-    if (threadIdx.x < csize) atomicMax(cluster.map_shared_rank(&expert_max, threadIdx.x), m_cta);
-    cluster.sync();                                 // every CTA's maximum has arrived everywhere;
-                                                    // no shared memory of a peer is used after this
-    const uint32_t m = expert_max;
-    const uint32_t M = m * kOnes;
-    uint4 *dst = reinterpret_cast<uint4 *>(e4m3 + 2 * (static_cast<long long>(e) * per_expert + lo));
-    uint32_t in_range = 0;
-#pragma unroll
-    for (int u = 0; u < kRegVec; ++u) {
-        const long long j = threadIdx.x + static_cast<long long>(u) * kOneNT;
-        if (j < nvec) {
-            uint4 o0, o1;
-            convert16(w[u], M, in_range, o0, o1);
-            __stcs(dst + 2 * j, o0);
-            __stcs(dst + 2 * j + 1, o1);
+    const uint32_t len = static_cast<uint32_t>(max(0LL, min(kSlice, per_expert - lo)));
+    const int nwords = static_cast<int>(len / 8);
+    if (tid == 0) {
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&sm.full[b], 1);
+            mbar_init(&sm.xfull[b], 1);
         }
+        mbar_fence_init();
     }
-    const uint32_t r_warp = __reduce_add_sync(0xffffffffu, in_range);
-    __syncthreads();                                // warp_vals reused
-    const uint32_t r_cta =
-        block_reduce<kOneNT>(r_warp, [](uint32_t a, uint32_t b) { return a + b; }, warp_vals);
-    if (threadIdx.x == 0) atomicAdd(cluster.map_shared_rank(&expert_in_range, 0), r_cta);
-    cluster.sync();                                 // all counts are in CTA 0
-    if (rank == 0 && threadIdx.x == 0) {
-        out_of_range[e] = static_cast<unsigned long long>(per_expert) - expert_in_range;
-        weight_scale_2[e] = weight_scale_2_of(m);
-        if (m == 255u) set_status(status, MOE_ERR_DATA);
+    __syncthreads();
+    // Use k of the slice buffer: expert e's slice, in 16 KiB copies.
+    auto load = [&](int e, int k) {
+        uint64_t *bar = &sm.full[k & 1];
+        mbar_arrive_expect_tx(bar, len);
+        const uint8_t *src = scales + static_cast<long long>(e) * per_expert + lo;
+        for (uint32_t off = 0; off < len; off += 16384u)
+            bulk_load(smem_u32(sm.slice + off), src + off, min(16384u, len - off), bar);
+    };
+    // Exchange k: block maximum and count, one message to every CTA of the
+    // cluster; starts the copy of expert e_next once the slice is free (every
+    // thread has passed the block barrier, so it holds its words in registers).
+    auto exchange = [&](int k, uint32_t m_warp, uint32_t c_warp, int e_next) {
+        if ((tid & 31) == 0) {
+            sm.wmax[tid >> 5] = m_warp;
+            sm.wcnt[tid >> 5] = c_warp;
+        }
+        __syncthreads();
+        if (tid == 0 && e_next < E) load(e_next, k + 1);
+        const int xb = k & 1;
+        if (tid < static_cast<int>(C)) {
+            uint32_t m = 0, c = 0;
+            for (int w = 0; w < kOneNT / 32; ++w) {
+                m = max(m, sm.wmax[w]);
+                c += sm.wcnt[w];
+            }
+            if (tid == 0) mbar_arrive_expect_tx(&sm.xfull[xb], 8u * C);
+            st_async_v2(cluster_addr(&sm.xch[xb][rank][0], tid), m, c, cluster_addr(&sm.xfull[xb], tid));
+        }
+        wait_bounded(&sm.xfull[xb], (k >> 1) & 1, nullptr, status, limit_ns);
+    };
+    auto count_sum = [&](int xb) {
+        uint32_t t = 0;
+        for (uint32_t r = 0; r < C; ++r) t += sm.xch[xb][r][1];
+        return t;
+    };
+    if (tid == 0 && first < E) load(first, 0);
+    // Every CTA's barriers are initialised before a peer's first message.
+    cluster_sync();
+    uint32_t prev_in_range = 0;            // this thread's count for the previous expert
+    int k = 0, e_prev = -1;
+    for (int e = first; e < E; e += n_clusters, ++k) {
+        if (!wait_bounded(&sm.full[k & 1], (k >> 1) & 1, nullptr, status, limit_ns))
+            wait_bounded(&sm.full[k & 1], (k >> 1) & 1, nullptr, nullptr, limit_ns);   // drain
+        const uint2 *s = reinterpret_cast<const uint2 *>(sm.slice);
+        uint2 v[kOneWords];
+        uint32_t acc = 0;
+#pragma unroll
+        for (int u = 0; u < kOneWords; ++u) {
+            const int j = tid + u * kOneNT;
+            v[u] = j < nwords ? s[j] : make_uint2(0u, 0u);
+            acc = __vmaxu4(acc, __vmaxu4(v[u].x, v[u].y));
+        }
+        // The next bulk copy (async proxy) overwrites what these reads saw.
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        exchange(k, __reduce_max_sync(0xffffffffu, max_byte4(acc)),
+                 __reduce_add_sync(0xffffffffu, prev_in_range), e + n_clusters);
+        const int xb = k & 1;
+        uint32_t m = 0;
+        for (uint32_t r = 0; r < C; ++r) m = max(m, sm.xch[xb][r][0]);
+        if (rank == 0 && tid == 0) {
+            if (e_prev >= 0)
+                out_of_range[e_prev] = static_cast<unsigned long long>(per_expert) - count_sum(xb);
+            weight_scale_2[e] = weight_scale_2_of(m);
+            if (m == 255u) set_status(status, MOE_ERR_DATA);
+        }
+        const uint32_t M = m * kOnes;
+        uint32_t in_range = 0;
+        uint4 *dst = reinterpret_cast<uint4 *>(e4m3 + 2 * (static_cast<long long>(e) * per_expert + lo));
+        // 8 scale bytes -> 16 output bytes per word: a warp stores 512
+        // contiguous bytes per instruction.
+#pragma unroll
+        for (int u = 0; u < kOneWords; ++u) {
+            const int j = tid + u * kOneNT;
+            if (j < nwords) {
+                const uint32_t a = convert_word(v[u].x, M, in_range);
+                const uint32_t b = convert_word(v[u].y, M, in_range);
+                __stcs(dst + j, make_uint4(prmt(a, 0u, 0x1100u), prmt(a, 0u, 0x3322u), prmt(b, 0u, 0x1100u),
+                                           prmt(b, 0u, 0x3322u)));
+            }
+        }
+        prev_in_range = in_range;
+        e_prev = e;
     }
+    // The last expert's counts (every cluster has at least one expert).
+    if (k > 0) {
+        exchange(k, 0u, __reduce_add_sync(0xffffffffu, prev_in_range), E);
+        if (rank == 0 && tid == 0)
+            out_of_range[e_prev] = static_cast<unsigned long long>(per_expert) - count_sum(k & 1);
+    }
+    // No CTA leaves while a peer may still address its shared memory.
+    cluster_sync();
 }
 
 // ---------------------------------------------------------------- two passes
@@ -302,33 +367,43 @@ bool nvfp4_cast_one_pass(const void *scales, const void *e4m3, int N, int K) {
 
 moe_status launch_mxfp4_to_nvfp4(const uint8_t *scales, int E, int N, int K, uint8_t *e4m3,
                                  float *weight_scale_2, unsigned long long *out_of_range,
-                                 int *kmax_scratch, int *status, cudaStream_t stream, int num_sms,
-                                 int *launches) {
+                                 int *kmax_scratch, int *status, uint64_t wait_limit_ns,
+                                 cudaStream_t stream, int num_sms, int *launches) {
     using namespace cast;
     *launches = 0;
     const long long per_expert = static_cast<long long>(N) * (K / 32);
     if (nvfp4_cast_one_pass(scales, e4m3, N, K)) {
-        const unsigned csize = static_cast<unsigned>((per_expert + kSlice - 1) / kSlice);
+        const int C = static_cast<int>((per_expert + kSlice - 1) / kSlice);
+        const int smem = static_cast<int>(sizeof(OnePassSmem));
+        static const cudaError_t attr_ok =
+            cudaFuncSetAttribute(onepass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (attr_ok != cudaSuccess) return MOE_ERR_CUDA;
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(csize, static_cast<unsigned>(E), 1);
-        cfg.blockDim = dim3(kOneNT, 1, 1);
-        if (kMaxCluster > 8) {
-            // Clusters beyond the portable 8 need the opt-in (set once per process).
-            static const cudaError_t opt = cudaFuncSetAttribute(
-                onepass_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-            if (opt != cudaSuccess) return MOE_ERR_CUDA;
-        }
-        cfg.dynamicSmemBytes = 0;
-        cfg.stream = stream;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = csize;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(C);
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, onepass_kernel, scales, per_expert, e4m3, weight_scale_2,
-                               out_of_range, status) != cudaSuccess)
+        cfg.blockDim = dim3(kOneNT, 1, 1);
+        cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+        cfg.stream = stream;
+        // Resident clusters of this size, per device (queried once).
+        static std::atomic<int> resident[64][kMaxCluster + 1];
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+        int nc = dev < 64 ? resident[dev][C].load(std::memory_order_relaxed) : 0;
+        if (nc <= 0) {
+            cfg.gridDim = dim3(static_cast<unsigned>(C * num_sms), 1, 1);
+            if (cudaOccupancyMaxActiveClusters(&nc, onepass_kernel, &cfg) != cudaSuccess || nc <= 0)
+                return MOE_ERR_CUDA;
+            if (dev < 64) resident[dev][C].store(nc, std::memory_order_relaxed);
+        }
+        nc = min(nc, E);
+        cfg.gridDim = dim3(static_cast<unsigned>(C * nc), 1, 1);
+        if (cudaLaunchKernelEx(&cfg, onepass_kernel, scales, per_expert, E, e4m3, weight_scale_2,
+                               out_of_range, status, wait_limit_ns) != cudaSuccess)
             return MOE_ERR_CUDA;
         *launches = 1;
         return MOE_OK;

@@ -506,9 +506,11 @@ MOE_API size_t moe_nvfp4_cast_workspace_bytes(int32_t E);
  *                  16-byte aligned; its status word as for every call.
  * Launches one kernel when each expert's scale tensor (N * K/32 bytes) is a
  * multiple of 16 bytes and at most 512 KiB and both byte buffers are 16-byte
- * aligned: a cluster of up to 16 CTAs per expert reads the scales once.
- * Otherwise two kernels (per-expert maximum into the workspace, then the
- * conversion).  Results are exact integers, identical from run to run.
+ * aligned: persistent clusters of up to 8 CTAs (64 KiB of an expert each) read
+ * the scales once.  Otherwise two kernels (per-expert maximum into the
+ * workspace, then the conversion).  A bulk copy or a message between the CTAs
+ * of a cluster that does not arrive within 2 s records MOE_ERR_TIMEOUT.
+ * Results are exact integers, identical from run to run.
  */
 MOE_API moe_status moe_mxfp4_to_nvfp4(const uint8_t *scales, int32_t E, int32_t N, int32_t K,
                                       uint8_t *e4m3_scales, float *weight_scale_2,

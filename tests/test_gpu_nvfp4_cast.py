@@ -93,6 +93,11 @@ CASES = {
     "cluster_2": ((3, 1000, 100), 100, 127),
     # One pass with 5 CTAs per cluster.
     "cluster_5": ((2, 2560, 128), 110, 125),
+    # One pass with 8 CTAs per cluster, the last one partly filled; fewer experts
+    # than resident clusters.
+    "cluster_8_ragged": ((3, 4000, 128), 100, 127),
+    # The w2 scale tensor of the workloads: clusters of 4, many experts per cluster.
+    "w2_shape": ((256, 4096, 64), 117, 125),
     # Aligned but over 512 KiB per expert: two passes, 16-byte vector path.
     "two_pass_aligned": ((2, 4096, 160), 110, 127),
     # The same over every byte but the NaN: two passes with blocks out of range.
