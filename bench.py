@@ -64,18 +64,26 @@ FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
 # DRAM bytes (read + write) per launch of the w13 GEMM kernel measured by ncu for
 # each workload, with the hash of the kernel source they were taken on.  A
 # changed kernel reports traffic = null until re-measured.
-NCU_TRAFFIC = {"layer_T8192": 4 * (671368960 + 45664768)}   # the 64-expert, 2048-token capture x 4
-NCU_KERNEL_HASH = "f758ab7cbf2cf451"
+NCU_TRAFFIC = {"layer_T8192": 4 * (671451392 + 44724992)}   # the 64-expert, 2048-token capture x 4
+NCU_KERNEL_HASH = "c0848f16b07fb6fc"
+# The same for the scale cast kernel (a capture of the full cast_w13 launch; the
+# writes still in L2 when the kernel ends are not counted).
+NCU_CAST_TRAFFIC = 134278912 + 207835392
+NCU_CAST_HASH = "5b5274bcc8477fba"
 
 WEIGHT_BYTES_PER_ELEM = 17.0 / 32.0       # 4-bit code + one E8M0 byte per 32
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(files=("grouped_gemm.cu", "mxfp4_decode.cuh", "device_common.cuh")) -> str:
     h = hashlib.sha256()
-    for f in ("grouped_gemm.cu", "mxfp4_decode.cuh", "device_common.cuh"):
+    for f in files:
         with open(os.path.join(ROOT, "fp4_weight_grouped_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
+
+
+def cast_source_hash() -> str:
+    return kernel_source_hash(("nvfp4_cast.cu", "device_common.cuh"))
 
 
 def load_peaks():
@@ -668,10 +676,13 @@ def run_cast(args, rank, world, local):
                    "shape": list(CAST_SHAPE),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "256 MiB L2 flush before every timed cast, outside its events"},
-        "roofline": {"kernel": "onepass_kernel (one cast call)" if launches_per_cast == 1
+        "roofline": {"kernel": "onepass_kernel (one cast call: persistent clusters)" if launches_per_cast == 1
                      else "kmax_kernel + convert_kernel (one cast call, timed together)",
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                     "frac": round(achieved / hbm, 4), "traffic": None, "peak_source": peak_src,
+                     "frac": round(achieved / hbm, 4),
+                     "traffic": NCU_CAST_TRAFFIC if (launches_per_cast == 1 and
+                                                     NCU_CAST_HASH == cast_source_hash()) else None,
+                     "peak_source": peak_src,
                      "algorithmic_bytes_per_launch": alg, "avg_launch_ms": round(launch_ms, 5)},
         "e2e": {"value": round(whole_job_rate(alg, e2e_ms, world) / 1e9, 1), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": int(h2d),

@@ -1233,12 +1233,15 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             }
             const bool slots_ready = mbar_test_wait(&slot_empty[wg], sphase ^ 1u);
-            {
-                Ring nx = code;
-                nx.next(CS);
-                nx.next(CS);
-                code_ready = c + 2 < total_cs && mbar_test_wait(&code_full[nx.slot], nx.phase);
+            // Ring position of this pair's next code stage, c + 2 (one wrap at
+            // most: the depth is at least 2).
+            Ring nx = code;
+            nx.slot += 2;
+            if (nx.slot >= CS) {
+                nx.slot -= CS;
+                nx.phase ^= 1u;
             }
+            code_ready = c + 2 < total_cs && mbar_test_wait(&code_full[nx.slot], nx.phase);
             // Scale bytes 0..128 take one bf16 FMA, 129..252 two, 253..255 are
             // errors; the warp agrees on the path.  A byte is above 128 exactly
             // when its top bit and one of its low seven bits are set.
@@ -1297,8 +1300,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
                 }
             }
             // Next code stage of this pair: c + 2.
-            code.next(CS);
-            code.next(CS);
+            code = nx;
             sphase ^= 1u;
             m += 2;
             while (m >= KT4) {
