@@ -440,6 +440,10 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
                                           const CUtensorMap &tm_act3, const CUtensorMap &tm_scales,
                                           const CUtensorMap &tm_act64, const Params &p,
                                           const float *ws2) {
+    // A programmatic dependent launch that follows may start as this grid's
+    // CTAs retire.  Only the second band-class launch of the same GEMM is
+    // launched that way; it depends on nothing this grid writes.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned start, derived from the shared array itself so that the
     // compiler keeps the shared address space (shared loads, not generic ones).
@@ -1675,32 +1679,55 @@ static moe_status launch_gemm(const uint16_t *act, int rows, int K, const uint8_
         if (2 * nc >= num_sms / 2) pair_grid = 2 * (nc < num_sms / 2 ? nc : num_sms / 2);
     }
     // Two launches: bands of 1..32 rows, then bands of 33 or more (a launch
-    // whose class has no band returns from its prologue).
+    // whose class has no band returns from its prologue).  The second is a
+    // programmatic dependent launch: the two read the same inputs and write
+    // disjoint output rows, so its CTAs may start on the SMs the first one's
+    // CTAs leave (every kernel here signals its dependents on entry).  The
+    // first launch, and whatever follows the second, keep full stream order:
+    // the first starts after all earlier work, so the second does too.
     for (int cls = 0; cls < 2; ++cls) {
         p.band_lo = cls == 0 ? 1 : kPartCols + 1;
         p.band_hi = cls == 0 ? kPartCols : INT32_MAX;
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
+        cfg.stream = stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = cls == 1 ? 1 : 0;
+        cudaError_t err;
         if constexpr (kNv) {
-            if (cls == 0)
-                grouped_gemm_nvfp4_kernel<true><<<num_sms, kThreads, smem_bytes, stream>>>(
-                    tm_codes, tm_act, tm_act3, tm_scales, tm_act64, p, ws2);
-            else if (pair_grid > 0)
-                grouped_gemm_nvfp4_pair_kernel<<<pair_grid, kThreads, smem_bytes, stream>>>(
-                    tm_codes, tm_act, tm_act32, tm_scales, tm_act64, p, ws2);
-            else
-                grouped_gemm_nvfp4_kernel<false><<<num_sms, kThreads, smem_bytes, stream>>>(
-                    tm_codes, tm_act, tm_act32, tm_scales, tm_act64, p, ws2);
+            if (cls == 0) {
+                cfg.gridDim = dim3(num_sms);
+                err = cudaLaunchKernelEx(&cfg, grouped_gemm_nvfp4_kernel<true>, tm_codes, tm_act, tm_act3,
+                                         tm_scales, tm_act64, p, ws2);
+            } else if (pair_grid > 0) {
+                cfg.gridDim = dim3(pair_grid);
+                err = cudaLaunchKernelEx(&cfg, grouped_gemm_nvfp4_pair_kernel, tm_codes, tm_act, tm_act32,
+                                         tm_scales, tm_act64, p, ws2);
+            } else {
+                cfg.gridDim = dim3(num_sms);
+                err = cudaLaunchKernelEx(&cfg, grouped_gemm_nvfp4_kernel<false>, tm_codes, tm_act, tm_act32,
+                                         tm_scales, tm_act64, p, ws2);
+            }
         } else {
-            if (cls == 0)
-                grouped_gemm_kernel<true, kMap><<<num_sms, kThreads, smem_bytes, stream>>>(
-                    tm_codes, tm_act, tm_act3, tm_scales, tm_act64, p);
-            else if (pair_grid > 0)
-                grouped_gemm_pair_kernel<<<pair_grid, kThreads, smem_bytes, stream>>>(
-                    tm_codes, tm_act, tm_act32, tm_scales, tm_act64, p);
-            else
-                grouped_gemm_kernel<false, kMap><<<num_sms, kThreads, smem_bytes, stream>>>(
-                    tm_codes, tm_act, tm_act32, tm_scales, tm_act64, p);
+            if (cls == 0) {
+                cfg.gridDim = dim3(num_sms);
+                err = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<true, kMap>, tm_codes, tm_act, tm_act3,
+                                         tm_scales, tm_act64, p);
+            } else if (pair_grid > 0) {
+                cfg.gridDim = dim3(pair_grid);
+                err = cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel, tm_codes, tm_act, tm_act32,
+                                         tm_scales, tm_act64, p);
+            } else {
+                cfg.gridDim = dim3(num_sms);
+                err = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<false, kMap>, tm_codes, tm_act, tm_act32,
+                                         tm_scales, tm_act64, p);
+            }
         }
-        if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+        if (err != cudaSuccess) return MOE_ERR_CUDA;
     }
     return MOE_OK;
 }
