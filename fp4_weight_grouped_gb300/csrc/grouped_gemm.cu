@@ -503,6 +503,10 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
         *abort_flag = 0;
         *bad_flag = 0;
     }
+    // The group sizes, staged in roff (which the scan below overwrites entry
+    // by entry, each after reading it): one load per thread, all in flight at
+    // once, instead of the scanning warp's dependent chunks of 32.
+    for (int e = tid; e < E; e += kThreads) roff[e] = p.group_sizes[e];
     __syncthreads();
     // Row offsets and work-item offsets: exclusive prefix sums over experts,
     // done by warp 0 in chunks of 32 (E <= 1024); also the widest work item.
@@ -514,7 +518,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
         int g_max = 0;
         for (int base = 0; base < E; base += 32) {
             const int e = base + lane;
-            const int gs = e < E ? p.group_sizes[e] : 0;
+            const int gs = e < E ? roff[e] : 0;
             if (gs < 0) *bad_flag = 1;
             if (gs >= p.band_lo && gs <= p.band_hi) g_max = max(g_max, gs);
         }
@@ -524,7 +528,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tm_codes, const CUt
         int nt_max = 0;
         for (int base = 0; base < E; base += 32) {
             const int e = base + lane;
-            const int gs = e < E ? p.group_sizes[e] : 0;
+            const int gs = e < E ? roff[e] : 0;
             const int g = gs > 0 ? gs : 0;
             const int gw = (g >= p.band_lo && g <= p.band_hi) ? g : 0;   // rows with work here
             const long long items = ((static_cast<long long>(gw) + chunk - 1) / chunk) * item_tiles;
