@@ -64,8 +64,8 @@ FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
 # DRAM bytes (read + write) per launch of the w13 GEMM kernel measured by ncu for
 # each workload, with the hash of the kernel source they were taken on.  A
 # changed kernel reports traffic = null until re-measured.
-NCU_TRAFFIC = {"layer_T8192": 4 * (671601408 + 44736000)}   # the 64-expert, 2048-token capture x 4
-NCU_KERNEL_HASH = "fe98b8886ae81974"
+NCU_TRAFFIC = {"layer_T8192": 4 * (671377920 + 44720640)}   # the 64-expert, 2048-token capture x 4
+NCU_KERNEL_HASH = "0cc5e171b6f17838"
 # The same for the scale cast kernel (a capture of the full cast_w13 launch; the
 # writes still in L2 when the kernel ends are not counted).
 NCU_CAST_TRAFFIC = 134278912 + 207835392
