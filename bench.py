@@ -50,11 +50,15 @@ WORKLOADS = {
                        "rows per expert) on 64 experts, T=2048 tokens (12288 rows); fits an ncu capture",
     "decode_E64_T16": "Profiling shape: the full layer path with decode-sized bands (T=16 tokens, "
                       "top-6 of 64 experts, 96 rows); fits an ncu capture",
+    "prefill_E96_T1024": "Profiling shape: the prefill band mix on 96 experts (Zipf(1.1), T=1024 "
+                         "tokens, 6144 rows; 38 of the 76 used experts at 32 rows or fewer, 5 over "
+                         "256); fits an ncu capture",
     "cast_w13": "Lossless MXFP4 -> NVFP4 scale cast of the w13 scales: E8M0 [256, 4096, 128] "
                 "(128 MiB) -> E4M3 [256, 4096, 256] + per-expert f32 scale + out-of-range count",
 }
 DEFAULT_STEPS = {"decode_T64": 2000, "decode_T256": 1000, "prefill_T4096": 300, "layer_T8192": 300,
-                 "layer_E64_T2048": 300, "decode_E64_T16": 1000, "cast_w13": 200}
+                 "layer_E64_T2048": 300, "decode_E64_T16": 1000, "prefill_E96_T1024": 300,
+                 "cast_w13": 200}
 CAST_METRIC = "lossless MXFP4 -> NVFP4 scale cast GB/s (algorithmic bytes), % of measured HBM, 1 GPU"
 CAST_SHAPE, CAST_BYTES = (256, 4096, 128), (117, 125)   # w13 scale tensor, exponents [-10, -2]
 

@@ -208,7 +208,9 @@ WORKLOAD_TOKENS = {"decode_T64": (64, "uniform", 256), "decode_T256": (256, "uni
                    # the layer's band shape (about 192 rows per expert) on 64 experts
                    "layer_E64_T2048": (2048, "logits", 64),
                    # decode-sized bands (one or two rows per expert) on 64 experts
-                   "decode_E64_T16": (16, "uniform", 64)}
+                   "decode_E64_T16": (16, "uniform", 64),
+                   # the prefill band mix (half the used experts at 32 rows or fewer) on 96 experts
+                   "prefill_E96_T1024": (1024, "zipf", 96)}
 
 
 def layer_weights(seed: int = 0, E: int = 256, hidden: int = 4096, inter: int = 2048):
