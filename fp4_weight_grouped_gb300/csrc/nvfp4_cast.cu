@@ -375,9 +375,17 @@ moe_status launch_mxfp4_to_nvfp4(const uint8_t *scales, int E, int N, int K, uin
     if (nvfp4_cast_one_pass(scales, e4m3, N, K)) {
         const int C = static_cast<int>((per_expert + kSlice - 1) / kSlice);
         const int smem = static_cast<int>(sizeof(OnePassSmem));
-        static const cudaError_t attr_ok =
-            cudaFuncSetAttribute(onepass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (attr_ok != cudaSuccess) return MOE_ERR_CUDA;
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+        // The shared-memory attribute, once per device (0..63; others every call).
+        static std::atomic<uint64_t> attr_dev_mask{0};
+        const uint64_t dev_bit = dev >= 0 && dev < 64 ? 1ull << dev : 0;
+        if (!(attr_dev_mask.load(std::memory_order_acquire) & dev_bit) || !dev_bit) {
+            if (cudaFuncSetAttribute(onepass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+                cudaSuccess)
+                return MOE_ERR_CUDA;
+            attr_dev_mask.fetch_or(dev_bit, std::memory_order_release);
+        }
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -391,14 +399,12 @@ moe_status launch_mxfp4_to_nvfp4(const uint8_t *scales, int E, int N, int K, uin
         cfg.stream = stream;
         // Resident clusters of this size, per device (queried once).
         static std::atomic<int> resident[64][kMaxCluster + 1];
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
-        int nc = dev < 64 ? resident[dev][C].load(std::memory_order_relaxed) : 0;
+        int nc = dev >= 0 && dev < 64 ? resident[dev][C].load(std::memory_order_relaxed) : 0;
         if (nc <= 0) {
             cfg.gridDim = dim3(static_cast<unsigned>(C * num_sms), 1, 1);
             if (cudaOccupancyMaxActiveClusters(&nc, onepass_kernel, &cfg) != cudaSuccess || nc <= 0)
                 return MOE_ERR_CUDA;
-            if (dev < 64) resident[dev][C].store(nc, std::memory_order_relaxed);
+            if (dev >= 0 && dev < 64) resident[dev][C].store(nc, std::memory_order_relaxed);
         }
         nc = min(nc, E);
         cfg.gridDim = dim3(static_cast<unsigned>(C * nc), 1, 1);
