@@ -72,8 +72,8 @@ NCU_TRAFFIC = {"layer_T8192": 4 * (671377920 + 44720640)}   # the 64-expert, 204
 NCU_KERNEL_HASH = "0cc5e171b6f17838"
 # The same for the scale cast kernel (a capture of the full cast_w13 launch; the
 # writes still in L2 when the kernel ends are not counted).
-NCU_CAST_TRAFFIC = 134278912 + 207835392
-NCU_CAST_HASH = "5b5274bcc8477fba"
+NCU_CAST_TRAFFIC = 134274048 + 206422016
+NCU_CAST_HASH = "335971da53e6986d"
 
 WEIGHT_BYTES_PER_ELEM = 17.0 / 32.0       # 4-bit code + one E8M0 byte per 32
 
