@@ -213,7 +213,10 @@ MOE_API moe_status moe_route_sort_noalloc(const int32_t *topk_ids, int32_t T, in
  *  workspace    device, >= 256 bytes (status word).
  * Each call enqueues two kernel launches: bands of 1..32 rows (streamed
  * weights, split accumulators) and bands of more rows (128- or 256-token
- * work items); a launch whose class has no band exits at once.
+ * work items); a launch whose class has no band exits at once.  The second
+ * is a programmatic dependent launch that may overlap the first (the two
+ * read the same inputs and write disjoint rows); work enqueued after the
+ * call still waits for both.
  * Every weight is decoded exactly to bf16.  With scale bytes >= 2 every
  * nonzero weight is a normal bf16 number, its products with bf16 activations
  * are exact in f32, and results differ from an exact sum only by f32
