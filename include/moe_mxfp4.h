@@ -215,8 +215,11 @@ MOE_API moe_status moe_route_sort_noalloc(const int32_t *topk_ids, int32_t T, in
  * weights, split accumulators) and bands of more rows (128- or 256-token
  * work items); a launch whose class has no band exits at once.  The second
  * is a programmatic dependent launch that may overlap the first (the two
- * read the same inputs and write disjoint rows); work enqueued after the
- * call still waits for both.
+ * read the same inputs and write disjoint rows).  Work enqueued after the
+ * call in the ordinary way waits for both.  A kernel enqueued right after it
+ * with programmatic stream serialization must not rely on griddepcontrol.wait
+ * (cudaGridDependencySynchronize) alone to see the rows of the first launch:
+ * that waits for the second launch only.
  * Every weight is decoded exactly to bf16.  With scale bytes >= 2 every
  * nonzero weight is a normal bf16 number, its products with bf16 activations
  * are exact in f32, and results differ from an exact sum only by f32
